@@ -1,0 +1,478 @@
+"""Benchmark of one paged-decode step on GB300.
+
+A step is one pass of the whole hot path over one batch: paged_kv_write of
+one new token per sequence, paged_attention_decode of every sequence, and
+copy_blocks of the copy-on-write pairs.  The default workload is the
+Qwen2.5-72B-shaped long-context decode (32 sequences x 32,768 tokens,
+64 query / 8 K/V heads, d = 128, bf16 KV, 512-token partitions): 4 GiB of K/V,
+far larger than L2, so every step streams it from HBM.
+
+Prints one JSON line (rank 0).  `value` is algorithmic bytes per step
+(query + K/V of the unique blocks read + output + block tables, plus the
+write and copy bytes) over the device-timed step, in GB/s, summed over ranks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--kernel auto|cuda_cores|tensor_cores] [--impl ours|reference]
+
+Under torchrun each rank runs its own replica of the workload (decode
+shards by sequence with no exchange, so N GPUs are N independent units).
+`--impl reference` times the CPU oracle instead, on a bounded sample of the
+same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s and % of HBM peak; seq-steps/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+ELEM = {W.DT_F32: 4, W.DT_BF16: 2, W.DT_E4M3: 1}
+
+
+# ------------------------------------------------------------- byte counts
+
+def decode_bytes(w: W.Workload, unique: bool = True) -> int:
+    """Algorithmic bytes of one decode: query read + output write + K/V of
+    every block read (shared blocks once when unique) + table entries read
+    + context lengths."""
+    bq = ELEM[w.q_dtype]
+    bkv = ELEM[w.cache_dtype]
+    qo = 2 * w.S * w.Hq * w.d * bq
+    nblk = -(-w.context_lens.astype(np.int64) // w.bs)
+    if unique and w.shared_seqs:
+        # K/V bytes of distinct physical blocks, counting only the tokens read
+        seen = {}
+        for s in range(w.S):
+            n = int(w.context_lens[s])
+            for j in range(int(nblk[s])):
+                b = int(w.block_tables[s, j])
+                seen[b] = max(seen.get(b, 0), min(w.bs, n - j * w.bs))
+        kv_tokens = sum(seen.values())
+    else:
+        kv_tokens = int(w.context_lens.astype(np.int64).sum())
+    kv = kv_tokens * w.Hkv * w.d * 2 * bkv
+    return qo + kv + int(nblk.sum()) * 4 + w.S * 4
+
+
+def write_bytes(w: W.Workload) -> int:
+    return w.S * w.Hkv * w.d * 2 * (ELEM[w.q_dtype] + ELEM[w.cache_dtype]) + w.S * 8
+
+
+def copy_bytes(w: W.Workload) -> int:
+    blk = w.bs * w.Hkv * w.d * ELEM[w.cache_dtype]
+    return len(w.cow_pairs) * (2 * 2 * blk + 16)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_uuid: str):
+        self.uuid = dev_uuid
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.uuid, "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self._t is not None:
+                self._t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------- CPU baseline
+
+def cpu_oracle_sample(w: W.Workload, budget_s: float, threads: int):
+    """Time the CPU oracle's decode on whole sequences of the workload, one
+    after another, until `budget_s` of CPU work is done.  Returns
+    (GB/s of decode bytes, seq-steps/s, sequences, seconds)."""
+    import oracle as O
+    O.build()
+    order = W.sample_sequences(w, w.S, seed_tag="cpu-sample")
+    done_bytes, done_seqs, spent = 0, 0, 0.0
+    odt = {W.DT_F32: O.F32, W.DT_BF16: O.BF16, W.DT_E4M3: O.E4M3}
+    for s in order:
+        sw = W.sub_workload(w, np.array([s]))
+        hv = W.host_values(sw)
+        q = W.bf16_bits(hv.query) if w.q_dtype == W.DT_BF16 else hv.query
+        if w.cache_dtype == W.DT_E4M3:
+            kc = np.zeros(hv.k_pool.shape, np.uint8)
+            vc = np.zeros_like(kc)
+            sl = np.arange(kc.shape[0] * w.bs, dtype=np.int64)
+            flat = lambda a: a.reshape(-1, w.Hkv, w.d)  # noqa: E731
+            O.paged_kv_write(flat(hv.k_pool), flat(hv.v_pool), O.F32, kc, vc, O.E4M3, sl, w.bs,
+                             hv.k_scale, hv.v_scale)
+        elif w.cache_dtype == W.DT_BF16:
+            kc, vc = W.bf16_bits(hv.k_pool), W.bf16_bits(hv.v_pool)
+        else:
+            kc, vc = hv.k_pool, hv.v_pool
+        t0 = time.perf_counter()
+        O.paged_attention_decode(q, odt[w.q_dtype], kc, vc, odt[w.cache_dtype], sw.block_tables,
+                                 sw.context_lens, w.scale, hv.k_scale, hv.v_scale, threads=threads)
+        spent += time.perf_counter() - t0
+        done_bytes += decode_bytes(sw, unique=False)
+        done_seqs += 1
+        if spent >= budget_s:
+            break
+    return done_bytes / spent / 1e9, done_seqs / spent, done_seqs, spent
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- helpers
+
+def peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_44_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.startswith("pkv_decode") or f.endswith(".cuh") or f.endswith(".h"):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str, kernel: str):
+    """DRAM bytes per decode launch from a committed ncu summary, if it was
+    taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f).get(f"{workload}/{kernel}")
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------- arms
+
+def run_reference(args, w: W.Workload):
+    ws, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    threads = cpu_threads()
+    per_step = []
+    total_bytes = 0
+    budget = max(0.5, min(10.0, 60.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup + args.steps):
+        gbs, sps, nseq, spent = cpu_oracle_sample(w, budget, threads)
+        if i >= args.warmup:
+            per_step.append((gbs, sps, nseq, spent))
+    gbs = statistics.median(p[0] for p in per_step)
+    sps = statistics.median(p[1] for p in per_step)
+    nseq = per_step[0][2]
+    ms = statistics.median(p[3] / p[2] for p in per_step) * w.S * 1e3   # time for a full step's sequences
+    sample = f"{nseq} whole sequences of the workload per step (decode only), {threads} threads"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "bs": w.bs,
+                   "cache_dtype": w.cache_dtype, "max_context_len": w.max_context_len},
+        "seq_steps_per_s": round(sps, 4),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w: W.Workload):
+    import torch
+    import paged_kv_cache_44_gb300 as pkv
+
+    ws, rank, local = dist_setup()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    # ---- inputs, resident in HBM before timing
+    tdt = {W.DT_F32: torch.float32, W.DT_BF16: torch.bfloat16, W.DT_E4M3: torch.uint8}
+    shape = (w.NB, w.bs, w.Hkv, w.d)
+    numel = int(np.prod(shape))
+    seed = w.seed + 7919 * rank
+    k_scale = v_scale = 1.0
+    caches = []
+    with torch.cuda.stream(stream):
+        for which in (1, 2):
+            if w.cache_dtype == W.DT_E4M3:
+                cache = torch.empty(shape, dtype=torch.uint8, device=dev)
+                sc = 0.0
+                for _, x in W.device_pool_chunks(seed, which, numel, dev):
+                    sc = max(sc, float(x.abs().max()))
+                scale = float(np.float32(sc) / np.float32(W.E4M3_MAX))
+                if which == 1:
+                    k_scale = scale
+                else:
+                    v_scale = scale
+                rows = w.Hkv * w.d
+                for c0, x in W.device_pool_chunks(seed, which, numel, dev):
+                    n = x.numel() // rows
+                    slots = torch.arange(c0 // rows, c0 // rows + n, device=dev, dtype=torch.int64)
+                    vals = x.view(n, w.Hkv, w.d)
+                    pkv.paged_kv_write(vals, vals, cache, cache, slots, scale, scale, stream=stream)
+            else:
+                cache = torch.empty(numel, dtype=tdt[w.cache_dtype], device=dev)
+                for c0, x in W.device_pool_chunks(seed, which, numel, dev):
+                    cache[c0:c0 + x.numel()] = W.device_bf16_from_draws(x) if w.cache_dtype == W.DT_BF16 else x
+                cache = cache.view(shape)
+            caches.append(cache)
+        kc, vc = caches
+
+        def dev_vals(tag, shp):
+            x = W.device_normal(seed, tag, int(np.prod(shp)), dev).view(shp)
+            return W.device_bf16_from_draws(x) if w.q_dtype == W.DT_BF16 else x
+
+        q = dev_vals(11, (w.S, w.Hq, w.d))
+        new_k = dev_vals(12, (w.S, w.Hkv, w.d))
+        new_v = dev_vals(13, (w.S, w.Hkv, w.d))
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    sm = torch.from_numpy(w.slot_mapping).to(dev)
+    cow = torch.from_numpy(w.cow_pairs.astype(np.int64)).to(dev)
+    out = torch.empty_like(q)
+    P = args.partition if args.partition is not None else w.partition_size
+    Pres = pkv.decode_partition_size(w.S, w.Hq, w.Hkv, w.d, w.bs, w.max_context_len, P)
+    wsp = pkv.make_workspace(w.S, w.Hq, w.Hkv, w.d, w.bs, w.max_context_len, P, device=dev)
+    mc = w.max_context_len
+    split = Pres > 0 and -(-mc // Pres) > 1
+    launches_per_step = 1 + (2 if split else 1) + (1 if len(w.cow_pairs) else 0)
+    torch.cuda.synchronize(dev)
+
+    def step(ev0=None, ev1=None, qq=q, nk=new_k, nv=new_v, btab=bt, clen=cl, slots=sm, pairs=cow, o=out):
+        pkv.paged_kv_write(nk, nv, kc, vc, slots, k_scale, v_scale, stream=stream)
+        if ev0 is not None:
+            ev0.record(stream)
+        pkv.paged_attention_decode(o, qq, kc, vc, btab, clen, mc, scale=w.scale, k_scale=k_scale,
+                                   v_scale=v_scale, partition_size=P, workspace=wsp, stream=stream,
+                                   kernel=args.kernel)
+        if ev1 is not None:
+            ev1.record(stream)
+        if len(w.cow_pairs):
+            pkv.copy_blocks([kc], [vc], pairs, stream=stream)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier(device_ids=[dev.index])
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: K steps, events on the launching stream
+    dec0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    dec1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(uuid) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            step(dec0[i], dec1[i])
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    ms_total = t0.elapsed_time(t1)
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(dec0, dec1))
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_total, dec_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total, dec_ms = float(tt[0]), float(tt[1])
+    ms_step = ms_total / args.steps
+
+    # ---- end to end: host buffers in, host result out, through the public API
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    h_in = {k: pin(v) for k, v in dict(q=q, nk=new_k, nv=new_v, bt=bt, cl=cl, sm=sm, cow=cow).items()}
+    d_in = {k: torch.empty_like(v, device=dev) for k, v in h_in.items()}
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    d2h = h_out.numel() * h_out.element_size()
+    e2e_steps = max(3, min(args.steps, 200))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for k in h_in:
+                d_in[k].copy_(h_in[k], non_blocking=True)
+        step(qq=d_in["q"], nk=d_in["nk"], nv=d_in["nv"], btab=d_in["bt"], clen=d_in["cl"], slots=d_in["sm"],
+             pairs=d_in["cow"])
+        with torch.cuda.stream(stream):
+            h_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    w0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = (time.perf_counter() - w0) / e2e_steps
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_s = float(tt[0])
+
+    # ---- numbers
+    dbytes = decode_bytes(w)
+    sbytes = dbytes + write_bytes(w) + copy_bytes(w)
+    value = ws * sbytes / (ms_step * 1e-3) / 1e9
+    achieved = dbytes / (dec_ms * 1e-3) / 1e9
+    peak, peak_kind = peak_hbm()
+    traffic = measured_traffic(w.name, args.kernel)
+    clocks = clk.summary()
+    kname = args.kernel
+    if kname == "auto":
+        kname = "tensor_cores" if (w.cache_dtype == W.DT_E4M3 or
+                                   (w.cache_dtype == W.DT_BF16 and w.q_dtype == W.DT_BF16)) else "cuda_cores"
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.cache_dtype == W.DT_BF16 else w.cache_dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "bs": w.bs,
+                   "cache_dtype": w.cache_dtype, "q_dtype": w.q_dtype, "max_context_len": mc,
+                   "partition_size": Pres, "decode_kernel": kname,
+                   "kv_bytes": int(w.context_lens.astype(np.int64).sum()) * w.Hkv * w.d * 2 * ELEM[w.cache_dtype],
+                   "l2": "inputs larger than L2" if dbytes > 2 * 129e6 else "not flushed: inputs near L2 size",
+                   "step": "paged_kv_write(1 token/seq) + paged_attention_decode + copy_blocks(%d pairs)"
+                           % len(w.cow_pairs)},
+        "seq_steps_per_s": round(ws * w.S / (ms_step * 1e-3), 1),
+        "decode_gbs": round(achieved, 2),
+        "hbm_frac_of_measured": round(achieved / peak, 4),
+        "hbm_frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "traffic": traffic, "kernel": "paged_attention_decode (" + kname + ")",
+                     "algorithmic_bytes_per_launch": dbytes, "launch_ms": round(dec_ms, 5)},
+        "e2e": {"value": round(ws * sbytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = cpu_threads()
+        gbs, sps, nseq, spent = cpu_oracle_sample(w, args.cpu_seconds, threads)
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{nseq} whole sequences of the workload (decode only, "
+                                          f"{spent:.1f} s of CPU time)",
+                                "seq_steps_per_s": round(sps, 4)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="qwen2.5-72b-long", choices=sorted(W.SHAPES))
+    ap.add_argument("--kernel", default="auto", choices=["auto", "cuda_cores", "tensor_cores"])
+    ap.add_argument("--partition", type=int, default=None)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = W.make(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

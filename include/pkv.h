@@ -1,0 +1,226 @@
+/*
+ * pkv -- paged KV-cache decode attention for GB300 (sm_103a).
+ *
+ * C ABI of libpkv.so.  Every pointer argument is a DEVICE pointer unless its
+ * comment says "host".  Every call is asynchronous on `stream`: it validates
+ * its arguments on the host, enqueues kernels, and returns without waiting
+ * for the GPU.  No call allocates memory or synchronises the host, so the
+ * calls can be recorded into a CUDA graph.  The caller owns every buffer,
+ * including the decode workspace.
+ *
+ * Layouts (all row-major, contiguous, 16-byte aligned base pointers):
+ *   new tokens  key / value        [T,  Hkv, d]
+ *   query / out                    [S,  Hq,  d]
+ *   caches      key / value_cache  [NB, bs,  Hkv, d]   (one layer)
+ *   block_tables                   int32 [S, MB]
+ *   context_lens                   int32 [S]
+ *   slot_mapping                   int64 [T]
+ *   block_mapping                  int64 [P, 2]  (src, dst)
+ * Sizes: Hq = query heads, Hkv = K/V heads (Hq % Hkv == 0; query head h
+ * reads K/V head h / (Hq / Hkv)), d = head dimension, bs = tokens per
+ * physical block, NB = physical blocks in the pool, MB = table entries per
+ * sequence.
+ *
+ * Error behaviour.  Problems visible on the host (null pointers, bad sizes,
+ * unsupported dtypes or shapes, a workspace that is too small) return a
+ * status other than PKV_OK before anything is enqueued.  Problems visible
+ * only on the device (a block id outside [0, NB), a context length above
+ * MB * bs, a slot outside [0, NB * bs), a copy pair out of range) never
+ * fault: the offending block, token or pair is skipped and, when `err_word`
+ * is not NULL, the first such problem's code (PKV_DEVERR_*) is stored there
+ * with an atomic compare-and-swap from 0.  A launch failure returns
+ * PKV_ERR_CUDA.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pkv_stream_t;   /* same handle as cudaStream_t; NULL = legacy stream */
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,
+    PKV_ERR_UNSUPPORTED = 2,
+    PKV_ERR_WORKSPACE = 3,
+    PKV_ERR_CUDA = 4
+} pkv_status;
+
+typedef enum {
+    PKV_F32 = 0,       /* IEEE binary32 */
+    PKV_BF16 = 1,      /* bfloat16 */
+    PKV_FP8_E4M3 = 2   /* OCP fp8 E4M3 ("fn": max 448, no infinities); value = code * scale */
+} pkv_dtype;
+
+/* Device-side error codes stored into *err_word. */
+enum {
+    PKV_DEVERR_NONE = 0,
+    PKV_DEVERR_BLOCK_ID = 1,      /* a block table entry outside [0, NB) */
+    PKV_DEVERR_CONTEXT_LEN = 2,   /* context_lens[s] < 0 or > MB * bs */
+    PKV_DEVERR_SLOT = 3,          /* slot_mapping[i] >= NB * bs */
+    PKV_DEVERR_COPY_PAIR = 4      /* a copy pair with an id outside [0, NB) */
+};
+
+/*
+ * paged_kv_write -- store each new token's K and V into its slot
+ * (vLLM's reshape_and_cache).
+ *
+ * Source: "LLM推論の基礎とvLLMの内部", section 4 "PagedAttentionとブロック
+ * 管理": the KV cache is cut into fixed-size blocks that are handed to a
+ * request one at a time as its tokens arrive, so each new token lands in one
+ * slot of one physical block; section 2 of the same page: an fp8 KV cache
+ * (--kv-cache-dtype fp8) stores one byte per element.
+ *
+ * For token i with s = slot_mapping[i]: s < 0 skips the token; otherwise
+ * key_cache[s / bs][s % bs][h][:] = convert(key[i][h][:]) for every K/V head
+ * h, and the same for value.  Conversions: f32->f32, bf16->bf16, bf16->f32
+ * exact; f32->bf16 round to nearest even; (f32|bf16)->E4M3 stores
+ * e4m3(float(x) / k_scale) (v_scale for V) with one IEEE fp32 divide,
+ * round-to-nearest-even and saturation to +-448.
+ * Supported: in_dtype in {F32, BF16}; cache_dtype in {F32, BF16, FP8_E4M3};
+ * d a multiple of 8, at most 512.  T == 0 is a no-op.  Duplicate slots in
+ * one call race (which token wins is unspecified).
+ */
+PKV_API pkv_status pkv_paged_kv_write(const void* key, const void* value, pkv_dtype in_dtype,
+                              void* key_cache, void* value_cache, pkv_dtype cache_dtype,
+                              const int64_t* slot_mapping, int T,
+                              int NB, int bs, int Hkv, int d,
+                              float k_scale, float v_scale,
+                              int32_t* err_word, pkv_stream_t stream);
+
+/*
+ * Bytes of workspace pkv_paged_attention_decode needs for these sizes and
+ * this partition request (see below); 0 for invalid arguments.  The
+ * workspace holds a 256-byte scheduling header and, when a sequence may span
+ * several partitions, one (max, sum, weighted sum) triple per (sequence,
+ * query head, partition).  The header must be zero before a workspace is
+ * first used (every decode leaves it zero when it completes, so zero-filling
+ * once at allocation is enough).  One workspace must not be used by two
+ * decodes that may run at the same time.
+ */
+PKV_API size_t pkv_decode_workspace_size(int S, int Hq, int Hkv, int d, int bs,
+                                 int max_context_len, int partition_size);
+
+/*
+ * Partition size (tokens) that a decode with these arguments will use:
+ * the request itself when it is > 0, no split (returns 0) when it is -1,
+ * and the library's choice when it is 0.  Returns -1 for invalid arguments.
+ */
+PKV_API int pkv_decode_partition_size(int S, int Hq, int Hkv, int d, int bs,
+                              int max_context_len, int partition_size);
+
+/*
+ * paged_attention_decode -- one query token per sequence attends to every
+ * cached token of that sequence, read through its block table.
+ *
+ * Source: "LLM推論の基礎とvLLMの内部", section 4: each request keeps a table
+ * from logical blocks to physical blocks and the attention kernel reads K/V
+ * through it; section 12 of the same page: PagedAttention changes where K/V
+ * live, not what attention computes; section 2: GQA lets several query
+ * heads share one K/V head.  "vLLM 内部構造 (2) — PagedAttention", section
+ * "ブロックテーブル": logically contiguous, physically scattered blocks.
+ *
+ * For sequence s with n = context_lens[s] and query head h (K/V head
+ * kvh = h / (Hq / Hkv)):
+ *   k_t, v_t = key/value_cache[block_tables[s][t / bs]][t % bs][kvh], t < n
+ *   x_t = scale * <query[s][h], k_t>,  p = softmax(x),  out[s][h] = sum p_t v_t
+ * (for E4M3 caches k_t and v_t are code * k_scale and code * v_scale).  A
+ * sequence with n == 0 gets zeros.  Arithmetic is fp32 with fp32
+ * accumulation; out has the dtype of query.
+ *
+ * Long contexts are split into partitions of `partition_size` tokens
+ * (a multiple of bs): each partition keeps its own running max and sum, and
+ * a second pass merges them (M = max m_p, L = sum e^(m_p - M) l_p,
+ * O = sum e^(m_p - M) acc_p / L).  partition_size: 0 = library choice,
+ * -1 = never split, > 0 = that size.  When any sequence may span more than
+ * one partition, `workspace` must hold pkv_decode_workspace_size(...) bytes,
+ * else PKV_ERR_WORKSPACE is returned.
+ *
+ * max_context_len (host) must be >= every context_lens[s] and <= MB * bs; it
+ * sizes the launch without reading device memory.  Supported: q_dtype in
+ * {F32, BF16}; cache_dtype in {F32, BF16, FP8_E4M3}; d in {64, 128};
+ * bs in {16, 32}; any group size Hq / Hkv >= 1 (a K/V head's query heads
+ * are processed up to 8 at a time, each such set reading the head's K/V).
+ * For E4M3 caches the query is rounded to fp16 for the tensor-core
+ * products, so |query| must stay below 65504.
+ */
+PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* query, pkv_dtype q_dtype,
+                                      const void* key_cache, const void* value_cache,
+                                      pkv_dtype cache_dtype,
+                                      const int32_t* block_tables, int MB,
+                                      const int32_t* context_lens, int S, int max_context_len,
+                                      int Hq, int Hkv, int d, int bs, int NB,
+                                      float scale, float k_scale, float v_scale,
+                                      int partition_size,
+                                      void* workspace, size_t workspace_bytes,
+                                      int32_t* err_word, pkv_stream_t stream);
+
+/* Kernel choice for pkv_paged_attention_decode_ex. */
+typedef enum {
+    PKV_DECODE_AUTO = 0,          /* tensor cores where supported, else CUDA cores */
+    PKV_DECODE_CUDA_CORES = 1,    /* the CUDA-core kernel (every dtype) */
+    PKV_DECODE_TENSOR_CORES = 2   /* the tensor-core kernel; PKV_ERR_UNSUPPORTED where it does not apply
+                                     (it needs a bf16 query with a bf16 cache, or an E4M3 cache) */
+} pkv_decode_kernel;
+
+/*
+ * Same as pkv_paged_attention_decode, with an explicit kernel choice
+ * (`kernel` is a pkv_decode_kernel).  Both kernels compute the same
+ * function; the choice exists so the two can be measured against each
+ * other.
+ */
+PKV_API pkv_status pkv_paged_attention_decode_ex(void* out, const void* query, pkv_dtype q_dtype,
+                                         const void* key_cache, const void* value_cache,
+                                         pkv_dtype cache_dtype,
+                                         const int32_t* block_tables, int MB,
+                                         const int32_t* context_lens, int S, int max_context_len,
+                                         int Hq, int Hkv, int d, int bs, int NB,
+                                         float scale, float k_scale, float v_scale,
+                                         int partition_size,
+                                         void* workspace, size_t workspace_bytes,
+                                         int32_t* err_word, pkv_stream_t stream, int kernel);
+
+/*
+ * copy_blocks -- copy-on-write duplication of physical blocks.
+ *
+ * Source: "LLM推論の基礎とvLLMの内部", section 4: blocks of a shared prefix
+ * carry a reference count and are copied when written (copy-on-write);
+ * "vLLM 内部構造 (2) — PagedAttention", section "共有": many requests with
+ * the same system prompt point at one set of physical blocks.
+ *
+ * For every layer l < num_layers and pair p < P with
+ * (src, dst) = block_mapping[p]: block dst of key_caches[l] and of
+ * value_caches[l] becomes a byte copy of block src (block_bytes bytes each,
+ * = bs * Hkv * d * element size).  key_caches / value_caches are HOST arrays
+ * of num_layers device pointers (at most 256 layers); the call copies them
+ * into the launch, so the arrays may be freed when it returns.  The
+ * destinations must be distinct and must not be sources (the host that
+ * decides copy-on-write guarantees this; it is not checked).  block_bytes
+ * must be a multiple of 16.
+ */
+PKV_API pkv_status pkv_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
+                           const int64_t* block_mapping, int P, int NB, size_t block_bytes,
+                           int32_t* err_word, pkv_stream_t stream);
+
+/* Static, human-readable text for a status. */
+PKV_API const char* pkv_status_string(pkv_status status);
+
+/* Version of this library, e.g. "pkv 0.1.0 sm_103a". */
+PKV_API const char* pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

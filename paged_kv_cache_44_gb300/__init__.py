@@ -1,0 +1,192 @@
+"""Paged KV-cache decode attention for GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over ``libpkv.so`` (declared in ``include/pkv.h``).  It
+only marshals arguments: torch tensors become device pointers and sizes, the
+current torch stream becomes the launch stream, and a non-zero status
+becomes a :class:`PkvError`.  Every step of the computation runs in the
+library's CUDA kernels; there is no other implementation to fall back on.
+
+The three calls (vLLM-style PagedAttention, "LLM推論の基礎とvLLMの内部",
+section 4):
+
+* :func:`paged_kv_write` -- store each new token's K/V into its slot;
+* :func:`paged_attention_decode` -- one query token per sequence against the
+  paged K/V pool, through block tables;
+* :func:`copy_blocks` -- copy-on-write duplication of shared blocks.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpkv.so")
+
+F32, BF16, FP8_E4M3 = 0, 1, 2
+KERNELS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported dtype or shape",
+          3: "workspace missing or too small", 4: "CUDA launch failed"}
+
+EXPORTED = ("pkv_paged_kv_write", "pkv_decode_workspace_size", "pkv_decode_partition_size",
+            "pkv_paged_attention_decode", "pkv_paged_attention_decode_ex", "pkv_copy_blocks",
+            "pkv_status_string", "pkv_version")
+
+
+class PkvError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        super().__init__(f"{call} failed: {STATUS.get(status, status)} (status {status})")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built. Build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc for sm_103a).")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.pkv_paged_kv_write.argtypes = [vp, vp, i32, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, f32, vp, vp]
+    lib.pkv_paged_kv_write.restype = i32
+    lib.pkv_decode_workspace_size.argtypes = [i32] * 7
+    lib.pkv_decode_workspace_size.restype = sz
+    lib.pkv_decode_partition_size.argtypes = [i32] * 7
+    lib.pkv_decode_partition_size.restype = i32
+    dec = [vp, vp, i32, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, f32, f32, f32, i32,
+           vp, sz, vp, vp]
+    lib.pkv_paged_attention_decode.argtypes = dec
+    lib.pkv_paged_attention_decode.restype = i32
+    lib.pkv_paged_attention_decode_ex.argtypes = dec + [i32]
+    lib.pkv_paged_attention_decode_ex.restype = i32
+    lib.pkv_copy_blocks.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32, vp, i32, i32, sz, vp, vp]
+    lib.pkv_copy_blocks.restype = i32
+    lib.pkv_status_string.argtypes = [i32]
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    lib.pkv_version.argtypes = []
+    lib.pkv_version.restype = ctypes.c_char_p
+    return lib
+
+
+lib = _load()
+
+
+def version() -> str:
+    return lib.pkv_version().decode()
+
+
+def dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return F32
+    if t == torch.bfloat16:
+        return BF16
+    if t in (torch.float8_e4m3fn, torch.uint8):
+        return FP8_E4M3
+    raise TypeError(f"unsupported dtype {t}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("pkv calls take CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("pkv calls take contiguous tensors")
+    return t.data_ptr()
+
+
+def _check(call: str, st: int) -> None:
+    if st != 0:
+        raise PkvError(call, st)
+
+
+def paged_kv_write(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                   slot_mapping: torch.Tensor, k_scale: float = 1.0, v_scale: float = 1.0,
+                   err_word: Optional[torch.Tensor] = None, stream=None) -> None:
+    """key/value [T, Hkv, d] (fp32|bf16); caches [NB, bs, Hkv, d] (fp32|bf16|e4m3);
+    slot_mapping int64 [T] (negative = skip)."""
+    T, Hkv, d = key.shape
+    NB, bs = key_cache.shape[0], key_cache.shape[1]
+    if tuple(key_cache.shape[2:]) != (Hkv, d) or value.shape != key.shape or value_cache.shape != key_cache.shape:
+        raise ValueError("shape mismatch between tokens and caches")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != T:
+        raise ValueError("slot_mapping must be int64 [T]")
+    _check("paged_kv_write", lib.pkv_paged_kv_write(
+        _ptr(key), _ptr(value), dtype_code(key.dtype), _ptr(key_cache), _ptr(value_cache),
+        dtype_code(key_cache.dtype), _ptr(slot_mapping), T, NB, bs, Hkv, d, float(k_scale), float(v_scale),
+        _ptr(err_word), _stream(stream)))
+
+
+def decode_partition_size(S: int, Hq: int, Hkv: int, d: int, bs: int, max_context_len: int,
+                          partition_size: int = 0) -> int:
+    return int(lib.pkv_decode_partition_size(S, Hq, Hkv, d, bs, max_context_len, partition_size))
+
+
+def decode_workspace_size(S: int, Hq: int, Hkv: int, d: int, bs: int, max_context_len: int,
+                          partition_size: int = 0) -> int:
+    return int(lib.pkv_decode_workspace_size(S, Hq, Hkv, d, bs, max_context_len, partition_size))
+
+
+def make_workspace(S: int, Hq: int, Hkv: int, d: int, bs: int, max_context_len: int, partition_size: int = 0,
+                   device=None) -> torch.Tensor:
+    """A zero-filled workspace of the size the decode needs (the decode
+    leaves its header zero, so the tensor can be reused call after call)."""
+    n = decode_workspace_size(S, Hq, Hkv, d, bs, max_context_len, partition_size)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                           value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                           max_context_len: int, scale: Optional[float] = None, k_scale: float = 1.0,
+                           v_scale: float = 1.0, partition_size: int = 0,
+                           workspace: Optional[torch.Tensor] = None, err_word: Optional[torch.Tensor] = None,
+                           stream=None, kernel: str = "auto") -> torch.Tensor:
+    """out/query [S, Hq, d]; caches [NB, bs, Hkv, d]; block_tables int32 [S, MB];
+    context_lens int32 [S]; max_context_len (host) >= every context length."""
+    S, Hq, d = query.shape
+    NB, bs, Hkv, d2 = key_cache.shape
+    if d2 != d or out.shape != query.shape or out.dtype != query.dtype or value_cache.shape != key_cache.shape:
+        raise ValueError("shape or dtype mismatch")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 or block_tables.dim() != 2:
+        raise ValueError("block_tables and context_lens must be int32")
+    MB = block_tables.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
+    _check("paged_attention_decode", lib.pkv_paged_attention_decode_ex(
+        _ptr(out), _ptr(query), dtype_code(query.dtype), _ptr(key_cache), _ptr(value_cache),
+        dtype_code(key_cache.dtype), _ptr(block_tables), MB, _ptr(context_lens), S, int(max_context_len),
+        Hq, Hkv, d, bs, NB, float(scale), float(k_scale), float(v_scale), int(partition_size),
+        ws_ptr, ws_bytes, _ptr(err_word), _stream(stream), KERNELS[kernel]))
+    return out
+
+
+def copy_blocks(key_caches: Sequence[torch.Tensor], value_caches: Sequence[torch.Tensor],
+                block_mapping: torch.Tensor, err_word: Optional[torch.Tensor] = None, stream=None) -> None:
+    """For every layer: block dst of each cache becomes a copy of block src,
+    for every (src, dst) row of block_mapping (int64 [P, 2])."""
+    L = len(key_caches)
+    if len(value_caches) != L or L == 0:
+        raise ValueError("need the same, non-zero number of key and value caches")
+    NB = key_caches[0].shape[0]
+    block_bytes = key_caches[0][0].numel() * key_caches[0].element_size()
+    for t in list(key_caches) + list(value_caches):
+        if t.shape != key_caches[0].shape or t.dtype != key_caches[0].dtype:
+            raise ValueError("all caches must share shape and dtype")
+    if block_mapping.dtype != torch.int64:
+        raise ValueError("block_mapping must be int64 [P, 2]")
+    P = block_mapping.numel() // 2
+    kp = (ctypes.c_void_p * L)(*[_ptr(t) for t in key_caches])
+    vp = (ctypes.c_void_p * L)(*[_ptr(t) for t in value_caches])
+    _check("copy_blocks", lib.pkv_copy_blocks(kp, vp, L, _ptr(block_mapping), P, NB, block_bytes,
+                                              _ptr(err_word), _stream(stream)))

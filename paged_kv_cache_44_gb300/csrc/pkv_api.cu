@@ -1,0 +1,223 @@
+// C ABI of libpkv.so: host-side validation, workspace planning, dispatch.
+// Nothing here allocates, synchronises or reads device memory.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+// Units of work (sequence x K/V head x head-set x partition) the default
+// partition size aims for: about four per warp of a full GB300 (152 SMs x
+// 4 consumer warps), so that dynamic scheduling evens out ragged lengths.
+constexpr long long kTargetUnits = 152LL * 4 * 4;
+constexpr int kMinDefaultPartition = 256;
+constexpr int kHeadSet = 8;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool finite_pos(float x) { return isfinite(x) && x > 0.f; }
+
+bool decode_shape_ok(int S, int Hq, int Hkv, int d, int bs, int max_ctx) {
+    return S >= 0 && S <= 65535 && Hkv >= 1 && Hq >= Hkv && Hq % Hkv == 0 && (d == 64 || d == 128) &&
+           (bs == 16 || bs == 32) && max_ctx >= 0;
+}
+
+// Partition size in tokens (0 = no split) for a request; -1 if invalid.
+int resolve_partition(int S, int Hq, int Hkv, int d, int bs, int max_ctx, int req) {
+    if (!decode_shape_ok(S, Hq, Hkv, d, bs, max_ctx)) return -1;
+    if (req > 0) return req % bs == 0 ? req : -1;
+    if (req == -1) return 0;
+    if (req != 0) return -1;
+    const long long sets = (long long)S * Hkv * ((Hq / Hkv + kHeadSet - 1) / kHeadSet);
+    if (sets == 0 || max_ctx <= kMinDefaultPartition) return 0;
+    int P = 1 << 20;
+    while (P > kMinDefaultPartition && sets * ((max_ctx + P - 1) / P) < kTargetUnits) P >>= 1;
+    if (P >= max_ctx) return 0;
+    return P;
+}
+
+DecodePlan make_plan(int S, int Hq, int d, int max_ctx, int P) {
+    DecodePlan pl{};
+    pl.P = P;
+    pl.Pmax = P > 0 ? (max_ctx > 0 ? (max_ctx + P - 1) / P : 1) : 1;
+    pl.split = P > 0 && pl.Pmax > 1;
+    pl.bytes = kWorkspaceHeaderBytes;
+    if (!pl.split) return pl;
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t units = (size_t)S * Hq * pl.Pmax;
+    pl.ml_offset = kWorkspaceHeaderBytes;
+    pl.acc_offset = up(pl.ml_offset + units * 2 * sizeof(float));
+    pl.bytes = up(pl.acc_offset + units * d * sizeof(float));
+    return pl;
+}
+
+pkv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+int num_sms_current() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    std::lock_guard<std::mutex> g(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status st) {
+    switch (st) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID_ARG: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported dtype or shape";
+        case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+        case PKV_ERR_CUDA: return "CUDA launch failed";
+    }
+    return "unknown status";
+}
+
+const char* pkv_version(void) { return "pkv 0.1.0 sm_103a"; }
+
+pkv_status pkv_paged_kv_write(const void* key, const void* value, pkv_dtype in_dtype, void* key_cache,
+                              void* value_cache, pkv_dtype cache_dtype, const int64_t* slot_mapping, int T,
+                              int NB, int bs, int Hkv, int d, float k_scale, float v_scale, int32_t* err_word,
+                              pkv_stream_t stream) {
+    if (T < 0 || NB < 1 || bs < 1 || Hkv < 1 || d < 8) return PKV_ERR_INVALID_ARG;
+    if (in_dtype != PKV_F32 && in_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (cache_dtype != PKV_F32 && cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3)
+        return PKV_ERR_UNSUPPORTED;
+    if (d % 8 != 0 || d > 512) return PKV_ERR_UNSUPPORTED;
+    if (cache_dtype == PKV_FP8_E4M3 && (!finite_pos(k_scale) || !finite_pos(v_scale))) return PKV_ERR_INVALID_ARG;
+    if ((long long)NB * bs > (1LL << 40)) return PKV_ERR_INVALID_ARG;
+    if (T == 0) return PKV_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PKV_ERR_INVALID_ARG;
+    WriteParams p{};
+    p.key = key; p.value = value; p.key_cache = key_cache; p.value_cache = value_cache;
+    p.slot_mapping = slot_mapping; p.err = err_word;
+    p.T = T; p.NB = NB; p.bs = bs; p.Hkv = Hkv; p.d = d; p.k_scale = k_scale; p.v_scale = v_scale;
+    return from_cuda(launch_write(p, in_dtype, cache_dtype, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int pkv_decode_partition_size(int S, int Hq, int Hkv, int d, int bs, int max_context_len, int partition_size) {
+    return resolve_partition(S, Hq, Hkv, d, bs, max_context_len, partition_size);
+}
+
+size_t pkv_decode_workspace_size(int S, int Hq, int Hkv, int d, int bs, int max_context_len, int partition_size) {
+    const int P = resolve_partition(S, Hq, Hkv, d, bs, max_context_len, partition_size);
+    if (P < 0) return 0;
+    return make_plan(S, Hq, d, max_context_len, P).bytes;
+}
+
+pkv_status pkv_paged_attention_decode_ex(void* out, const void* query, pkv_dtype q_dtype, const void* key_cache,
+                                         const void* value_cache, pkv_dtype cache_dtype,
+                                         const int32_t* block_tables, int MB, const int32_t* context_lens, int S,
+                                         int max_context_len, int Hq, int Hkv, int d, int bs, int NB, float scale,
+                                         float k_scale, float v_scale, int partition_size, void* workspace,
+                                         size_t workspace_bytes, int32_t* err_word, pkv_stream_t stream,
+                                         int kernel) {
+    if (S < 0 || MB < 1 || NB < 1 || Hkv < 1 || Hq < 1 || max_context_len < 0) return PKV_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return PKV_ERR_INVALID_ARG;
+    if (q_dtype != PKV_F32 && q_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (cache_dtype != PKV_F32 && cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3)
+        return PKV_ERR_UNSUPPORTED;
+    if (!(d == 64 || d == 128) || !(bs == 16 || bs == 32)) return PKV_ERR_UNSUPPORTED;
+    if (S > 65535) return PKV_ERR_UNSUPPORTED;
+    if ((long long)max_context_len > (long long)MB * bs) return PKV_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    if (cache_dtype == PKV_FP8_E4M3 && (!finite_pos(k_scale) || !finite_pos(v_scale))) return PKV_ERR_INVALID_ARG;
+    if (partition_size < -1 || (partition_size > 0 && partition_size % bs != 0)) return PKV_ERR_INVALID_ARG;
+    if (kernel < 0 || kernel > 2) return PKV_ERR_INVALID_ARG;
+    if (S == 0) return PKV_OK;
+    if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+        return PKV_ERR_INVALID_ARG;
+
+    const int P = resolve_partition(S, Hq, Hkv, d, bs, max_context_len, partition_size);
+    if (P < 0) return PKV_ERR_INVALID_ARG;
+    const bool tc_ok = decode_tc_supports(q_dtype, cache_dtype, d, bs);
+    bool use_tc;
+    if (kernel == PKV_DECODE_AUTO) use_tc = tc_ok;
+    else if (kernel == PKV_DECODE_TENSOR_CORES) { if (!tc_ok) return PKV_ERR_UNSUPPORTED; use_tc = true; }
+    else use_tc = false;
+    const DecodePlan pl = make_plan(S, Hq, d, max_context_len, P);
+    if (pl.split) {
+        if (!workspace || workspace_bytes < pl.bytes) return PKV_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return PKV_ERR_INVALID_ARG;
+    }
+
+    DecodeParams p{};
+    p.out = out; p.q = query; p.kc = key_cache; p.vc = value_cache;
+    p.block_tables = block_tables; p.context_lens = context_lens; p.err = err_word;
+    p.S = S; p.MB = MB; p.Hq = Hq; p.Hkv = Hkv; p.g = Hq / Hkv; p.d = d; p.bs = bs; p.NB = NB;
+    p.P = pl.P > 0 ? pl.P : MB * bs;      // no split: one partition covers the whole table
+    p.Pmax = pl.Pmax;
+    p.max_ctx = max_context_len;
+    const float ks = cache_dtype == PKV_FP8_E4M3 ? k_scale : 1.f;
+    p.logit_scale_log2 = scale * ks * kLog2e;
+    p.out_scale = cache_dtype == PKV_FP8_E4M3 ? v_scale : 1.f;
+    if (pl.split) {
+        char* ws = static_cast<char*>(workspace);
+        p.sched = reinterpret_cast<unsigned*>(ws);
+        p.part_ml = reinterpret_cast<float*>(ws + pl.ml_offset);
+        p.part_acc = reinterpret_cast<float*>(ws + pl.acc_offset);
+    } else if (workspace && workspace_bytes >= kWorkspaceHeaderBytes && aligned16(workspace)) {
+        p.sched = reinterpret_cast<unsigned*>(workspace);
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = use_tc ? launch_decode_tc(p, q_dtype, cache_dtype, num_sms_current(), st)
+                           : launch_decode_simt(p, q_dtype, cache_dtype, st);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    if (pl.split) e = launch_decode_reduce(p, q_dtype, st);
+    return from_cuda(e);
+}
+
+pkv_status pkv_paged_attention_decode(void* out, const void* query, pkv_dtype q_dtype, const void* key_cache,
+                                      const void* value_cache, pkv_dtype cache_dtype, const int32_t* block_tables,
+                                      int MB, const int32_t* context_lens, int S, int max_context_len, int Hq,
+                                      int Hkv, int d, int bs, int NB, float scale, float k_scale, float v_scale,
+                                      int partition_size, void* workspace, size_t workspace_bytes,
+                                      int32_t* err_word, pkv_stream_t stream) {
+    return pkv_paged_attention_decode_ex(out, query, q_dtype, key_cache, value_cache, cache_dtype, block_tables, MB,
+                                         context_lens, S, max_context_len, Hq, Hkv, d, bs, NB, scale, k_scale,
+                                         v_scale, partition_size, workspace, workspace_bytes, err_word, stream,
+                                         PKV_DECODE_AUTO);
+}
+
+pkv_status pkv_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
+                           const int64_t* block_mapping, int P, int NB, size_t block_bytes, int32_t* err_word,
+                           pkv_stream_t stream) {
+    if (num_layers < 0 || num_layers > kMaxCopyLayers || P < 0 || NB < 1) return PKV_ERR_INVALID_ARG;
+    if (block_bytes == 0 || block_bytes % 16 != 0) return PKV_ERR_INVALID_ARG;
+    if (P == 0 || num_layers == 0) return PKV_OK;
+    if (!key_caches || !value_caches || !block_mapping) return PKV_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(block_mapping) & 7u) return PKV_ERR_INVALID_ARG;
+    CopyParams p{};
+    for (int l = 0; l < num_layers; ++l) {
+        if (!key_caches[l] || !value_caches[l] || !aligned16(key_caches[l]) || !aligned16(value_caches[l]))
+            return PKV_ERR_INVALID_ARG;
+        p.k[l] = key_caches[l];
+        p.v[l] = value_caches[l];
+    }
+    p.mapping = block_mapping; p.err = err_word; p.P = P; p.NB = NB; p.L = num_layers;
+    p.block_bytes = block_bytes;
+    return from_cuda(launch_copy(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// Internal launch interface between the C ABI (pkv_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+constexpr int kMaxCopyLayers = 256;
+constexpr size_t kWorkspaceHeaderBytes = 256;   // scheduler counters, zero between calls
+
+struct WriteParams {
+    const void* key;
+    const void* value;
+    void* key_cache;
+    void* value_cache;
+    const int64_t* slot_mapping;
+    int32_t* err;
+    int T, NB, bs, Hkv, d;
+    float k_scale, v_scale;
+};
+cudaError_t launch_write(const WriteParams& p, pkv_dtype in_dt, pkv_dtype cache_dt, cudaStream_t st);
+
+struct CopyParams {
+    const int64_t* mapping;
+    int32_t* err;
+    int P, NB, L;
+    unsigned long long block_bytes;
+    void* k[kMaxCopyLayers];
+    void* v[kMaxCopyLayers];
+};
+cudaError_t launch_copy(const CopyParams& p, cudaStream_t st);
+
+struct DecodeParams {
+    void* out;
+    const void* q;
+    const void* kc;
+    const void* vc;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    float* part_ml;       // [S][Hq][Pmax][2]: running max (log2 units) and sum
+    float* part_acc;      // [S][Hq][Pmax][d]: un-normalised weighted sums of V
+    unsigned* sched;      // scheduling counters in the workspace header (or null)
+    int32_t* err;
+    int S, MB, Hq, Hkv, g, d, bs, NB;
+    int P;                // tokens per partition (> 0)
+    int Pmax;             // partitions of the longest sequence
+    int max_ctx;
+    float logit_scale_log2;   // scale * k_scale * log2(e)
+    float out_scale;          // v_scale for E4M3 caches, else 1
+};
+
+// Resolved layout of the decode workspace.
+struct DecodePlan {
+    int P;            // tokens per partition; 0 = one partition per sequence
+    int Pmax;
+    bool split;       // a reduce pass is needed
+    size_t ml_offset, acc_offset, bytes;
+};
+
+enum class DecodeKernel { Simt = 0, TensorCore = 1 };
+
+cudaError_t launch_decode_simt(const DecodeParams& p, pkv_dtype q_dt, pkv_dtype c_dt, cudaStream_t st);
+cudaError_t launch_decode_tc(const DecodeParams& p, pkv_dtype q_dt, pkv_dtype c_dt, int num_sms,
+                             cudaStream_t st);
+cudaError_t launch_decode_reduce(const DecodeParams& p, pkv_dtype q_dt, cudaStream_t st);
+bool decode_tc_supports(pkv_dtype q_dt, pkv_dtype c_dt, int d, int bs);
+
+}  // namespace pkv

@@ -1,0 +1,123 @@
+"""The C-ABI library loads, exports every symbol include/*.h declares, and
+rejects bad arguments on the host before anything is launched.  No compute
+call is made here (these run without a GPU): every call below fails
+validation, so no kernel is ever reached."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_cache_44_gb300 import _build
+    _build.build()
+    import paged_kv_cache_44_gb300 as P
+    return P
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        txt = open(h, encoding="utf-8").read()
+        names |= set(re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", txt))
+    return names
+
+
+def test_every_declared_symbol_is_exported(pkv):
+    declared = _declared()
+    assert {"pkv_paged_kv_write", "pkv_paged_attention_decode", "pkv_copy_blocks"} <= declared
+    out = subprocess.run(["nm", "-D", "--defined-only", pkv.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\sT\s(pkv_\w+)", out))
+    assert declared <= exported, declared - exported
+    for n in declared:
+        assert hasattr(pkv.lib, n)
+    assert set(pkv.EXPORTED) == declared
+
+
+def test_status_strings_and_version(pkv):
+    for code, text in pkv.STATUS.items():
+        assert pkv.lib.pkv_status_string(code).decode() == text
+    assert pkv.version().endswith("sm_103a")
+
+
+def test_workspace_plan(pkv):
+    # 72B-shaped: 32 seqs x 64 heads x 64 partitions x (128 + 2) floats + header
+    n = pkv.decode_workspace_size(32, 64, 8, 128, 16, 32768, 512)
+    units = 32 * 64 * 64
+    assert n >= 256 + units * 130 * 4
+    assert n < 256 + units * 130 * 4 + 1024
+    # no split -> header only
+    assert pkv.decode_workspace_size(4, 4, 2, 64, 16, 38, -1) == 256
+    assert pkv.decode_partition_size(4, 4, 2, 64, 16, 38, -1) == 0
+    assert pkv.decode_partition_size(4, 4, 2, 64, 16, 38, 32) == 32
+    assert pkv.decode_partition_size(4, 4, 2, 64, 16, 38, 24) == -1       # not a multiple of bs
+    assert pkv.decode_partition_size(4, 4, 2, 96, 16, 38, 0) == -1        # unsupported d
+    P = pkv.decode_partition_size(64, 12, 2, 128, 16, 4096, 0)
+    assert P > 0 and P % 16 == 0
+
+
+FAKE = 0x10000   # aligned, never dereferenced: every call below fails validation first
+
+
+def _decode(pkv, **kw):
+    a = dict(out=FAKE, q=FAKE, qdt=1, k=FAKE, v=FAKE, cdt=1, bt=FAKE, MB=4, cl=FAKE, S=2, maxctx=64, Hq=8, Hkv=2,
+             d=128, bs=16, NB=10, scale=0.088, ks=1.0, vs=1.0, P=32, ws=None, wsb=0, err=None, stream=None,
+             kernel=0)
+    a.update(kw)
+    return pkv.lib.pkv_paged_attention_decode_ex(
+        a["out"], a["q"], a["qdt"], a["k"], a["v"], a["cdt"], a["bt"], a["MB"], a["cl"], a["S"], a["maxctx"],
+        a["Hq"], a["Hkv"], a["d"], a["bs"], a["NB"], a["scale"], a["ks"], a["vs"], a["P"], a["ws"], a["wsb"],
+        a["err"], a["stream"], a["kernel"])
+
+
+def test_decode_host_validation(pkv):
+    assert _decode(pkv, Hq=7) == 1                 # Hq % Hkv != 0
+    assert _decode(pkv, d=96) == 2                 # unsupported head dim
+    assert _decode(pkv, bs=8) == 2                 # unsupported block size
+    assert _decode(pkv, qdt=2) == 2                # fp8 query
+    assert _decode(pkv, cdt=7) == 2
+    assert _decode(pkv, out=None) == 1             # null pointer
+    assert _decode(pkv, q=FAKE + 4) == 1           # misaligned
+    assert _decode(pkv, maxctx=65) == 1            # exceeds MB * bs
+    assert _decode(pkv, P=24) == 1                 # partition not a multiple of bs
+    assert _decode(pkv, scale=float("nan")) == 1
+    assert _decode(pkv, cdt=2, ks=0.0) == 1        # fp8 needs positive scales
+    assert _decode(pkv, S=70000) == 2
+    assert _decode(pkv, kernel=5) == 1
+    assert _decode(pkv, kernel=2, cdt=0) == 2      # no tensor-core path for fp32 caches
+    assert _decode(pkv, ws=None, wsb=0) == 3       # split needs a workspace
+    need = pkv.decode_workspace_size(2, 8, 2, 128, 16, 64, 32)
+    assert _decode(pkv, ws=FAKE, wsb=need - 1) == 3
+    assert _decode(pkv, S=0) == 0                  # empty batch is a no-op
+
+
+def test_write_and_copy_host_validation(pkv):
+    L = pkv.lib
+    assert L.pkv_paged_kv_write(FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 4, 10, 16, 2, 12, 1.0, 1.0, None, None) == 2
+    assert L.pkv_paged_kv_write(FAKE, FAKE, 2, FAKE, FAKE, 0, FAKE, 4, 10, 16, 2, 64, 1.0, 1.0, None, None) == 2
+    assert L.pkv_paged_kv_write(None, FAKE, 0, FAKE, FAKE, 0, FAKE, 4, 10, 16, 2, 64, 1.0, 1.0, None, None) == 1
+    assert L.pkv_paged_kv_write(FAKE, FAKE, 0, FAKE, FAKE, 2, FAKE, 4, 10, 16, 2, 64, -1.0, 1.0, None, None) == 1
+    assert L.pkv_paged_kv_write(FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 0, 10, 16, 2, 64, 1.0, 1.0, None, None) == 0
+    arr = (ctypes.c_void_p * 1)(FAKE)
+    assert L.pkv_copy_blocks(arr, arr, 1, FAKE, 3, 10, 1000, None, None) == 1     # block_bytes % 16
+    assert L.pkv_copy_blocks(arr, arr, 300, FAKE, 3, 10, 1024, None, None) == 1   # too many layers
+    bad = (ctypes.c_void_p * 1)(FAKE + 8)
+    assert L.pkv_copy_blocks(bad, arr, 1, FAKE, 3, 10, 1024, None, None) == 1     # misaligned cache
+    assert L.pkv_copy_blocks(arr, arr, 1, FAKE, 0, 10, 1024, None, None) == 0     # nothing to copy
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    """The product path has no fallback: importing the binding from a copy
+    of the package that lacks libpkv.so raises ImportError."""
+    pkg = tmp_path / "paged_kv_cache_44_gb300"
+    pkg.mkdir()
+    (pkg / "__init__.py").write_text(open(os.path.join(ROOT, "paged_kv_cache_44_gb300", "__init__.py")).read())
+    r = subprocess.run(["python", "-c", "import paged_kv_cache_44_gb300"], cwd=tmp_path, capture_output=True,
+                       text=True)
+    assert r.returncode != 0 and "ImportError" in r.stderr and "not built" in r.stderr

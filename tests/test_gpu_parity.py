@@ -1,0 +1,256 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, on the
+same seeded inputs.  Write and copy must match bit for bit; decode must stay
+within the tolerance of its cache dtype (fp32 1e-5; bf16 2e-2 abs + 1e-2
+rel; fp8 5e-2 against the oracle fed the same dequantised values)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import oracle as O
+    import paged_kv_cache_44_gb300 as pkv
+    from tests.gpu_cases import (ODT, assert_close, build_case, gpu_decode, gpu_write, oracle_decode,
+                                 oracle_write)
+
+KERNELS = ["cuda_cores", "tensor_cores"]
+
+
+def _kernels_for(w):
+    """Kernels that apply to this workload (PKV_TEST_KERNELS narrows the list)."""
+    import os
+    ks = ["cuda_cores"]
+    if w.cache_dtype == W.DT_E4M3 or (w.cache_dtype == W.DT_BF16 and w.q_dtype == W.DT_BF16):
+        ks.append("tensor_cores")
+    only = os.environ.get("PKV_TEST_KERNELS")
+    return [k for k in ks if not only or k in only.split(",")]
+
+
+def _np_cache(t: torch.Tensor) -> np.ndarray:
+    t = t.cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+# --------------------------------------------------------------- tiny, fp32
+
+def test_tiny_step_write_decode_copy():
+    """The tiny configuration end to end: write one token per sequence
+    (lengths 1, 15, 16, 37 -> 2, 16, 17, 38), decode, copy-on-write."""
+    w = W.make("tiny")
+    c = build_case(w)
+    # reading (i): decode over the lengths before the write
+    before = w.context_lens - 1
+    ref_i = oracle_decode(c, context_lens=before)
+    out_i = gpu_decode(c, context_lens=torch.from_numpy(before).cuda(), max_context_len=int(before.max()))
+    assert_close(out_i, ref_i, w.cache_dtype, "decode before write")
+    # the write is bit-exact
+    gpu_write(c)
+    oracle_write(c)
+    np.testing.assert_array_equal(_np_cache(c.k_cache), c.o_k)
+    np.testing.assert_array_equal(_np_cache(c.v_cache), c.o_v)
+    # reading (ii): decode over the lengths after the write, every kernel and split
+    ref = oracle_decode(c)
+    for P in (0, -1, 16, 32):
+        out = gpu_decode(c, partition_size=P)
+        assert_close(out, ref, w.cache_dtype, f"decode P={P}")
+    # copy-on-write: bit-exact, then repointing a holder leaves outputs unchanged
+    pkv.copy_blocks([c.k_cache], [c.v_cache], c.cow)
+    O.copy_blocks([c.o_k], [c.o_v], w.cow_pairs)
+    np.testing.assert_array_equal(_np_cache(c.k_cache), c.o_k)
+    np.testing.assert_array_equal(_np_cache(c.v_cache), c.o_v)
+
+
+def test_tiny_single_token_is_v_exactly():
+    w = W.make("tiny")
+    c = build_case(w)
+    ones = torch.ones(w.S, dtype=torch.int32, device="cuda")
+    out = gpu_decode(c, context_lens=ones, max_context_len=1)
+    bt = w.block_tables
+    for s in range(w.S):
+        v0 = c.hv.v_pool[bt[s, 0], 0]                    # [Hkv, d]
+        np.testing.assert_array_equal(out[s].cpu().numpy(), np.repeat(v0, w.g, axis=0))
+
+
+# ------------------------------------------------------ dtype / shape sweep
+
+SWEEP = [
+    # (cache, q, d, bs, Hq, Hkv)
+    ("f32", "f32", 64, 16, 4, 2), ("f32", "f32", 128, 32, 8, 1), ("f32", "bf16", 128, 16, 6, 6),
+    ("bf16", "bf16", 128, 16, 12, 2), ("bf16", "bf16", 64, 32, 16, 2), ("bf16", "bf16", 128, 16, 8, 8),
+    ("bf16", "bf16", 128, 32, 28, 4), ("bf16", "f32", 128, 16, 8, 1),
+    ("e4m3", "bf16", 128, 16, 28, 4), ("e4m3", "bf16", 128, 32, 7, 1), ("e4m3", "f32", 64, 16, 4, 4),
+]
+
+
+def _sweep_workload(cache, q, d, bs, Hq, Hkv, seed):
+    """Ragged lengths around block and partition edges, one empty sequence."""
+    import dataclasses
+    lens = np.array([1, 1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 200, 513, 1000, 1537], np.int64)
+    base = W.make("qwen2.5-1.5b" if bs == 16 else "fp8-bs32", S=len(lens), lengths=lens, seed=seed)
+    cl = base.context_lens.copy()
+    cl[0] = 0
+    return dataclasses.replace(base, Hq=Hq, Hkv=Hkv, d=d, q_dtype=q, cache_dtype=cache, context_lens=cl)
+
+
+@pytest.mark.parametrize("cfg", SWEEP, ids=["-".join(map(str, c)) for c in SWEEP])
+def test_decode_sweep(cfg):
+    w = _sweep_workload(*cfg, seed=40 + SWEEP.index(cfg))
+    c = build_case(w)
+    gpu_write(c)
+    oracle_write(c)
+    np.testing.assert_array_equal(_np_cache(c.k_cache), c.o_k)
+    np.testing.assert_array_equal(_np_cache(c.v_cache), c.o_v)
+    ref = oracle_decode(c)
+    assert (ref[0] == 0).all()
+    for kernel in _kernels_for(w):
+        for P in (0, -1, w.bs, 256):
+            out = gpu_decode(c, partition_size=P, kernel=kernel)
+            assert_close(out, ref, w.cache_dtype, f"{kernel} P={P}")
+            assert (out[0] == 0).all()
+
+
+# ---------------------------------------------------------------- invariance
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_permutation_invariance_bit_identical(kernel):
+    w = W.make("qwen2.5-1.5b", S=8, lengths=np.array([1, 16, 17, 100, 513, 700, 2049, 4000]))
+    c = build_case(w)
+    if kernel not in _kernels_for(w):
+        pytest.skip("kernel does not apply or is not selected")
+    out = gpu_decode(c, kernel=kernel)
+    perm = torch.from_numpy(np.random.default_rng(9).permutation(w.NB)).cuda()
+    k2 = torch.empty_like(c.k_cache); v2 = torch.empty_like(c.v_cache)
+    k2[perm] = c.k_cache; v2[perm] = c.v_cache
+    c.k_cache, c.v_cache = k2, v2
+    out2 = gpu_decode(c, kernel=kernel, block_tables=perm[c.block_tables.long()].to(torch.int32).contiguous())
+    assert torch.equal(out, out2)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_shared_prefix_equals_private_copies(kernel):
+    w = W.make("qwen2.5-7b-prefix", S=12, lengths=np.array([1030, 1100, 2000, 1025, 5000, 1500, 3, 40, 700,
+                                                              1200, 90, 4000]), spare_blocks=64)
+    import dataclasses
+    w = dataclasses.replace(w, shared_seqs=6)
+    c = build_case(w)
+    if kernel not in _kernels_for(w):
+        pytest.skip("kernel does not apply or is not selected")
+    out = gpu_decode(c, kernel=kernel)
+    ref = oracle_decode(c)
+    assert_close(out, ref, w.cache_dtype, "shared prefix")
+    # private copy of the 64 prefix blocks for sequence 2 via copy_blocks, then repoint
+    used = set(w.block_tables[w.block_tables != 0].tolist()) | set(w.cow_pairs[:, 1].tolist())
+    spare = [b for b in range(1, w.NB) if b not in used][:64]
+    pairs = np.stack([w.block_tables[2, :64], spare], axis=1).astype(np.int64)
+    pkv.copy_blocks([c.k_cache], [c.v_cache], torch.from_numpy(pairs).cuda())
+    bt = c.block_tables.clone()
+    bt[2, :64] = torch.tensor(spare, dtype=torch.int32)
+    out2 = gpu_decode(c, kernel=kernel, block_tables=bt)
+    assert torch.equal(out, out2)
+
+
+# ---------------------------------------------------------------- device errors
+
+def test_bad_block_ids_are_skipped_and_reported():
+    w = W.make("qwen2.5-1.5b", S=3, lengths=np.array([40, 600, 33]))
+    c = build_case(w)
+    bt = c.block_tables.clone()
+    bt[1, 3] = w.NB + 1000          # out of range: must be skipped, not read
+    bt[2, 1] = -7
+    for kernel in _kernels_for(w):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = gpu_decode(c, kernel=kernel, block_tables=bt, err_word=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 1
+        assert torch.isfinite(out.float()).all()
+        ref = oracle_decode(c)
+        assert_close(out[0:1], ref[0:1], w.cache_dtype, "unaffected sequence")
+
+
+def test_bad_context_len_is_clamped_and_reported():
+    w = W.make("qwen2.5-1.5b", S=2, lengths=np.array([40, 60]))
+    c = build_case(w)
+    cl = c.context_lens.clone()
+    cl[1] = w.MB * w.bs + 50
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = gpu_decode(c, context_lens=cl, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 2
+    assert torch.isfinite(out.float()).all()
+
+
+def test_bad_slot_is_skipped_and_reported():
+    w = W.make("tiny")
+    c = build_case(w)
+    sm = c.slot_mapping.clone()
+    sm[0] = w.NB * w.bs + 3
+    sm[1] = -1
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.paged_kv_write(c.new_k, c.new_v, c.k_cache, c.v_cache, sm, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 3
+    c.slot_mapping = sm
+    ow_slots = c.ow.slot_mapping.copy()
+    ow_slots[0] = -1
+    ow_slots[1] = -1
+    c.ow.slot_mapping = ow_slots
+    oracle_write(c)
+    np.testing.assert_array_equal(_np_cache(c.k_cache), c.o_k)
+
+
+def test_bad_copy_pair_is_skipped_and_reported():
+    w = W.make("tiny")
+    c = build_case(w)
+    before = c.k_cache.clone()
+    pairs = torch.tensor([[1, w.NB + 2], [-1, 3]], dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.copy_blocks([c.k_cache], [c.v_cache], pairs, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 4
+    assert torch.equal(before, c.k_cache)
+
+
+# ------------------------------------------------------------ full-size runs
+
+FULL = [("qwen2.5-1.5b", None), ("qwen2.5-7b-prefix", None), ("qwen2.5-72b-long", 3), ("fp8-bs16", 4),
+        ("fp8-bs32", 4)]
+
+
+@pytest.mark.parametrize("name,sample", FULL, ids=[f[0] for f in FULL])
+def test_full_size_step(name, sample):
+    """The configuration at full size, in the launch configuration the
+    benchmark times: write -> decode -> copy_blocks.  Every sequence is
+    checked where the oracle finishes in seconds, else a sample of sequences
+    (shortest, longest, a prefix sharer, random), plus properties that hold
+    at any size: outputs are finite and bounded by max |V| (a convex
+    combination), and the write is bit-exact on the sampled blocks."""
+    w = W.make(name)
+    c = build_case(w, sample=sample)
+    gpu_write(c)
+    oracle_write(c)
+    if sample is None:
+        np.testing.assert_array_equal(_np_cache(c.k_cache), c.o_k)
+        np.testing.assert_array_equal(_np_cache(c.v_cache), c.o_v)
+    else:
+        ids = torch.from_numpy(c.ow.renumber.astype(np.int64)).cuda()
+        np.testing.assert_array_equal(_np_cache(c.k_cache[ids]), c.o_k)
+        np.testing.assert_array_equal(_np_cache(c.v_cache[ids]), c.o_v)
+    ref = oracle_decode(c)
+    for kernel in _kernels_for(w):
+        out = gpu_decode(c, kernel=kernel)
+        assert_close(out[torch.from_numpy(c.seqs).cuda()], ref, w.cache_dtype, f"{name} {kernel}")
+        of = out.float()
+        assert torch.isfinite(of).all()
+        if w.cache_dtype == W.DT_E4M3:
+            vmax = 448.0 * c.v_scale
+        else:
+            vmax = float(c.v_cache.float().abs().max())
+        assert float(of.abs().max()) <= vmax * 1.01 + 1e-3
+    pkv.copy_blocks([c.k_cache], [c.v_cache], c.cow)
+    src = c.cow[:, 0]; dst = c.cow[:, 1]
+    assert torch.equal(c.k_cache[src], c.k_cache[dst]) and torch.equal(c.v_cache[src], c.v_cache[dst])

@@ -282,3 +282,28 @@ def sub_workload(w: Workload, seqs: np.ndarray) -> Workload:
                              cow_pairs=np.zeros((0, 2), np.int64))
     sw.renumber = used  # type: ignore[attr-defined]
     return sw
+
+
+# ------------------------------------------------------ device-side draws
+
+def device_normal(seed: int, tag: int, numel: int, device="cuda"):
+    """float32 N(0, 1) draws from torch's seeded generator on `device`
+    (used where host draws of several GB would take too long)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 1000003 + tag)
+    return torch.randn(numel, generator=g, device=device, dtype=torch.float32)
+
+
+def device_bf16_from_draws(x):
+    """bf16 values from float32 draws on the device: keep the upper 16 bits
+    (the same drawing recipe as bf16_bits)."""
+    import torch
+    return (x.view(torch.int32) >> 16).to(torch.int16).view(torch.bfloat16)
+
+
+def device_pool_chunks(seed: int, which: int, numel: int, device="cuda", chunk: int = 1 << 26):
+    """Yield (offset, float32 draws) covering `numel` pool elements."""
+    for i, c0 in enumerate(range(0, numel, chunk)):
+        n = min(chunk, numel - c0)
+        yield c0, device_normal(seed, which * 100000 + i, n, device)
