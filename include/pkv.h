@@ -25,7 +25,7 @@
  * unsupported dtypes or shapes, a workspace that is too small) return a
  * status other than PKV_OK before anything is enqueued.  Problems visible
  * only on the device (a block id outside [0, NB), a context length above
- * MB * bs, a slot outside [0, NB * bs), a copy pair out of range) never
+ * max_context_len, a slot outside [0, NB * bs), a copy pair out of range) never
  * fault: the offending block, token or pair is skipped and, when `err_word`
  * is not NULL, the first such problem's code (PKV_DEVERR_*) is stored there
  * with an atomic compare-and-swap from 0.  A launch failure returns
@@ -67,7 +67,7 @@ typedef enum {
 enum {
     PKV_DEVERR_NONE = 0,
     PKV_DEVERR_BLOCK_ID = 1,      /* a block table entry outside [0, NB) */
-    PKV_DEVERR_CONTEXT_LEN = 2,   /* context_lens[s] < 0 or > MB * bs */
+    PKV_DEVERR_CONTEXT_LEN = 2,   /* context_lens[s] < 0 or > max_context_len (clamped) */
     PKV_DEVERR_SLOT = 3,          /* slot_mapping[i] >= NB * bs */
     PKV_DEVERR_COPY_PAIR = 4      /* a copy pair with an id outside [0, NB) */
 };

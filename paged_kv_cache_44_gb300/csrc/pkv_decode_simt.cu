@@ -37,9 +37,9 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     int n = p.context_lens[s];
-    if (n < 0 || n > p.MB * p.bs) {
+    if (n < 0 || n > p.max_ctx) {   // max_ctx <= MB * bs was checked on the host
         if (part == 0 && blockIdx.y == 0 && threadIdx.x == 0) report(p.err, PKV_DEVERR_CONTEXT_LEN);
-        n = n < 0 ? 0 : p.MB * p.bs;
+        n = n < 0 ? 0 : p.max_ctx;
     }
     const int np = n > 0 ? (n + p.P - 1) / p.P : 1;
     if (part >= np) return;
@@ -167,7 +167,7 @@ template <typename QF>
 __global__ void __launch_bounds__(128) decode_reduce_kernel(DecodeParams p) {
     const int h = blockIdx.x, s = blockIdx.y;
     int n = p.context_lens[s];
-    n = n < 0 ? 0 : min(n, p.MB * p.bs);
+    n = n < 0 ? 0 : min(n, p.max_ctx);     // same clamp as the decode kernel: np <= Pmax
     const int np = n > 0 ? (n + p.P - 1) / p.P : 1;
     if (np <= 1) return;
     const size_t u0 = ((size_t)s * p.Hq + h) * p.Pmax;

@@ -176,9 +176,9 @@ def test_bad_context_len_is_clamped_and_reported():
     w = W.make("qwen2.5-1.5b", S=2, lengths=np.array([40, 60]))
     c = build_case(w)
     cl = c.context_lens.clone()
-    cl[1] = w.MB * w.bs + 50
+    cl[1] = w.max_context_len + 50           # above the host bound: clamped, reported
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = gpu_decode(c, context_lens=cl, err_word=err)
+    out = gpu_decode(c, context_lens=cl, err_word=err, partition_size=16)
     torch.cuda.synchronize()
     assert int(err.item()) == 2
     assert torch.isfinite(out.float()).all()
