@@ -69,7 +69,8 @@ enum {
     PKV_DEVERR_BLOCK_ID = 1,      /* a block table entry outside [0, NB) */
     PKV_DEVERR_CONTEXT_LEN = 2,   /* context_lens[s] < 0 or > max_context_len (clamped) */
     PKV_DEVERR_SLOT = 3,          /* slot_mapping[i] >= NB * bs */
-    PKV_DEVERR_COPY_PAIR = 4      /* a copy pair with an id outside [0, NB) */
+    PKV_DEVERR_COPY_PAIR = 4,     /* a copy pair with an id outside [0, NB) */
+    PKV_DEVERR_TIMEOUT = 5        /* a staged copy did not land within ~2 s; the kernel gave up */
 };
 
 /*

@@ -46,7 +46,8 @@ def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
             f"{LIB_PATH} is not built. Build it with "
-            "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc for sm_103a).")
+            "`python -c 'import __graft_entry__ as g; g.build()'` or "
+            "`python paged_kv_cache_44_gb300/_build.py` (needs nvcc for sm_103a).")
     lib = ctypes.CDLL(LIB_PATH)
     vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.pkv_paged_kv_write.argtypes = [vp, vp, i32, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, f32, vp, vp]

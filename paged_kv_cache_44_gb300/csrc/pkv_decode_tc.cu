@@ -1,8 +1,626 @@
-// placeholder until the tensor-core kernel lands
+// paged_attention_decode on tensor cores (sm_103a).
+//
+// "LLM推論の基礎とvLLMの内部", section 4: each sequence's K/V is reached
+// through its block table; section 2: the query heads of a GQA group share
+// one K/V head, so one read of a K/V block serves the whole group; section 1:
+// decode is bound by memory bandwidth, so the design goal is to keep HBM
+// streaming.
+//
+// Work unit: (sequence, K/V head, set of <= 8 query heads, partition of P
+// tokens).  Each warp is an independent worker: it claims units from a
+// counter in the workspace header (or takes them round-robin without one),
+// and streams the unit's K/V through its own ring of shared-memory stages.
+// A stage is 32 tokens of K and V for one K/V head: one lane per token row
+// issues two 1-D bulk copies (cp.async.bulk, the TMA engine) from the
+// physical block the table names, completing on the stage's mbarrier.  Rows
+// are padded by 16 bytes so the tensor-core operand loads are free of bank
+// conflicts.  The warp keeps up to kStages-1 stages in flight while it works
+// on one, and it prefetches across unit boundaries.
+//
+// Math per stage (mma.sync m16n8k16, fp32 accumulate):
+//   S^T[16 tokens x 8 heads] = K[16 x d] . Q^T[d x 8]          (d/16 MMAs per 16 tokens)
+//   online softmax over the stage (running max m, sum l, base 2)
+//   O^T[d x 8 heads] += V^T[d x 16 tokens] . P^T[16 tokens x 8]  (d/16 MMAs per 16 tokens)
+// P^T is the S^T accumulator converted to 16-bit and transposed in registers
+// (movmatrix).  bf16 caches use bf16 operands loaded with ldmatrix; E4M3
+// caches are widened to fp16 in registers (cvt.rn.f16x2.e4m3x2, exact) and
+// use fp16 operands with the query rounded to fp16.  For E4M3 the head
+// dimension and the tokens are visited in a fixed permutation (the same on
+// both operands of each product) so that every thread reads contiguous bytes.
+//
+// A unit that covers its whole sequence writes `out`; otherwise it writes
+// (m, l, unnormalised O) to the workspace for the merge kernel.
+#include <math_constants.h>
+
+#include "pkv_common.cuh"
 #include "pkv_internal.h"
+
 namespace pkv {
-bool decode_tc_supports(pkv_dtype, pkv_dtype, int, int) { return false; }  // stub
-cudaError_t launch_decode_tc(const DecodeParams&, pkv_dtype, pkv_dtype, int, cudaStream_t) {
-    return cudaErrorNotSupported;
+namespace {
+
+constexpr int kWarps = 4;       // workers per CTA
+constexpr int kTok = 32;        // tokens per stage
+constexpr int kHeadsPerUnit = 8;
+constexpr long long kWaitLimitCycles = 4000000000LL;   // ~2 s: a stage that never lands
+
+template <int D, bool FP8>
+struct Cfg {
+    static constexpr int kRowBytes = FP8 ? D : 2 * D;
+    static constexpr int kPitch = kRowBytes + 16;
+    static constexpr int kHalfBytes = kTok * kPitch;             // K (or V) part of a stage
+    static constexpr int kStageBytes = 2 * kHalfBytes;
+    static constexpr int kStages = FP8 ? 5 : 3;
+    static constexpr int kQueue = kStages + 1;
+    // per-warp shared memory: stages, then barriers, masks, unit queue
+    static constexpr int kBarOff = kStages * kStageBytes;
+    static constexpr int kMaskOff = kBarOff + 8 * kStages;
+    static constexpr int kQueueOff = (kMaskOff + 4 * kStages + 7) / 8 * 8;   // 8-byte entries
+    static constexpr int kWarpBytes = (kQueueOff + 8 * kQueue + 127) / 128 * 128;
+    static constexpr int kSmemBytes = kWarps * kWarpBytes;
+    static constexpr int KS = D / 16;     // k-steps of the QK product, m-tiles of the PV product
+};
+
+// ------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+template <bool FP8>
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    if constexpr (FP8) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+}
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// two E4M3 codes (low byte first) -> two fp16 in one register, exactly
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    uint32_t r;
+    const uint16_t c = static_cast<uint16_t>(two_codes);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
+    return r;
+}
+template <bool FP8>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (FP8) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
+// ------------------------------------------------------------------- units
+
+struct Unit {
+    int s, kvh, h0, nh, part, t0, t1, np;
+};
+
+// Unit id -> coordinates.  Ids run partition-major so that the same
+// partition of every sequence is claimed close together in time (shared
+// prefix blocks are then read while still in L2).  Returns false for ids
+// past a sequence's last partition.
+__device__ __forceinline__ bool unit_of(const DecodeParams& p, unsigned long long u, int nsets, Unit& x) {
+    const unsigned long long per_part = (unsigned long long)p.S * p.Hkv * nsets;
+    x.part = (int)(u / per_part);
+    const unsigned long long rem = u - (unsigned long long)x.part * per_part;
+    x.s = (int)(rem / (unsigned)(p.Hkv * nsets));
+    const int r2 = (int)(rem - (unsigned long long)x.s * (p.Hkv * nsets));
+    x.kvh = r2 / nsets;
+    const int set = r2 - x.kvh * nsets;
+    x.h0 = x.kvh * p.g + set * kHeadsPerUnit;
+    x.nh = min(kHeadsPerUnit, p.g - set * kHeadsPerUnit);
+    int n = __ldg(p.context_lens + x.s);
+    if (n < 0 || n > p.max_ctx) {
+        if (x.part == 0 && r2 == 0) report(p.err, PKV_DEVERR_CONTEXT_LEN);
+        n = n < 0 ? 0 : p.max_ctx;
+    }
+    x.np = n > 0 ? (n + p.P - 1) / p.P : 1;
+    if (x.part >= x.np) return false;
+    x.t0 = x.part * p.P;
+    x.t1 = min(n, x.t0 + p.P);
+    return true;
+}
+
+template <typename QF>
+__device__ __forceinline__ void store_out(const DecodeParams& p, size_t idx, float v) {
+    store_elem<QF>(p.out, idx, v);
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int D, bool FP8, typename QF>
+__global__ void __launch_bounds__(kWarps * 32, 1)
+    decode_tc_kernel(const __grid_constant__ DecodeParams p, unsigned long long total_units, int nsets) {
+    using C = Cfg<D, FP8>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int r = lane >> 2, c = lane & 3;     // fragment row / column-pair of this lane
+    unsigned char* ws = smem + warp * C::kWarpBytes;
+    const uint32_t ws_addr = smem_addr(ws);
+    uint32_t* masks = reinterpret_cast<uint32_t*>(ws + C::kMaskOff);
+    unsigned long long* queue = reinterpret_cast<unsigned long long*>(ws + C::kQueueOff);
+    auto bar = [&](int i) { return ws_addr + C::kBarOff + 8 * i; };
+    auto stage_k = [&](int i) { return ws_addr + i * C::kStageBytes; };
+    auto stage_v = [&](int i) { return ws_addr + i * C::kStageBytes + C::kHalfBytes; };
+
+    if (lane == 0) {
+        for (int i = 0; i < C::kStages; ++i) mbar_init(bar(i), 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+
+    const unsigned long long total_warps = (unsigned long long)gridDim.x * kWarps;
+    const unsigned long long my_warp = (unsigned long long)blockIdx.x * kWarps + warp;
+    unsigned long long static_next = my_warp;
+    const size_t row_elems = (size_t)p.Hkv * D;      // elements between consecutive tokens of a block
+
+    // ---- issue side: claims units, fills stages
+    bool claiming = true;
+    bool i_have = false;
+    Unit iu{};
+    int i_stage = 0, i_nst = 0;
+    unsigned g_issue = 0, q_tail = 0;
+
+    auto claim = [&](unsigned long long& u) -> bool {
+        for (;;) {
+            unsigned long long v = 0;
+            if (lane == 0) {
+                if (p.sched != nullptr) {
+                    v = atomicAdd(reinterpret_cast<unsigned long long*>(p.sched), 1ull);
+                } else {
+                    v = static_next;
+                    static_next += total_warps;
+                }
+            }
+            v = __shfl_sync(0xffffffffu, v, 0);
+            if (lane != 0 && p.sched == nullptr) static_next += total_warps;
+            if (v >= total_units) return false;
+            Unit x;
+            if (!unit_of(p, v, nsets, x)) continue;
+            if (x.t1 <= x.t0) {
+                // a sequence with no tokens: its output is zero
+                for (int i = lane; i < x.nh * D; i += 32)
+                    store_out<QF>(p, ((size_t)x.s * p.Hq + x.h0 + i / D) * D + (i % D), 0.f);
+                continue;
+            }
+            u = v;
+            return true;
+        }
+    };
+
+    auto issue_one = [&]() -> bool {
+        while (!i_have || i_stage == i_nst) {
+            if (!claiming) return false;
+            unsigned long long u;
+            if (!claim(u)) {
+                claiming = false;
+                return false;
+            }
+            unit_of(p, u, nsets, iu);
+            if (lane == 0) queue[q_tail % C::kQueue] = u;
+            ++q_tail;
+            i_have = true;
+            i_stage = 0;
+            i_nst = (iu.t1 - iu.t0 + kTok - 1) / kTok;
+        }
+        const int slot = g_issue % C::kStages;
+        const int ts = iu.t0 + i_stage * kTok;
+        const int tn = min(kTok, iu.t1 - ts);
+        const int t = ts + lane;
+        bool ok = lane < tn;
+        int pb = 0;
+        if (ok) {
+            pb = __ldg(p.block_tables + (size_t)iu.s * p.MB + t / p.bs);
+            if (pb < 0 || pb >= p.NB) {
+                report(p.err, PKV_DEVERR_BLOCK_ID);
+                ok = false;
+            }
+        }
+        const uint32_t m = __ballot_sync(0xffffffffu, ok);
+        if (lane == 0) {
+            masks[slot] = m;
+            mbar_arrive_expect_tx(bar(slot), (uint32_t)__popc(m) * 2u * C::kRowBytes);
+        }
+        __syncwarp();
+        if (ok) {
+            const size_t off = ((size_t)pb * p.bs + (t % p.bs)) * row_elems + (size_t)iu.kvh * D;
+            const unsigned char* kg = static_cast<const unsigned char*>(p.kc) + off * (FP8 ? 1 : 2);
+            const unsigned char* vg = static_cast<const unsigned char*>(p.vc) + off * (FP8 ? 1 : 2);
+            bulk_load(stage_k(slot) + lane * C::kPitch, kg, C::kRowBytes, bar(slot));
+            bulk_load(stage_v(slot) + lane * C::kPitch, vg, C::kRowBytes, bar(slot));
+        }
+        ++g_issue;
+        ++i_stage;
+        return true;
+    };
+
+    // ---- consume side
+    unsigned g_cons = 0, q_head = 0;
+    bool have_unit = false;
+    Unit cu{};
+    int c_stage = 0, c_nst = 0;
+    uint32_t qf[C::KS][2];                // Q^T fragments (n = head r)
+    float o[C::KS][4];                    // O^T accumulators, m-tile t of d
+    float m_run[2], l_run[2];             // heads 2c, 2c+1
+    const float scl = p.logit_scale_log2;
+    bool bail = false;
+
+    for (int i = 0; i < C::kStages; ++i)
+        if (!issue_one()) break;
+
+    for (;;) {
+        if (!have_unit) {
+            if (q_head == q_tail) break;
+            __syncwarp();
+            const unsigned long long u = queue[q_head % C::kQueue];
+            ++q_head;
+            unit_of(p, u, nsets, cu);
+            c_stage = 0;
+            c_nst = (cu.t1 - cu.t0 + kTok - 1) / kTok;
+            have_unit = true;
+            // Q^T fragments of head r (zero past the unit's heads)
+            const bool hv = r < cu.nh;
+            const size_t qrow = ((size_t)cu.s * p.Hq + cu.h0 + (hv ? r : 0)) * D;
+#pragma unroll
+            for (int ks = 0; ks < C::KS; ++ks) {
+                int d0, d1;
+                if constexpr (FP8) {
+                    d0 = 64 * (ks / 4) + 16 * c + 4 * (ks % 4);      // 4 consecutive d: j = 0..3
+                    d1 = d0 + 2;
+                } else {
+                    d0 = 16 * ks + 2 * c;
+                    d1 = d0 + 8;
+                }
+                float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+                if (hv) {
+                    x0 = load_elem<QF>(p.q, qrow + d0);
+                    x1 = load_elem<QF>(p.q, qrow + d0 + 1);
+                    x2 = load_elem<QF>(p.q, qrow + d1);
+                    x3 = load_elem<QF>(p.q, qrow + d1 + 1);
+                }
+                qf[ks][0] = pack2<FP8>(x0, x1);
+                qf[ks][1] = pack2<FP8>(x2, x3);
+            }
+#pragma unroll
+            for (int t = 0; t < C::KS; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+            m_run[0] = m_run[1] = -CUDART_INF_F;
+            l_run[0] = l_run[1] = 0.f;
+        }
+
+        const int slot = g_cons % C::kStages;
+        const uint32_t parity = (g_cons / C::kStages) & 1u;
+        if (!mbar_try_wait(bar(slot), parity)) {
+            const long long t_start = clock64();
+            while (!mbar_try_wait(bar(slot), parity)) {
+                if (clock64() - t_start > kWaitLimitCycles) {
+                    report(p.err, PKV_DEVERR_TIMEOUT);
+                    bail = true;
+                    break;
+                }
+            }
+        }
+        if (__any_sync(0xffffffffu, bail)) break;
+        const uint32_t vmask = masks[slot];
+        const uint32_t kb = stage_k(slot), vb = stage_v(slot);
+
+        // ---- S^T = K . Q^T for the two 16-token m-tiles of the stage
+        float sacc[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            sacc[mt][0] = sacc[mt][1] = sacc[mt][2] = sacc[mt][3] = 0.f;
+            if constexpr (FP8) {
+                // rows of this lane: tokens pi(r) and pi(r+8) of the m-tile,
+                // pi(2i+b) = 4i+b, pi(2i+8+b) = 4i+2+b
+                const int ta = 16 * mt + 4 * (r >> 1) + (r & 1);
+                const int tb = ta + 2;
+                // Load both halves of both rows (odd rows start with the other
+                // half, which spreads a load over all banks), then run the
+                // MMAs in one k-step order common to every lane.
+                const unsigned char* ra = ws + (kb - ws_addr) + ta * C::kPitch + 16 * c;
+                const unsigned char* rb = ws + (kb - ws_addr) + tb * C::kPitch + 16 * c;
+                uint4 ka[D / 64], kbv[D / 64];
+                if constexpr (D == 128) {
+                    const int first = (r & 1) * 64, second = 64 - first;
+                    const uint4 a0 = *reinterpret_cast<const uint4*>(ra + first);
+                    const uint4 b0 = *reinterpret_cast<const uint4*>(rb + first);
+                    const uint4 a1 = *reinterpret_cast<const uint4*>(ra + second);
+                    const uint4 b1 = *reinterpret_cast<const uint4*>(rb + second);
+                    const bool odd = r & 1;
+                    ka[0] = odd ? a1 : a0;  ka[1] = odd ? a0 : a1;
+                    kbv[0] = odd ? b1 : b0; kbv[1] = odd ? b0 : b1;
+                } else {
+                    ka[0] = *reinterpret_cast<const uint4*>(ra);
+                    kbv[0] = *reinterpret_cast<const uint4*>(rb);
+                }
+#pragma unroll
+                for (int hh = 0; hh < D / 64; ++hh) {
+                    const uint32_t wa[4] = {ka[hh].x, ka[hh].y, ka[hh].z, ka[hh].w};
+                    const uint32_t wb[4] = {kbv[hh].x, kbv[hh].y, kbv[hh].z, kbv[hh].w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int ks = 4 * hh + j;
+                        mma16816<true>(sacc[mt], e4m3x2_to_f16x2(wa[j]), e4m3x2_to_f16x2(wb[j]),
+                                       e4m3x2_to_f16x2(wa[j] >> 16), e4m3x2_to_f16x2(wb[j] >> 16), qf[ks][0],
+                                       qf[ks][1]);
+                    }
+                }
+            } else {
+                const int mi = lane >> 3;
+                const uint32_t rowaddr = kb + (16 * mt + 8 * (mi & 1) + (lane & 7)) * C::kPitch + 16 * (mi >> 1);
+#pragma unroll
+                for (int ks = 0; ks < C::KS; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(rowaddr + 32 * ks, a0, a1, a2, a3);
+                    mma16816<false>(sacc[mt], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+                }
+            }
+        }
+
+        // ---- online softmax over the stage's 32 tokens (log2 units)
+        // token of accumulator rows: (mt, row r) and (mt, row r+8)
+        float x[2][4];
+        float cmax0 = -CUDART_INF_F, cmax1 = -CUDART_INF_F;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            int ta, tb;
+            if constexpr (FP8) {
+                ta = 16 * mt + 4 * (r >> 1) + (r & 1);
+                tb = ta + 2;
+            } else {
+                ta = 16 * mt + r;
+                tb = ta + 8;
+            }
+            const bool va = (vmask >> ta) & 1u, vb2 = (vmask >> tb) & 1u;
+            x[mt][0] = va ? sacc[mt][0] * scl : -CUDART_INF_F;
+            x[mt][1] = va ? sacc[mt][1] * scl : -CUDART_INF_F;
+            x[mt][2] = vb2 ? sacc[mt][2] * scl : -CUDART_INF_F;
+            x[mt][3] = vb2 ? sacc[mt][3] * scl : -CUDART_INF_F;
+            cmax0 = fmaxf(cmax0, fmaxf(x[mt][0], x[mt][2]));
+            cmax1 = fmaxf(cmax1, fmaxf(x[mt][1], x[mt][3]));
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            cmax0 = fmaxf(cmax0, __shfl_xor_sync(0xffffffffu, cmax0, off));
+            cmax1 = fmaxf(cmax1, __shfl_xor_sync(0xffffffffu, cmax1, off));
+        }
+        const float mn0 = fmaxf(m_run[0], cmax0), mn1 = fmaxf(m_run[1], cmax1);
+        const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
+        const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
+        const float al0 = fast_exp2(m_run[0] - mu0), al1 = fast_exp2(m_run[1] - mu1);
+        m_run[0] = mn0;
+        m_run[1] = mn1;
+        float ls0 = 0.f, ls1 = 0.f;
+        uint32_t pb[2][2];                 // P^T B-fragments for the two k-tiles
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            const float p0 = fast_exp2(x[mt][0] - mu0), p1 = fast_exp2(x[mt][1] - mu1);
+            const float p2 = fast_exp2(x[mt][2] - mu0), p3 = fast_exp2(x[mt][3] - mu1);
+            ls0 += p0 + p2;
+            ls1 += p1 + p3;
+            pb[mt][0] = movmatrix_t(pack2<FP8>(p0, p1));
+            pb[mt][1] = movmatrix_t(pack2<FP8>(p2, p3));
+        }
+        l_run[0] = l_run[0] * al0 + ls0;
+        l_run[1] = l_run[1] * al1 + ls1;
+#pragma unroll
+        for (int t = 0; t < C::KS; ++t) {
+            o[t][0] *= al0;
+            o[t][1] *= al1;
+            o[t][2] *= al0;
+            o[t][3] *= al1;
+        }
+
+        // ---- O^T += V^T . P^T
+        const bool full = vmask == 0xffffffffu;
+#pragma unroll
+        for (int kt = 0; kt < 2; ++kt) {
+            if constexpr (FP8) {
+                // this lane's tokens: 16kt + 4c + j, bytes [D/8 * r, D/8 * (r+1)) of each row
+                uint32_t w[4][D / 32];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const unsigned char* row = ws + (vb - ws_addr) + (16 * kt + 4 * c + j) * C::kPitch + (D / 8) * r;
+                    if constexpr (D == 128) {
+                        const uint4 v4 = *reinterpret_cast<const uint4*>(row);
+                        w[j][0] = v4.x; w[j][1] = v4.y; w[j][2] = v4.z; w[j][3] = v4.w;
+                    } else {
+                        const uint2 v2 = *reinterpret_cast<const uint2*>(row);
+                        w[j][0] = v2.x; w[j][1] = v2.y;
+                    }
+                    if (!full && !((vmask >> (16 * kt + 4 * c + j)) & 1u)) {
+#pragma unroll
+                        for (int q = 0; q < D / 32; ++q) w[j][q] = 0u;
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < C::KS; ++t) {
+                    // d = (D/8) r + 2t (rows r) and +1 (rows r+8): byte 2t and 2t+1 of the lane's bytes
+                    const int wi = t >> 1;
+                    const uint32_t sel = (t & 1) ? 0x7362u : 0x5140u;
+                    const uint32_t p01 = __byte_perm(w[0][wi], w[1][wi], sel);   // tokens 4c, 4c+1
+                    const uint32_t p23 = __byte_perm(w[2][wi], w[3][wi], sel);   // tokens 4c+2, 4c+3
+                    mma16816<true>(o[t], e4m3x2_to_f16x2(p01), e4m3x2_to_f16x2(p01 >> 16), e4m3x2_to_f16x2(p23),
+                                   e4m3x2_to_f16x2(p23 >> 16), pb[kt][0], pb[kt][1]);
+                }
+            } else {
+                const int mi = lane >> 3;
+                const uint32_t rowaddr = vb + (16 * kt + 8 * (mi >> 1) + (lane & 7)) * C::kPitch + 16 * (mi & 1);
+                const int tk0 = 16 * kt + 2 * c;     // tokens of a0a1/a2a3: tk0, tk0+1; of a4a5/a6a7: +8
+                const uint32_t keep01 = (vmask >> tk0) & 3u, keep89 = (vmask >> (tk0 + 8)) & 3u;
+                const uint32_t mlo = (keep01 & 1u ? 0x0000ffffu : 0u) | (keep01 & 2u ? 0xffff0000u : 0u);
+                const uint32_t mhi = (keep89 & 1u ? 0x0000ffffu : 0u) | (keep89 & 2u ? 0xffff0000u : 0u);
+#pragma unroll
+                for (int t = 0; t < C::KS; ++t) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(rowaddr + 32 * t, a0, a1, a2, a3);
+                    if (!full) {
+                        a0 &= mlo; a1 &= mlo; a2 &= mhi; a3 &= mhi;
+                    }
+                    mma16816<false>(o[t], a0, a1, a2, a3, pb[kt][0], pb[kt][1]);
+                }
+            }
+        }
+
+        // the slot is free again: let the issue side refill it
+        __syncwarp();
+        fence_proxy_async();
+        ++g_cons;
+        ++c_stage;
+        issue_one();
+
+        if (c_stage == c_nst) {
+            // ---- finish the unit: full sums over the 8 lanes that share c
+            float l0 = l_run[0], l1 = l_run[1];
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+            }
+            const int hA = 2 * c, hB = 2 * c + 1;
+            const bool wA = hA < cu.nh, wB = hB < cu.nh;
+            if (cu.np == 1) {
+                const float fA = l0 > 0.f ? p.out_scale / l0 : 0.f;
+                const float fB = l1 > 0.f ? p.out_scale / l1 : 0.f;
+                const size_t oA = ((size_t)cu.s * p.Hq + cu.h0 + hA) * D, oB = oA + D;
+#pragma unroll
+                for (int t = 0; t < C::KS; ++t) {
+                    int d0, d1;
+                    if constexpr (FP8) { d0 = (D / 8) * r + 2 * t; d1 = d0 + 1; }
+                    else { d0 = 16 * t + r; d1 = d0 + 8; }
+                    if (wA) { store_out<QF>(p, oA + d0, o[t][0] * fA); store_out<QF>(p, oA + d1, o[t][2] * fA); }
+                    if (wB) { store_out<QF>(p, oB + d0, o[t][1] * fB); store_out<QF>(p, oB + d1, o[t][3] * fB); }
+                }
+            } else {
+                const size_t uA = ((size_t)cu.s * p.Hq + cu.h0 + hA) * p.Pmax + cu.part;
+                const size_t uB = uA + p.Pmax;
+#pragma unroll
+                for (int t = 0; t < C::KS; ++t) {
+                    int d0, d1;
+                    if constexpr (FP8) { d0 = (D / 8) * r + 2 * t; d1 = d0 + 1; }
+                    else { d0 = 16 * t + r; d1 = d0 + 8; }
+                    if (wA) { p.part_acc[uA * D + d0] = o[t][0]; p.part_acc[uA * D + d1] = o[t][2]; }
+                    if (wB) { p.part_acc[uB * D + d0] = o[t][1]; p.part_acc[uB * D + d1] = o[t][3]; }
+                }
+                if (r == 0) {
+                    if (wA) { p.part_ml[2 * uA] = m_run[0]; p.part_ml[2 * uA + 1] = l0; }
+                    if (wB) { p.part_ml[2 * uB] = m_run[1]; p.part_ml[2 * uB + 1] = l1; }
+                }
+            }
+            have_unit = false;
+        }
+    }
+
+    // ---- leave the scheduling counters at zero for the next launch
+    if (p.sched != nullptr && lane == 0) {
+        unsigned long long* ctr = reinterpret_cast<unsigned long long*>(p.sched);
+        __threadfence();
+        const unsigned long long done = atomicAdd(ctr + 1, 1ull);
+        if (done == total_warps - 1) {
+            atomicExch(ctr, 0ull);
+            atomicExch(ctr + 1, 0ull);
+        }
+    }
+}
+
+template <int D, bool FP8, typename QF>
+cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t st) {
+    using C = Cfg<D, FP8>;
+    auto kern = decode_tc_kernel<D, FP8, QF>;
+    // the shared-memory opt-in is per device: remember it per device ordinal
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = true;
+    }
+    const int nsets = (p.g + kHeadsPerUnit - 1) / kHeadsPerUnit;
+    const unsigned long long units = (unsigned long long)p.Pmax * p.S * p.Hkv * nsets;
+    unsigned long long want = (units + kWarps - 1) / kWarps;
+    int grid = (int)(want < (unsigned long long)num_sms ? want : (unsigned long long)num_sms);
+    if (grid < 1) grid = 1;
+    kern<<<grid, kWarps * 32, C::kSmemBytes, st>>>(p, units, nsets);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_tc_supports(pkv_dtype q_dt, pkv_dtype c_dt, int d, int bs) {
+    if (!(d == 64 || d == 128) || !(bs == 16 || bs == 32)) return false;
+    if (c_dt == PKV_BF16) return q_dt == PKV_BF16;
+    return c_dt == PKV_FP8_E4M3 && (q_dt == PKV_BF16 || q_dt == PKV_F32);
+}
+
+cudaError_t launch_decode_tc(const DecodeParams& p, pkv_dtype q_dt, pkv_dtype c_dt, int num_sms, cudaStream_t st) {
+    if (p.S == 0) return cudaSuccess;
+    if (c_dt == PKV_BF16) {
+        return p.d == 64 ? launch_one<64, false, BF16>(p, num_sms, st) : launch_one<128, false, BF16>(p, num_sms, st);
+    }
+    if (q_dt == PKV_BF16)
+        return p.d == 64 ? launch_one<64, true, BF16>(p, num_sms, st) : launch_one<128, true, BF16>(p, num_sms, st);
+    return p.d == 64 ? launch_one<64, true, F32>(p, num_sms, st) : launch_one<128, true, F32>(p, num_sms, st);
+}
+
 }  // namespace pkv

@@ -15,8 +15,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def pkv():
-    from paged_kv_cache_44_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import paged_kv_cache_44_gb300 as P
     return P
 
