@@ -134,9 +134,9 @@ def test_permutation_invariance_bit_identical(kernel):
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_shared_prefix_equals_private_copies(kernel):
     w = W.make("qwen2.5-7b-prefix", S=12, lengths=np.array([1030, 1100, 2000, 1025, 5000, 1500, 3, 40, 700,
-                                                              1200, 90, 4000]), spare_blocks=64)
-    import dataclasses
-    w = dataclasses.replace(w, shared_seqs=6)
+                                                              1200, 90, 4000]), spare_blocks=64,
+               shared_seqs=6)
+    assert w.shared_seqs == 6 and (w.block_tables[:6, :64] == w.block_tables[0, :64]).all()
     c = build_case(w)
     if kernel not in _kernels_for(w):
         pytest.skip("kernel does not apply or is not selected")

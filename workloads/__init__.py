@@ -131,7 +131,7 @@ COW_PAIRS = 64
 
 def make(name: str, *, seed: Optional[int] = None, S: Optional[int] = None,
          lengths: Optional[np.ndarray] = None, cow_pairs: int = COW_PAIRS,
-         spare_blocks: int = 0) -> Workload:
+         spare_blocks: int = 0, shared_seqs: Optional[int] = None) -> Workload:
     """Build the structure of workload `name` (see SHAPES).
 
     Blocks are handed out from a seeded random permutation of the pool's
@@ -139,11 +139,13 @@ def make(name: str, *, seed: Optional[int] = None, S: Optional[int] = None,
     prefix blocks are allocated once and referenced by every sharer.  The
     pool has exactly the blocks in use, plus `cow_pairs` free blocks used as
     copy-on-write destinations, plus `spare_blocks`, plus the null block
-    (the tiny case uses a fixed pool of 16)."""
+    (the tiny case uses a fixed pool of 16).  `shared_seqs` overrides how
+    many leading sequences share the prefix (for prefix workloads)."""
     cfg = dict(SHAPES[name])
     seed = cfg.pop("seed") if seed is None else seed
     cfg.pop("seed", None)
-    shared_seqs = cfg.pop("shared_seqs", 0)
+    cfg_shared = cfg.pop("shared_seqs", 0)
+    shared_seqs = cfg_shared if shared_seqs is None else shared_seqs
     shared_tokens = cfg.pop("shared_tokens", 0)
     fixed_nb = cfg.pop("NB", None)
     if S is not None:
