@@ -464,10 +464,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--S", type=int, default=None, help="fewer sequences (small profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    w = W.make(args.workload)
+    w = W.make(args.workload, S=args.S) if args.S else W.make(args.workload)
     if args.impl == "reference":
         run_reference(args, w)
     else:
