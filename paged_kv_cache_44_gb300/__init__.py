@@ -24,7 +24,8 @@ from typing import Optional, Sequence
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libpkv.so")
+# PKV_LIBRARY may name another build of the same library (e.g. a tuning variant)
+LIB_PATH = os.environ.get("PKV_LIBRARY") or os.path.join(_PKG, "libpkv.so")
 
 F32, BF16, FP8_E4M3 = 0, 1, 2
 KERNELS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}

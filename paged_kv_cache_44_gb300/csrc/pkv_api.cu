@@ -151,7 +151,7 @@ pkv_status pkv_paged_attention_decode_ex(void* out, const void* query, pkv_dtype
 
     const int P = resolve_partition(S, Hq, Hkv, d, bs, max_context_len, partition_size);
     if (P < 0) return PKV_ERR_INVALID_ARG;
-    const bool tc_ok = decode_tc_supports(q_dtype, cache_dtype, d, bs);
+    const bool tc_ok = decode_tc_supports(q_dtype, cache_dtype, d, bs, NB);
     bool use_tc;
     if (kernel == PKV_DECODE_AUTO) use_tc = tc_ok;
     else if (kernel == PKV_DECODE_TENSOR_CORES) { if (!tc_ok) return PKV_ERR_UNSUPPORTED; use_tc = true; }

@@ -10,11 +10,13 @@
 // tokens).  Each warp is an independent worker: it claims units from a
 // counter in the workspace header (or takes them round-robin without one),
 // and streams the unit's K/V through its own ring of shared-memory stages.
-// A stage is 32 tokens of K and V for one K/V head: one lane per token row
-// issues two 1-D bulk copies (cp.async.bulk, the TMA engine) from the
-// physical block the table names, completing on the stage's mbarrier.  Rows
-// are padded by 16 bytes so the tensor-core operand loads are free of bank
-// conflicts.  The warp keeps up to kStages-1 stages in flight while it works
+// A stage is 32 tokens of K and V for one K/V head.  The cache is seen by
+// the TMA engine as a 2-D tensor [NB * bs rows, Hkv * d elements]; one
+// tiled copy (cp.async.bulk.tensor) moves the 128-byte half-rows of one
+// K/V head for all bs tokens of the physical block the table names, with
+// the 128-byte swizzle (64-byte for 64-byte rows) so that tensor-core
+// operand loads are free of bank conflicts.  Copies complete on the stage's
+// mbarrier.  The warp keeps up to kStages-1 stages in flight while it works
 // on one, and it prefetches across unit boundaries.
 //
 // Math per stage (mma.sync m16n8k16, fp32 accumulate):
@@ -30,7 +32,11 @@
 //
 // A unit that covers its whole sequence writes `out`; otherwise it writes
 // (m, l, unnormalised O) to the workspace for the merge kernel.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math_constants.h>
+
+#include <mutex>
 
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
@@ -38,27 +44,55 @@
 namespace pkv {
 namespace {
 
-constexpr int kWarps = 4;       // workers per CTA
-constexpr int kTok = 32;        // tokens per stage
+#ifndef PKV_TC_WARPS
+#define PKV_TC_WARPS 4
+#endif
+#ifndef PKV_TC_STAGES_BF16
+#define PKV_TC_STAGES_BF16 3
+#endif
+#ifndef PKV_TC_STAGES_FP8
+#define PKV_TC_STAGES_FP8 5
+#endif
+
+constexpr int kWarps = PKV_TC_WARPS;        // workers per CTA
+constexpr int kTok = 32;                    // tokens per stage
 constexpr int kHeadsPerUnit = 8;
 constexpr long long kWaitLimitCycles = 4000000000LL;   // ~2 s: a stage that never lands
 
 template <int D, bool FP8>
 struct Cfg {
-    static constexpr int kRowBytes = FP8 ? D : 2 * D;
-    static constexpr int kPitch = kRowBytes + 16;
-    static constexpr int kHalfBytes = kTok * kPitch;             // K (or V) part of a stage
-    static constexpr int kStageBytes = 2 * kHalfBytes;
-    static constexpr int kStages = FP8 ? 5 : 3;
+    static constexpr int kRowBytes = FP8 ? D : 2 * D;            // one token of one K/V head
+    static constexpr int kBoxRow = kRowBytes >= 128 ? 128 : kRowBytes;   // bytes per row of one TMA box
+    static constexpr int kHalves = kRowBytes / kBoxRow;         // boxes per (block, K or V)
+    static constexpr int kPartBytes = kTok * kRowBytes;         // K (or V) part of a stage
+    static constexpr int kStageBytes = 2 * kPartBytes;
+    static constexpr int kStages = FP8 ? PKV_TC_STAGES_FP8 : PKV_TC_STAGES_BF16;
     static constexpr int kQueue = kStages + 1;
-    // per-warp shared memory: stages, then barriers, masks, unit queue
+    // per-warp shared memory: stages (1024-byte aligned), barriers, masks, unit queue
     static constexpr int kBarOff = kStages * kStageBytes;
     static constexpr int kMaskOff = kBarOff + 8 * kStages;
     static constexpr int kQueueOff = (kMaskOff + 4 * kStages + 7) / 8 * 8;   // 8-byte entries
-    static constexpr int kWarpBytes = (kQueueOff + 8 * kQueue + 127) / 128 * 128;
-    static constexpr int kSmemBytes = kWarps * kWarpBytes;
+    static constexpr int kWarpBytes = (kQueueOff + 8 * kQueue + 1023) / 1024 * 1024;
+    static constexpr int kSmemBytes = kWarps * kWarpBytes + 1024;   // + room to align the base
     static constexpr int KS = D / 16;     // k-steps of the QK product, m-tiles of the PV product
+    static_assert(kStageBytes % 1024 == 0, "stages must keep the swizzle atoms aligned");
 };
+
+// Shared-memory byte address of logical byte `x` (a multiple of 16, plus an
+// offset inside the 16-byte chunk) of token row `tok` in a stage part laid
+// out by the tensor copies: rows of kBoxRow bytes, one region of kTok rows
+// per 128-byte half, 16-byte chunks permuted by the swizzle (128-byte mode:
+// chunk ^= row % 8; 64-byte mode: chunk ^= (row / 2) % 4).
+template <int RB>
+__device__ __forceinline__ uint32_t swz(uint32_t part, int tok, int x) {
+    if constexpr (RB >= 128) {
+        const int h = x >> 7, j = (x >> 4) & 7;
+        return part + h * (kTok * 128) + tok * 128 + ((j ^ (tok & 7)) << 4) + (x & 15);
+    } else {
+        const int j = (x >> 4) & 3;
+        return part + tok * 64 + ((j ^ ((tok >> 1) & 3)) << 4) + (x & 15);
+    }
+}
 
 // ------------------------------------------------------------- PTX wrappers
 
@@ -82,10 +116,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+__device__ __forceinline__ void tensor_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() {
@@ -190,18 +225,25 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, size_t idx, flo
 
 template <int D, bool FP8, typename QF>
 __global__ void __launch_bounds__(kWarps * 32, 1)
-    decode_tc_kernel(const __grid_constant__ DecodeParams p, unsigned long long total_units, int nsets) {
+    decode_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap, unsigned long long total_units, int nsets) {
     using C = Cfg<D, FP8>;
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int r = lane >> 2, c = lane & 3;     // fragment row / column-pair of this lane
+    // swizzle atoms need 1024-byte alignment: align the base ourselves
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
+    unsigned char* smem = smem_raw + (base_addr - raw_addr);
     unsigned char* ws = smem + warp * C::kWarpBytes;
-    const uint32_t ws_addr = smem_addr(ws);
+    const uint32_t ws_addr = base_addr + warp * C::kWarpBytes;
     uint32_t* masks = reinterpret_cast<uint32_t*>(ws + C::kMaskOff);
     unsigned long long* queue = reinterpret_cast<unsigned long long*>(ws + C::kQueueOff);
     auto bar = [&](int i) { return ws_addr + C::kBarOff + 8 * i; };
     auto stage_k = [&](int i) { return ws_addr + i * C::kStageBytes; };
-    auto stage_v = [&](int i) { return ws_addr + i * C::kStageBytes + C::kHalfBytes; };
+    auto stage_v = [&](int i) { return ws_addr + i * C::kStageBytes + C::kPartBytes; };
+    auto lds128 = [&](uint32_t a) { return *reinterpret_cast<const uint4*>(ws + (a - ws_addr)); };
+    auto lds64 = [&](uint32_t a) { return *reinterpret_cast<const uint2*>(ws + (a - ws_addr)); };
 
     if (lane == 0) {
         for (int i = 0; i < C::kStages; ++i) mbar_init(bar(i), 1);
@@ -212,7 +254,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const unsigned long long total_warps = (unsigned long long)gridDim.x * kWarps;
     const unsigned long long my_warp = (unsigned long long)blockIdx.x * kWarps + warp;
     unsigned long long static_next = my_warp;
-    const size_t row_elems = (size_t)p.Hkv * D;      // elements between consecutive tokens of a block
+    const int blocks_per_stage = kTok / p.bs;              // 2 (bs 16) or 1 (bs 32)
+    const uint32_t box_bytes = (uint32_t)p.bs * C::kBoxRow;
 
     // ---- issue side: claims units, fills stages
     bool claiming = true;
@@ -229,11 +272,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                     v = atomicAdd(reinterpret_cast<unsigned long long*>(p.sched), 1ull);
                 } else {
                     v = static_next;
-                    static_next += total_warps;
                 }
             }
             v = __shfl_sync(0xffffffffu, v, 0);
-            if (lane != 0 && p.sched == nullptr) static_next += total_warps;
+            static_next += total_warps;
             if (v >= total_units) return false;
             Unit x;
             if (!unit_of(p, v, nsets, x)) continue;
@@ -266,28 +308,33 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         const int slot = g_issue % C::kStages;
         const int ts = iu.t0 + i_stage * kTok;
         const int tn = min(kTok, iu.t1 - ts);
+        // per token: inside the unit and in a block with a valid id
         const int t = ts + lane;
         bool ok = lane < tn;
-        int pb = 0;
         if (ok) {
-            pb = __ldg(p.block_tables + (size_t)iu.s * p.MB + t / p.bs);
+            const int pb = __ldg(p.block_tables + (size_t)iu.s * p.MB + t / p.bs);
             if (pb < 0 || pb >= p.NB) {
                 report(p.err, PKV_DEVERR_BLOCK_ID);
                 ok = false;
             }
         }
         const uint32_t m = __ballot_sync(0xffffffffu, ok);
+        // one box per (block of the stage, K or V, 128-byte half): lane i issues box i
+        const int nbox = blocks_per_stage * 2 * C::kHalves;
+        const int b = lane / (2 * C::kHalves), kv = (lane / C::kHalves) & 1, h = lane % C::kHalves;
+        const bool block_live = lane < nbox && ((m >> (b * p.bs)) & ((p.bs == 32) ? 0xffffffffu : 0xffffu)) != 0;
+        const uint32_t nissue = __popc(__ballot_sync(0xffffffffu, block_live));
         if (lane == 0) {
             masks[slot] = m;
-            mbar_arrive_expect_tx(bar(slot), (uint32_t)__popc(m) * 2u * C::kRowBytes);
+            mbar_arrive_expect_tx(bar(slot), nissue * box_bytes);
         }
         __syncwarp();
-        if (ok) {
-            const size_t off = ((size_t)pb * p.bs + (t % p.bs)) * row_elems + (size_t)iu.kvh * D;
-            const unsigned char* kg = static_cast<const unsigned char*>(p.kc) + off * (FP8 ? 1 : 2);
-            const unsigned char* vg = static_cast<const unsigned char*>(p.vc) + off * (FP8 ? 1 : 2);
-            bulk_load(stage_k(slot) + lane * C::kPitch, kg, C::kRowBytes, bar(slot));
-            bulk_load(stage_v(slot) + lane * C::kPitch, vg, C::kRowBytes, bar(slot));
+        if (block_live) {
+            const int pb = __ldg(p.block_tables + (size_t)iu.s * p.MB + (ts + b * p.bs) / p.bs);
+            const uint32_t dst = (kv ? stage_v(slot) : stage_k(slot)) + h * (kTok * C::kBoxRow) +
+                                 b * p.bs * C::kBoxRow;
+            tensor_load_2d(dst, kv ? &vmap : &kmap, iu.kvh * D + h * (C::kBoxRow / (FP8 ? 1 : 2)), pb * p.bs,
+                           bar(slot));
         }
         ++g_issue;
         ++i_stage;
@@ -376,21 +423,19 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                 // Load both halves of both rows (odd rows start with the other
                 // half, which spreads a load over all banks), then run the
                 // MMAs in one k-step order common to every lane.
-                const unsigned char* ra = ws + (kb - ws_addr) + ta * C::kPitch + 16 * c;
-                const unsigned char* rb = ws + (kb - ws_addr) + tb * C::kPitch + 16 * c;
                 uint4 ka[D / 64], kbv[D / 64];
                 if constexpr (D == 128) {
                     const int first = (r & 1) * 64, second = 64 - first;
-                    const uint4 a0 = *reinterpret_cast<const uint4*>(ra + first);
-                    const uint4 b0 = *reinterpret_cast<const uint4*>(rb + first);
-                    const uint4 a1 = *reinterpret_cast<const uint4*>(ra + second);
-                    const uint4 b1 = *reinterpret_cast<const uint4*>(rb + second);
+                    const uint4 a0 = lds128(swz<C::kRowBytes>(kb, ta, 16 * c + first));
+                    const uint4 b0 = lds128(swz<C::kRowBytes>(kb, tb, 16 * c + first));
+                    const uint4 a1 = lds128(swz<C::kRowBytes>(kb, ta, 16 * c + second));
+                    const uint4 b1 = lds128(swz<C::kRowBytes>(kb, tb, 16 * c + second));
                     const bool odd = r & 1;
                     ka[0] = odd ? a1 : a0;  ka[1] = odd ? a0 : a1;
                     kbv[0] = odd ? b1 : b0; kbv[1] = odd ? b0 : b1;
                 } else {
-                    ka[0] = *reinterpret_cast<const uint4*>(ra);
-                    kbv[0] = *reinterpret_cast<const uint4*>(rb);
+                    ka[0] = lds128(swz<C::kRowBytes>(kb, ta, 16 * c));
+                    kbv[0] = lds128(swz<C::kRowBytes>(kb, tb, 16 * c));
                 }
 #pragma unroll
                 for (int hh = 0; hh < D / 64; ++hh) {
@@ -406,18 +451,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                 }
             } else {
                 const int mi = lane >> 3;
-                const uint32_t rowaddr = kb + (16 * mt + 8 * (mi & 1) + (lane & 7)) * C::kPitch + 16 * (mi >> 1);
+                const int tok = 16 * mt + 8 * (mi & 1) + (lane & 7);
 #pragma unroll
                 for (int ks = 0; ks < C::KS; ++ks) {
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4(rowaddr + 32 * ks, a0, a1, a2, a3);
+                    ldsm_x4(swz<C::kRowBytes>(kb, tok, 32 * ks + 16 * (mi >> 1)), a0, a1, a2, a3);
                     mma16816<false>(sacc[mt], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
                 }
             }
         }
 
         // ---- online softmax over the stage's 32 tokens (log2 units)
-        // token of accumulator rows: (mt, row r) and (mt, row r+8)
         float x[2][4];
         float cmax0 = -CUDART_INF_F, cmax1 = -CUDART_INF_F;
 #pragma unroll
@@ -479,15 +523,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                 uint32_t w[4][D / 32];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const unsigned char* row = ws + (vb - ws_addr) + (16 * kt + 4 * c + j) * C::kPitch + (D / 8) * r;
+                    const int tok = 16 * kt + 4 * c + j;
                     if constexpr (D == 128) {
-                        const uint4 v4 = *reinterpret_cast<const uint4*>(row);
+                        const uint4 v4 = lds128(swz<C::kRowBytes>(vb, tok, 16 * r));
                         w[j][0] = v4.x; w[j][1] = v4.y; w[j][2] = v4.z; w[j][3] = v4.w;
                     } else {
-                        const uint2 v2 = *reinterpret_cast<const uint2*>(row);
+                        const uint2 v2 = lds64(swz<C::kRowBytes>(vb, tok, 8 * r));
                         w[j][0] = v2.x; w[j][1] = v2.y;
                     }
-                    if (!full && !((vmask >> (16 * kt + 4 * c + j)) & 1u)) {
+                    if (!full && !((vmask >> tok) & 1u)) {
 #pragma unroll
                         for (int q = 0; q < D / 32; ++q) w[j][q] = 0u;
                     }
@@ -504,7 +548,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                 }
             } else {
                 const int mi = lane >> 3;
-                const uint32_t rowaddr = vb + (16 * kt + 8 * (mi >> 1) + (lane & 7)) * C::kPitch + 16 * (mi & 1);
+                const int tok = 16 * kt + 8 * (mi >> 1) + (lane & 7);
                 const int tk0 = 16 * kt + 2 * c;     // tokens of a0a1/a2a3: tk0, tk0+1; of a4a5/a6a7: +8
                 const uint32_t keep01 = (vmask >> tk0) & 3u, keep89 = (vmask >> (tk0 + 8)) & 3u;
                 const uint32_t mlo = (keep01 & 1u ? 0x0000ffffu : 0u) | (keep01 & 2u ? 0xffff0000u : 0u);
@@ -512,7 +556,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 #pragma unroll
                 for (int t = 0; t < C::KS; ++t) {
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4_t(rowaddr + 32 * t, a0, a1, a2, a3);
+                    ldsm_x4_t(swz<C::kRowBytes>(vb, tok, 32 * t + 16 * (mi & 1)), a0, a1, a2, a3);
                     if (!full) {
                         a0 &= mlo; a1 &= mlo; a2 &= mhi; a3 &= mhi;
                     }
@@ -582,6 +626,42 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
 }
 
+// ------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// The cache [NB, bs, Hkv, d] as a 2-D tensor: rows = NB * bs tokens, row
+// length = Hkv * d elements; a box is (one 128-byte half-row of one K/V
+// head) x (the bs tokens of one block).
+template <int D, bool FP8>
+bool encode_cache_map(CUtensorMap* map, const void* base, const DecodeParams& p) {
+    using C = Cfg<D, FP8>;
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const int esize = FP8 ? 1 : 2;
+    const cuuint64_t dims[2] = {(cuuint64_t)p.Hkv * D, (cuuint64_t)p.NB * p.bs};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.Hkv * D * esize};
+    const cuuint32_t box[2] = {(cuuint32_t)(C::kBoxRow / esize), (cuuint32_t)p.bs};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle sw = C::kBoxRow == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const CUresult rc = fn(map, FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return rc == CUDA_SUCCESS;
+}
+
 template <int D, bool FP8, typename QF>
 cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t st) {
     using C = Cfg<D, FP8>;
@@ -596,19 +676,23 @@ cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
+    CUtensorMap kmap, vmap;
+    if (!encode_cache_map<D, FP8>(&kmap, p.kc, p) || !encode_cache_map<D, FP8>(&vmap, p.vc, p))
+        return cudaErrorInvalidValue;
     const int nsets = (p.g + kHeadsPerUnit - 1) / kHeadsPerUnit;
     const unsigned long long units = (unsigned long long)p.Pmax * p.S * p.Hkv * nsets;
     unsigned long long want = (units + kWarps - 1) / kWarps;
     int grid = (int)(want < (unsigned long long)num_sms ? want : (unsigned long long)num_sms);
     if (grid < 1) grid = 1;
-    kern<<<grid, kWarps * 32, C::kSmemBytes, st>>>(p, units, nsets);
+    kern<<<grid, kWarps * 32, C::kSmemBytes, st>>>(p, kmap, vmap, units, nsets);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-bool decode_tc_supports(pkv_dtype q_dt, pkv_dtype c_dt, int d, int bs) {
+bool decode_tc_supports(pkv_dtype q_dt, pkv_dtype c_dt, int d, int bs, int NB) {
     if (!(d == 64 || d == 128) || !(bs == 16 || bs == 32)) return false;
+    if ((long long)NB * bs >= (1LL << 31)) return false;      // TMA row coordinates are 32-bit
     if (c_dt == PKV_BF16) return q_dt == PKV_BF16;
     return c_dt == PKV_FP8_E4M3 && (q_dt == PKV_BF16 || q_dt == PKV_F32);
 }

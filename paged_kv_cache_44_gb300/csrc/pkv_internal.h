@@ -67,6 +67,6 @@ cudaError_t launch_decode_simt(const DecodeParams& p, pkv_dtype q_dt, pkv_dtype 
 cudaError_t launch_decode_tc(const DecodeParams& p, pkv_dtype q_dt, pkv_dtype c_dt, int num_sms,
                              cudaStream_t st);
 cudaError_t launch_decode_reduce(const DecodeParams& p, pkv_dtype q_dt, cudaStream_t st);
-bool decode_tc_supports(pkv_dtype q_dt, pkv_dtype c_dt, int d, int bs);
+bool decode_tc_supports(pkv_dtype q_dt, pkv_dtype c_dt, int d, int bs, int NB);
 
 }  // namespace pkv
