@@ -44,38 +44,53 @@
 namespace pkv {
 namespace {
 
-#ifndef PKV_TC_WARPS
-#define PKV_TC_WARPS 4
+// Tuning knobs: workers per CTA, stages per worker, tokens per stage, for
+// bf16 and for E4M3 caches (E4M3 does more arithmetic per byte and wants
+// more workers).
+#ifndef PKV_TC_WARPS_BF16
+#define PKV_TC_WARPS_BF16 6
 #endif
 #ifndef PKV_TC_STAGES_BF16
-#define PKV_TC_STAGES_BF16 3
+#define PKV_TC_STAGES_BF16 2
+#endif
+#ifndef PKV_TC_TOK_BF16
+#define PKV_TC_TOK_BF16 32
+#endif
+#ifndef PKV_TC_WARPS_FP8
+#define PKV_TC_WARPS_FP8 12
 #endif
 #ifndef PKV_TC_STAGES_FP8
-#define PKV_TC_STAGES_FP8 5
+#define PKV_TC_STAGES_FP8 2
+#endif
+#ifndef PKV_TC_TOK_FP8
+#define PKV_TC_TOK_FP8 32
 #endif
 
-constexpr int kWarps = PKV_TC_WARPS;        // workers per CTA
-constexpr int kTok = 32;                    // tokens per stage
 constexpr int kHeadsPerUnit = 8;
 constexpr long long kWaitLimitCycles = 4000000000LL;   // ~2 s: a stage that never lands
 
 template <int D, bool FP8>
 struct Cfg {
+    static constexpr int kWarps = FP8 ? PKV_TC_WARPS_FP8 : PKV_TC_WARPS_BF16;     // workers per CTA
+    static constexpr int kStages = FP8 ? PKV_TC_STAGES_FP8 : PKV_TC_STAGES_BF16;  // ring depth per worker
+    static constexpr int kTok = FP8 ? PKV_TC_TOK_FP8 : PKV_TC_TOK_BF16;          // tokens per stage
+    static constexpr int kMT = kTok / 16;                        // 16-token m-tiles per stage
     static constexpr int kRowBytes = FP8 ? D : 2 * D;            // one token of one K/V head
     static constexpr int kBoxRow = kRowBytes >= 128 ? 128 : kRowBytes;   // bytes per row of one TMA box
     static constexpr int kHalves = kRowBytes / kBoxRow;         // boxes per (block, K or V)
     static constexpr int kPartBytes = kTok * kRowBytes;         // K (or V) part of a stage
     static constexpr int kStageBytes = 2 * kPartBytes;
-    static constexpr int kStages = FP8 ? PKV_TC_STAGES_FP8 : PKV_TC_STAGES_BF16;
     static constexpr int kQueue = kStages + 1;
-    // per-warp shared memory: stages (1024-byte aligned), barriers, masks, unit queue
-    static constexpr int kBarOff = kStages * kStageBytes;
-    static constexpr int kMaskOff = kBarOff + 8 * kStages;
-    static constexpr int kQueueOff = (kMaskOff + 4 * kStages + 7) / 8 * 8;   // 8-byte entries
-    static constexpr int kWarpBytes = (kQueueOff + 8 * kQueue + 1023) / 1024 * 1024;
-    static constexpr int kSmemBytes = kWarps * kWarpBytes + 1024;   // + room to align the base
+    // shared memory: every worker's stages (1024-byte aligned), then one
+    // trailer with each worker's barriers, stage masks and unit queue
+    static constexpr int kWarpBytes = kStages * kStageBytes;
+    static constexpr int kCtlBytes = (8 * kStages + 4 * kStages + 7) / 8 * 8 + 8 * kQueue;
+    static constexpr int kCtlOff = kWarps * kWarpBytes;
+    static constexpr int kSmemBytes = kCtlOff + kWarps * kCtlBytes + 1024;   // + room to align the base
     static constexpr int KS = D / 16;     // k-steps of the QK product, m-tiles of the PV product
-    static_assert(kStageBytes % 1024 == 0, "stages must keep the swizzle atoms aligned");
+    static_assert(kTok == 16 || kTok == 32, "stages hold 16 or 32 tokens");
+    static_assert(kStageBytes % 1024 == 0 || kRowBytes < 128, "stages must keep the swizzle atoms aligned");
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 // Shared-memory byte address of logical byte `x` (a multiple of 16, plus an
@@ -83,11 +98,11 @@ struct Cfg {
 // out by the tensor copies: rows of kBoxRow bytes, one region of kTok rows
 // per 128-byte half, 16-byte chunks permuted by the swizzle (128-byte mode:
 // chunk ^= row % 8; 64-byte mode: chunk ^= (row / 2) % 4).
-template <int RB>
+template <int RB, int TOK>
 __device__ __forceinline__ uint32_t swz(uint32_t part, int tok, int x) {
     if constexpr (RB >= 128) {
         const int h = x >> 7, j = (x >> 4) & 7;
-        return part + h * (kTok * 128) + tok * 128 + ((j ^ (tok & 7)) << 4) + (x & 15);
+        return part + h * (TOK * 128) + tok * 128 + ((j ^ (tok & 7)) << 4) + (x & 15);
     } else {
         const int j = (x >> 4) & 3;
         return part + tok * 64 + ((j ^ ((tok >> 1) & 3)) << 4) + (x & 15);
@@ -224,7 +239,7 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, size_t idx, flo
 // ------------------------------------------------------------------ kernel
 
 template <int D, bool FP8, typename QF>
-__global__ void __launch_bounds__(kWarps * 32, 1)
+__global__ void __launch_bounds__(Cfg<D, FP8>::kWarps * 32, 1)
     decode_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, unsigned long long total_units, int nsets) {
     using C = Cfg<D, FP8>;
@@ -235,11 +250,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
     unsigned char* smem = smem_raw + (base_addr - raw_addr);
+    constexpr int kWarps = C::kWarps, kTok = C::kTok;
     unsigned char* ws = smem + warp * C::kWarpBytes;
     const uint32_t ws_addr = base_addr + warp * C::kWarpBytes;
-    uint32_t* masks = reinterpret_cast<uint32_t*>(ws + C::kMaskOff);
-    unsigned long long* queue = reinterpret_cast<unsigned long long*>(ws + C::kQueueOff);
-    auto bar = [&](int i) { return ws_addr + C::kBarOff + 8 * i; };
+    unsigned char* ctl = smem + C::kCtlOff + warp * C::kCtlBytes;
+    const uint32_t ctl_addr = base_addr + C::kCtlOff + warp * C::kCtlBytes;
+    uint32_t* masks = reinterpret_cast<uint32_t*>(ctl + 8 * C::kStages);
+    unsigned long long* queue =
+        reinterpret_cast<unsigned long long*>(ctl + (8 * C::kStages + 4 * C::kStages + 7) / 8 * 8);
+    auto bar = [&](int i) { return ctl_addr + 8 * i; };
     auto stage_k = [&](int i) { return ws_addr + i * C::kStageBytes; };
     auto stage_v = [&](int i) { return ws_addr + i * C::kStageBytes + C::kPartBytes; };
     auto lds128 = [&](uint32_t a) { return *reinterpret_cast<const uint4*>(ws + (a - ws_addr)); };
@@ -254,8 +273,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const unsigned long long total_warps = (unsigned long long)gridDim.x * kWarps;
     const unsigned long long my_warp = (unsigned long long)blockIdx.x * kWarps + warp;
     unsigned long long static_next = my_warp;
-    const int blocks_per_stage = kTok / p.bs;              // 2 (bs 16) or 1 (bs 32)
-    const uint32_t box_bytes = (uint32_t)p.bs * C::kBoxRow;
+    const int box_rows = min(p.bs, kTok);                  // tokens one box covers
+    const int boxes_per_stage = kTok / box_rows;           // 2 (bs 16, 32-token stages) or 1
+    const uint32_t box_bytes = (uint32_t)box_rows * C::kBoxRow;
 
     // ---- issue side: claims units, fills stages
     bool claiming = true;
@@ -319,22 +339,24 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             }
         }
         const uint32_t m = __ballot_sync(0xffffffffu, ok);
-        // one box per (block of the stage, K or V, 128-byte half): lane i issues box i
-        const int nbox = blocks_per_stage * 2 * C::kHalves;
+        // one box per (box_rows tokens of the stage, K or V, 128-byte half): lane i issues box i
+        const int nbox = boxes_per_stage * 2 * C::kHalves;
         const int b = lane / (2 * C::kHalves), kv = (lane / C::kHalves) & 1, h = lane % C::kHalves;
-        const bool block_live = lane < nbox && ((m >> (b * p.bs)) & ((p.bs == 32) ? 0xffffffffu : 0xffffu)) != 0;
-        const uint32_t nissue = __popc(__ballot_sync(0xffffffffu, block_live));
+        const uint32_t rows_mask = box_rows == 32 ? 0xffffffffu : 0xffffu;
+        const bool box_live = lane < nbox && ((m >> (b * box_rows)) & rows_mask) != 0;
+        const uint32_t nissue = __popc(__ballot_sync(0xffffffffu, box_live));
         if (lane == 0) {
             masks[slot] = m;
             mbar_arrive_expect_tx(bar(slot), nissue * box_bytes);
         }
         __syncwarp();
-        if (block_live) {
-            const int pb = __ldg(p.block_tables + (size_t)iu.s * p.MB + (ts + b * p.bs) / p.bs);
+        if (box_live) {
+            const int t0b = ts + b * box_rows;                 // first token of the box
+            const int pb = __ldg(p.block_tables + (size_t)iu.s * p.MB + t0b / p.bs);
             const uint32_t dst = (kv ? stage_v(slot) : stage_k(slot)) + h * (kTok * C::kBoxRow) +
-                                 b * p.bs * C::kBoxRow;
-            tensor_load_2d(dst, kv ? &vmap : &kmap, iu.kvh * D + h * (C::kBoxRow / (FP8 ? 1 : 2)), pb * p.bs,
-                           bar(slot));
+                                 b * box_rows * C::kBoxRow;
+            tensor_load_2d(dst, kv ? &vmap : &kmap, iu.kvh * D + h * (C::kBoxRow / (FP8 ? 1 : 2)),
+                           pb * p.bs + t0b % p.bs, bar(slot));
         }
         ++g_issue;
         ++i_stage;
@@ -410,10 +432,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         const uint32_t vmask = masks[slot];
         const uint32_t kb = stage_k(slot), vb = stage_v(slot);
 
-        // ---- S^T = K . Q^T for the two 16-token m-tiles of the stage
-        float sacc[2][4];
+        // ---- S^T = K . Q^T for the 16-token m-tiles of the stage
+        float sacc[C::kMT][4];
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
+        for (int mt = 0; mt < C::kMT; ++mt) {
             sacc[mt][0] = sacc[mt][1] = sacc[mt][2] = sacc[mt][3] = 0.f;
             if constexpr (FP8) {
                 // rows of this lane: tokens pi(r) and pi(r+8) of the m-tile,
@@ -426,16 +448,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                 uint4 ka[D / 64], kbv[D / 64];
                 if constexpr (D == 128) {
                     const int first = (r & 1) * 64, second = 64 - first;
-                    const uint4 a0 = lds128(swz<C::kRowBytes>(kb, ta, 16 * c + first));
-                    const uint4 b0 = lds128(swz<C::kRowBytes>(kb, tb, 16 * c + first));
-                    const uint4 a1 = lds128(swz<C::kRowBytes>(kb, ta, 16 * c + second));
-                    const uint4 b1 = lds128(swz<C::kRowBytes>(kb, tb, 16 * c + second));
+                    const uint4 a0 = lds128(swz<C::kRowBytes, C::kTok>(kb, ta, 16 * c + first));
+                    const uint4 b0 = lds128(swz<C::kRowBytes, C::kTok>(kb, tb, 16 * c + first));
+                    const uint4 a1 = lds128(swz<C::kRowBytes, C::kTok>(kb, ta, 16 * c + second));
+                    const uint4 b1 = lds128(swz<C::kRowBytes, C::kTok>(kb, tb, 16 * c + second));
                     const bool odd = r & 1;
                     ka[0] = odd ? a1 : a0;  ka[1] = odd ? a0 : a1;
                     kbv[0] = odd ? b1 : b0; kbv[1] = odd ? b0 : b1;
                 } else {
-                    ka[0] = lds128(swz<C::kRowBytes>(kb, ta, 16 * c));
-                    kbv[0] = lds128(swz<C::kRowBytes>(kb, tb, 16 * c));
+                    ka[0] = lds128(swz<C::kRowBytes, C::kTok>(kb, ta, 16 * c));
+                    kbv[0] = lds128(swz<C::kRowBytes, C::kTok>(kb, tb, 16 * c));
                 }
 #pragma unroll
                 for (int hh = 0; hh < D / 64; ++hh) {
@@ -455,17 +477,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 #pragma unroll
                 for (int ks = 0; ks < C::KS; ++ks) {
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4(swz<C::kRowBytes>(kb, tok, 32 * ks + 16 * (mi >> 1)), a0, a1, a2, a3);
+                    ldsm_x4(swz<C::kRowBytes, C::kTok>(kb, tok, 32 * ks + 16 * (mi >> 1)), a0, a1, a2, a3);
                     mma16816<false>(sacc[mt], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
                 }
             }
         }
 
-        // ---- online softmax over the stage's 32 tokens (log2 units)
-        float x[2][4];
+        // ---- online softmax over the stage's tokens (log2 units)
+        float x[C::kMT][4];
         float cmax0 = -CUDART_INF_F, cmax1 = -CUDART_INF_F;
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
+        for (int mt = 0; mt < C::kMT; ++mt) {
             int ta, tb;
             if constexpr (FP8) {
                 ta = 16 * mt + 4 * (r >> 1) + (r & 1);
@@ -494,9 +516,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         m_run[0] = mn0;
         m_run[1] = mn1;
         float ls0 = 0.f, ls1 = 0.f;
-        uint32_t pb[2][2];                 // P^T B-fragments for the two k-tiles
+        uint32_t pb[C::kMT][2];            // P^T B-fragments, one pair per 16-token k-tile
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
+        for (int mt = 0; mt < C::kMT; ++mt) {
             const float p0 = fast_exp2(x[mt][0] - mu0), p1 = fast_exp2(x[mt][1] - mu1);
             const float p2 = fast_exp2(x[mt][2] - mu0), p3 = fast_exp2(x[mt][3] - mu1);
             ls0 += p0 + p2;
@@ -515,9 +537,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         }
 
         // ---- O^T += V^T . P^T
-        const bool full = vmask == 0xffffffffu;
+        const bool full = vmask == (kTok == 32 ? 0xffffffffu : 0xffffu);
 #pragma unroll
-        for (int kt = 0; kt < 2; ++kt) {
+        for (int kt = 0; kt < C::kMT; ++kt) {
             if constexpr (FP8) {
                 // this lane's tokens: 16kt + 4c + j, bytes [D/8 * r, D/8 * (r+1)) of each row
                 uint32_t w[4][D / 32];
@@ -525,10 +547,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                 for (int j = 0; j < 4; ++j) {
                     const int tok = 16 * kt + 4 * c + j;
                     if constexpr (D == 128) {
-                        const uint4 v4 = lds128(swz<C::kRowBytes>(vb, tok, 16 * r));
+                        const uint4 v4 = lds128(swz<C::kRowBytes, C::kTok>(vb, tok, 16 * r));
                         w[j][0] = v4.x; w[j][1] = v4.y; w[j][2] = v4.z; w[j][3] = v4.w;
                     } else {
-                        const uint2 v2 = lds64(swz<C::kRowBytes>(vb, tok, 8 * r));
+                        const uint2 v2 = lds64(swz<C::kRowBytes, C::kTok>(vb, tok, 8 * r));
                         w[j][0] = v2.x; w[j][1] = v2.y;
                     }
                     if (!full && !((vmask >> tok) & 1u)) {
@@ -556,7 +578,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 #pragma unroll
                 for (int t = 0; t < C::KS; ++t) {
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4_t(swz<C::kRowBytes>(vb, tok, 32 * t + 16 * (mi & 1)), a0, a1, a2, a3);
+                    ldsm_x4_t(swz<C::kRowBytes, C::kTok>(vb, tok, 32 * t + 16 * (mi & 1)), a0, a1, a2, a3);
                     if (!full) {
                         a0 &= mlo; a1 &= mlo; a2 &= mhi; a3 &= mhi;
                     }
@@ -644,7 +666,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // The cache [NB, bs, Hkv, d] as a 2-D tensor: rows = NB * bs tokens, row
 // length = Hkv * d elements; a box is (one 128-byte half-row of one K/V
-// head) x (the bs tokens of one block).
+// head) x (min(bs, tokens per stage) consecutive tokens of one block).
 template <int D, bool FP8>
 bool encode_cache_map(CUtensorMap* map, const void* base, const DecodeParams& p) {
     using C = Cfg<D, FP8>;
@@ -653,7 +675,7 @@ bool encode_cache_map(CUtensorMap* map, const void* base, const DecodeParams& p)
     const int esize = FP8 ? 1 : 2;
     const cuuint64_t dims[2] = {(cuuint64_t)p.Hkv * D, (cuuint64_t)p.NB * p.bs};
     const cuuint64_t strides[1] = {(cuuint64_t)p.Hkv * D * esize};
-    const cuuint32_t box[2] = {(cuuint32_t)(C::kBoxRow / esize), (cuuint32_t)p.bs};
+    const cuuint32_t box[2] = {(cuuint32_t)(C::kBoxRow / esize), (cuuint32_t)(p.bs < C::kTok ? p.bs : C::kTok)};
     const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapSwizzle sw = C::kBoxRow == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     const CUresult rc = fn(map, FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
@@ -681,10 +703,10 @@ cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t st) {
         return cudaErrorInvalidValue;
     const int nsets = (p.g + kHeadsPerUnit - 1) / kHeadsPerUnit;
     const unsigned long long units = (unsigned long long)p.Pmax * p.S * p.Hkv * nsets;
-    unsigned long long want = (units + kWarps - 1) / kWarps;
+    unsigned long long want = (units + C::kWarps - 1) / C::kWarps;
     int grid = (int)(want < (unsigned long long)num_sms ? want : (unsigned long long)num_sms);
     if (grid < 1) grid = 1;
-    kern<<<grid, kWarps * 32, C::kSmemBytes, st>>>(p, kmap, vmap, units, nsets);
+    kern<<<grid, C::kWarps * 32, C::kSmemBytes, st>>>(p, kmap, vmap, units, nsets);
     return cudaGetLastError();
 }
 
