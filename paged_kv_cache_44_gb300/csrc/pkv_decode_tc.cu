@@ -57,7 +57,7 @@ namespace {
 #define PKV_TC_TOK_BF16 32
 #endif
 #ifndef PKV_TC_WARPS_FP8
-#define PKV_TC_WARPS_FP8 12
+#define PKV_TC_WARPS_FP8 8
 #endif
 #ifndef PKV_TC_STAGES_FP8
 #define PKV_TC_STAGES_FP8 2
