@@ -13,11 +13,11 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 // Units of work (sequence x K/V head x head-set x partition) the default
 // partition size aims for, counted as if every sequence had the maximum
-// length: about eight per worker warp of a full GB300 (152 SMs x 8 warps),
+// length: about four per worker warp of a full GB300 (152 SMs x 8 warps),
 // so that dynamic scheduling evens out ragged lengths and the last units to
 // finish are short next to the whole launch.  It depends on no dtype, so the
 // workspace size and the launch always agree.
-constexpr long long kTargetUnits = 152LL * 8 * 8;
+constexpr long long kTargetUnits = 152LL * 8 * 4;
 constexpr int kMinDefaultPartition = 256;
 constexpr int kHeadSet = 8;
 
