@@ -214,6 +214,54 @@ PKV_API pkv_status pkv_copy_blocks(void* const* key_caches, void* const* value_c
                            const int64_t* block_mapping, int P, int NB, size_t block_bytes,
                            int32_t* err_word, pkv_stream_t stream);
 
+/*
+ * Bytes of fixed device scratch behind pkv_paged_attention_decode_static
+ * (32 MiB).
+ */
+#define PKV_STATIC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * pkv_paged_attention_decode_static -- the same decode, for callers that
+ * cannot allocate device memory.
+ *
+ * This call has no counterpart on the pages: it is a convenience of this
+ * library.  pkv_paged_attention_decode needs a workspace that its caller
+ * allocates.  Some callers cannot allocate device memory where they decode:
+ * an engine that reserves all of its memory at start-up and forbids later
+ * allocations, a latency-critical loop that must not wait on the allocator,
+ * a foreign-language caller that holds raw pointers but no allocator.  This
+ * entry point takes the same arguments minus the workspace and allocates
+ * nothing: its scratch is a fixed array of PKV_STATIC_SCRATCH_BYTES in
+ * device memory that the library defines at file scope.  Every GPU that
+ * loads the library holds that array until the process exits.  The caller
+ * still passes and owns every input and output.
+ *
+ * Limits and behaviour:
+ *  - The scratch the call needs is pkv_decode_workspace_size(...) for the
+ *    same sizes and partition request.  If that exceeds
+ *    PKV_STATIC_SCRATCH_BYTES the call returns PKV_ERR_WORKSPACE and
+ *    enqueues nothing; a larger partition_size needs less scratch.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - Each call clears the array's 256-byte work-counter header on `stream`
+ *    (a memset) before the decode; the rest keeps the previous call's
+ *    contents and needs no clearing.
+ *  - All calls share the one array per device: two calls whose work may
+ *    overlap on the GPU (different streams, or different host threads)
+ *    race and give wrong results.  Serialise them.
+ *  - The call makes no cudaMalloc or cudaFree and no other allocating call.
+ */
+PKV_API pkv_status pkv_paged_attention_decode_static(void* out, const void* query, pkv_dtype q_dtype,
+                                                     const void* key_cache, const void* value_cache,
+                                                     pkv_dtype cache_dtype,
+                                                     const int32_t* block_tables, int MB,
+                                                     const int32_t* context_lens, int S, int max_context_len,
+                                                     int Hq, int Hkv, int d, int bs, int NB,
+                                                     float scale, float k_scale, float v_scale,
+                                                     int partition_size,
+                                                     int32_t* err_word, pkv_stream_t stream);
+
 /* Static, human-readable text for a status. */
 PKV_API const char* pkv_status_string(pkv_status status);
 

@@ -34,7 +34,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported dtype or shape",
 
 EXPORTED = ("pkv_paged_kv_write", "pkv_decode_workspace_size", "pkv_decode_partition_size",
             "pkv_paged_attention_decode", "pkv_paged_attention_decode_ex", "pkv_copy_blocks",
-            "pkv_status_string", "pkv_version")
+            "pkv_status_string", "pkv_version", "pkv_paged_attention_decode_static")
+STATIC_SCRATCH_BYTES = 32 << 20
 
 
 class PkvError(RuntimeError):
@@ -63,6 +64,8 @@ def _load() -> ctypes.CDLL:
     lib.pkv_paged_attention_decode.restype = i32
     lib.pkv_paged_attention_decode_ex.argtypes = dec + [i32]
     lib.pkv_paged_attention_decode_ex.restype = i32
+    lib.pkv_paged_attention_decode_static.argtypes = dec[:20] + [vp, vp]
+    lib.pkv_paged_attention_decode_static.restype = i32
     lib.pkv_copy_blocks.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32, vp, i32, i32, sz, vp, vp]
     lib.pkv_copy_blocks.restype = i32
     lib.pkv_status_string.argtypes = [i32]
@@ -170,6 +173,30 @@ def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
         dtype_code(key_cache.dtype), _ptr(block_tables), MB, _ptr(context_lens), S, int(max_context_len),
         Hq, Hkv, d, bs, NB, float(scale), float(k_scale), float(v_scale), int(partition_size),
         ws_ptr, ws_bytes, _ptr(err_word), _stream(stream), KERNELS[kernel]))
+    return out
+
+
+def paged_attention_decode_static(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                                  value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                  max_context_len: int, scale: Optional[float] = None, k_scale: float = 1.0,
+                                  v_scale: float = 1.0, partition_size: int = 0,
+                                  err_word: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """paged_attention_decode without a workspace: the library's fixed device
+    scratch (STATIC_SCRATCH_BYTES per GPU) stands in for it, so nothing is
+    allocated.  Calls that may overlap on the GPU must not use it together."""
+    S, Hq, d = query.shape
+    NB, bs, Hkv, d2 = key_cache.shape
+    if d2 != d or out.shape != query.shape or out.dtype != query.dtype or value_cache.shape != key_cache.shape:
+        raise ValueError("shape or dtype mismatch")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 or block_tables.dim() != 2:
+        raise ValueError("block_tables and context_lens must be int32")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check("paged_attention_decode_static", lib.pkv_paged_attention_decode_static(
+        _ptr(out), _ptr(query), dtype_code(query.dtype), _ptr(key_cache), _ptr(value_cache),
+        dtype_code(key_cache.dtype), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), S,
+        int(max_context_len), Hq, Hkv, d, bs, NB, float(scale), float(k_scale), float(v_scale),
+        int(partition_size), _ptr(err_word), _stream(stream)))
     return out
 
 
