@@ -69,7 +69,7 @@ namespace {
 constexpr int kHeadsPerUnit = 8;
 constexpr long long kWaitLimitCycles = 4000000000LL;   // ~2 s: a stage that never lands
 
-template <int D, bool FP8>
+template <int D, bool FP8, int QB>
 struct Cfg {
     static constexpr int kWarps = FP8 ? PKV_TC_WARPS_FP8 : PKV_TC_WARPS_BF16;     // workers per CTA
     static constexpr int kStages = FP8 ? PKV_TC_STAGES_FP8 : PKV_TC_STAGES_BF16;  // ring depth per worker
@@ -80,10 +80,16 @@ struct Cfg {
     static constexpr int kHalves = kRowBytes / kBoxRow;         // boxes per (block, K or V)
     static constexpr int kPartBytes = kTok * kRowBytes;         // K (or V) part of a stage
     static constexpr int kStageBytes = 2 * kPartBytes;
-    static constexpr int kQueue = kStages + 1;
-    // shared memory: every worker's stages (1024-byte aligned), then one
-    // trailer with each worker's barriers, stage masks and unit queue
-    static constexpr int kWarpBytes = kStages * kStageBytes;
+    // queued units (claimed, first stage issued, not yet started): at most
+    // one per stage in flight
+    static constexpr int kQueue = kStages;
+    // each queued unit's query rows (up to 8 heads) land in a slot of their own
+    static constexpr int kQSlotBytes = kHeadsPerUnit * D * QB;
+    // shared memory: every worker's stages and query slots (1024-byte
+    // aligned), then one trailer with each worker's barriers, stage masks and
+    // unit queue
+    static constexpr int kQOff = kStages * kStageBytes;
+    static constexpr int kWarpBytes = (kQOff + kQueue * kQSlotBytes + 1023) / 1024 * 1024;
     static constexpr int kCtlBytes = (8 * kStages + 4 * kStages + 7) / 8 * 8 + 8 * kQueue;
     static constexpr int kCtlOff = kWarps * kWarpBytes;
     static constexpr int kSmemBytes = kCtlOff + kWarps * kCtlBytes + 1024;   // + room to align the base
@@ -130,6 +136,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
 }
 __device__ __forceinline__ void tensor_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
     asm volatile(
@@ -239,10 +251,10 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, size_t idx, flo
 // ------------------------------------------------------------------ kernel
 
 template <int D, bool FP8, typename QF>
-__global__ void __launch_bounds__(Cfg<D, FP8>::kWarps * 32, 1)
+__global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
     decode_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, unsigned long long total_units, int nsets) {
-    using C = Cfg<D, FP8>;
+    using C = Cfg<D, FP8, QF::bytes>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int r = lane >> 2, c = lane & 3;     // fragment row / column-pair of this lane
@@ -281,7 +293,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::kWarps * 32, 1)
     bool claiming = true;
     bool i_have = false;
     Unit iu{};
-    int i_stage = 0, i_nst = 0;
+    int i_stage = 0, i_nst = 0, i_qslot = 0;
     unsigned g_issue = 0, q_tail = 0;
 
     auto claim = [&](unsigned long long& u) -> bool {
@@ -319,12 +331,15 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::kWarps * 32, 1)
                 return false;
             }
             unit_of(p, u, nsets, iu);
-            if (lane == 0) queue[q_tail % C::kQueue] = u;
+            i_qslot = q_tail % C::kQueue;
+            if (lane == 0) queue[i_qslot] = u;
             ++q_tail;
             i_have = true;
             i_stage = 0;
             i_nst = (iu.t1 - iu.t0 + kTok - 1) / kTok;
         }
+        // the unit's query rows ride on its first stage
+        const uint32_t q_bytes = i_stage == 0 ? (uint32_t)(iu.nh * D * QF::bytes) : 0u;
         const int slot = g_issue % C::kStages;
         const int ts = iu.t0 + i_stage * kTok;
         const int tn = min(kTok, iu.t1 - ts);
@@ -347,7 +362,11 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::kWarps * 32, 1)
         const uint32_t nissue = __popc(__ballot_sync(0xffffffffu, box_live));
         if (lane == 0) {
             masks[slot] = m;
-            mbar_arrive_expect_tx(bar(slot), nissue * box_bytes);
+            mbar_arrive_expect_tx(bar(slot), nissue * box_bytes + q_bytes);
+            if (q_bytes)
+                bulk_load(ws_addr + C::kQOff + i_qslot * C::kQSlotBytes,
+                          static_cast<const unsigned char*>(p.q) + ((size_t)iu.s * p.Hq + iu.h0) * D * QF::bytes,
+                          q_bytes, bar(slot));
         }
         __syncwarp();
         if (box_live) {
@@ -365,9 +384,9 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::kWarps * 32, 1)
 
     // ---- consume side
     unsigned g_cons = 0, q_head = 0;
-    bool have_unit = false;
+    bool have_unit = false, need_q = false;
     Unit cu{};
-    int c_stage = 0, c_nst = 0;
+    int c_stage = 0, c_nst = 0, c_qslot = 0;
     uint32_t qf[C::KS][2];                // Q^T fragments (n = head r)
     float o[C::KS][4];                    // O^T accumulators, m-tile t of d
     float m_run[2], l_run[2];             // heads 2c, 2c+1
@@ -387,29 +406,8 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::kWarps * 32, 1)
             c_stage = 0;
             c_nst = (cu.t1 - cu.t0 + kTok - 1) / kTok;
             have_unit = true;
-            // Q^T fragments of head r (zero past the unit's heads)
-            const bool hv = r < cu.nh;
-            const size_t qrow = ((size_t)cu.s * p.Hq + cu.h0 + (hv ? r : 0)) * D;
-#pragma unroll
-            for (int ks = 0; ks < C::KS; ++ks) {
-                int d0, d1;
-                if constexpr (FP8) {
-                    d0 = 64 * (ks / 4) + 16 * c + 4 * (ks % 4);      // 4 consecutive d: j = 0..3
-                    d1 = d0 + 2;
-                } else {
-                    d0 = 16 * ks + 2 * c;
-                    d1 = d0 + 8;
-                }
-                float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-                if (hv) {
-                    x0 = load_elem<QF>(p.q, qrow + d0);
-                    x1 = load_elem<QF>(p.q, qrow + d0 + 1);
-                    x2 = load_elem<QF>(p.q, qrow + d1);
-                    x3 = load_elem<QF>(p.q, qrow + d1 + 1);
-                }
-                qf[ks][0] = pack2<FP8>(x0, x1);
-                qf[ks][1] = pack2<FP8>(x2, x3);
-            }
+            c_qslot = (q_head - 1) % C::kQueue;
+            need_q = true;
 #pragma unroll
             for (int t = 0; t < C::KS; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
             m_run[0] = m_run[1] = -CUDART_INF_F;
@@ -429,6 +427,32 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::kWarps * 32, 1)
             }
         }
         if (__any_sync(0xffffffffu, bail)) break;
+        if (need_q) {
+            // Q^T fragments of head r from the unit's query slot (zero past its heads)
+            need_q = false;
+            const bool hv = r < cu.nh;
+            const unsigned char* qs = ws + C::kQOff + c_qslot * C::kQSlotBytes + (size_t)(hv ? r : 0) * D * QF::bytes;
+#pragma unroll
+            for (int ks = 0; ks < C::KS; ++ks) {
+                int d0, d1;
+                if constexpr (FP8) {
+                    d0 = 64 * (ks / 4) + 16 * c + 4 * (ks % 4);      // 4 consecutive d: j = 0..3
+                    d1 = d0 + 2;
+                } else {
+                    d0 = 16 * ks + 2 * c;
+                    d1 = d0 + 8;
+                }
+                float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+                if (hv) {
+                    x0 = load_elem<QF>(qs, d0);
+                    x1 = load_elem<QF>(qs, d0 + 1);
+                    x2 = load_elem<QF>(qs, d1);
+                    x3 = load_elem<QF>(qs, d1 + 1);
+                }
+                qf[ks][0] = pack2<FP8>(x0, x1);
+                qf[ks][1] = pack2<FP8>(x2, x3);
+            }
+        }
         const uint32_t vmask = masks[slot];
         const uint32_t kb = stage_k(slot), vb = stage_v(slot);
 
@@ -669,7 +693,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // head) x (min(bs, tokens per stage) consecutive tokens of one block).
 template <int D, bool FP8>
 bool encode_cache_map(CUtensorMap* map, const void* base, const DecodeParams& p) {
-    using C = Cfg<D, FP8>;
+    using C = Cfg<D, FP8, 2>;
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     const int esize = FP8 ? 1 : 2;
@@ -686,7 +710,7 @@ bool encode_cache_map(CUtensorMap* map, const void* base, const DecodeParams& p)
 
 template <int D, bool FP8, typename QF>
 cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t st) {
-    using C = Cfg<D, FP8>;
+    using C = Cfg<D, FP8, QF::bytes>;
     auto kern = decode_tc_kernel<D, FP8, QF>;
     // the shared-memory opt-in is per device: remember it per device ordinal
     static bool configured[64] = {false};
