@@ -90,13 +90,17 @@ struct Cfg {
     // unit queue
     static constexpr int kQOff = kStages * kStageBytes;
     static constexpr int kWarpBytes = (kQOff + kQueue * kQSlotBytes + 1023) / 1024 * 1024;
-    static constexpr int kCtlBytes = (8 * kStages + 4 * kStages + 7) / 8 * 8 + 8 * kQueue;
+    // trailer per worker: barriers (8 B each), stage masks (4 B each), then
+    // the unit queue (32-byte entries, 16-byte aligned)
+    static constexpr int kQueueCtlOff = (8 * kStages + 4 * kStages + 15) / 16 * 16;
+    static constexpr int kCtlBytes = kQueueCtlOff + 32 * kQueue;
     static constexpr int kCtlOff = kWarps * kWarpBytes;
     static constexpr int kSmemBytes = kCtlOff + kWarps * kCtlBytes + 1024;   // + room to align the base
     static constexpr int KS = D / 16;     // k-steps of the QK product, m-tiles of the PV product
     static_assert(kTok == 16 || kTok == 32, "stages hold 16 or 32 tokens");
     static_assert(kStageBytes % 1024 == 0 || kRowBytes < 128, "stages must keep the swizzle atoms aligned");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+    static_assert(kCtlOff % 1024 == 0 && kCtlBytes % 16 == 0, "trailer alignment");
 };
 
 // Shared-memory byte address of logical byte `x` (a multiple of 16, plus an
@@ -213,7 +217,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 // ------------------------------------------------------------------- units
 
-struct Unit {
+struct __align__(16) Unit {
     int s, kvh, h0, nh, part, t0, t1, np;
 };
 
@@ -268,8 +272,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
     unsigned char* ctl = smem + C::kCtlOff + warp * C::kCtlBytes;
     const uint32_t ctl_addr = base_addr + C::kCtlOff + warp * C::kCtlBytes;
     uint32_t* masks = reinterpret_cast<uint32_t*>(ctl + 8 * C::kStages);
-    unsigned long long* queue =
-        reinterpret_cast<unsigned long long*>(ctl + (8 * C::kStages + 4 * C::kStages + 7) / 8 * 8);
+    Unit* queue = reinterpret_cast<Unit*>(ctl + C::kQueueCtlOff);
     auto bar = [&](int i) { return ctl_addr + 8 * i; };
     auto stage_k = [&](int i) { return ws_addr + i * C::kStageBytes; };
     auto stage_v = [&](int i) { return ws_addr + i * C::kStageBytes + C::kPartBytes; };
@@ -322,6 +325,14 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
         }
     };
 
+    // block-table entries of the issuing unit, 32 per chunk, one per lane;
+    // the next chunk is loaded while the current one is in use
+    int tab = 0, tab_next = 0, tab_chunk = 0, tab_blocks = 0;
+    auto load_chunk = [&](int chunk) -> int {
+        const int rb = 32 * chunk + lane;
+        return rb < tab_blocks ? __ldg(p.block_tables + (size_t)iu.s * p.MB + iu.t0 / p.bs + rb) : 0;
+    };
+
     auto issue_one = [&]() -> bool {
         while (!i_have || i_stage == i_nst) {
             if (!claiming) return false;
@@ -332,26 +343,37 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
             }
             unit_of(p, u, nsets, iu);
             i_qslot = q_tail % C::kQueue;
-            if (lane == 0) queue[i_qslot] = u;
+            if (lane == 0) {
+                int4* e = reinterpret_cast<int4*>(queue + i_qslot);
+                e[0] = make_int4(iu.s, iu.kvh, iu.h0, iu.nh);
+                e[1] = make_int4(iu.part, iu.t0, iu.t1, iu.np);
+            }
             ++q_tail;
             i_have = true;
             i_stage = 0;
             i_nst = (iu.t1 - iu.t0 + kTok - 1) / kTok;
+            tab_blocks = (iu.t1 - iu.t0 + p.bs - 1) / p.bs;
+            tab_chunk = 0;
+            tab = load_chunk(0);
+            tab_next = load_chunk(1);
         }
         // the unit's query rows ride on its first stage
         const uint32_t q_bytes = i_stage == 0 ? (uint32_t)(iu.nh * D * QF::bytes) : 0u;
         const int slot = g_issue % C::kStages;
         const int ts = iu.t0 + i_stage * kTok;
         const int tn = min(kTok, iu.t1 - ts);
+        const int rs = i_stage * kTok;                         // token offset of the stage in the unit
+        if (rs / p.bs / 32 != tab_chunk) {                     // the stage's blocks start a new chunk
+            ++tab_chunk;
+            tab = tab_next;
+            tab_next = load_chunk(tab_chunk + 1);
+        }
         // per token: inside the unit and in a block with a valid id
-        const int t = ts + lane;
+        const int pb_tok = __shfl_sync(0xffffffffu, tab, ((rs + lane) / p.bs) & 31);
         bool ok = lane < tn;
-        if (ok) {
-            const int pb = __ldg(p.block_tables + (size_t)iu.s * p.MB + t / p.bs);
-            if (pb < 0 || pb >= p.NB) {
-                report(p.err, PKV_DEVERR_BLOCK_ID);
-                ok = false;
-            }
+        if (ok && (pb_tok < 0 || pb_tok >= p.NB)) {
+            report(p.err, PKV_DEVERR_BLOCK_ID);
+            ok = false;
         }
         const uint32_t m = __ballot_sync(0xffffffffu, ok);
         // one box per (box_rows tokens of the stage, K or V, 128-byte half): lane i issues box i
@@ -360,6 +382,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
         const uint32_t rows_mask = box_rows == 32 ? 0xffffffffu : 0xffffu;
         const bool box_live = lane < nbox && ((m >> (b * box_rows)) & rows_mask) != 0;
         const uint32_t nissue = __popc(__ballot_sync(0xffffffffu, box_live));
+        const int pb_box = __shfl_sync(0xffffffffu, tab, ((rs + b * box_rows) / p.bs) & 31);
         if (lane == 0) {
             masks[slot] = m;
             mbar_arrive_expect_tx(bar(slot), nissue * box_bytes + q_bytes);
@@ -371,11 +394,10 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
         __syncwarp();
         if (box_live) {
             const int t0b = ts + b * box_rows;                 // first token of the box
-            const int pb = __ldg(p.block_tables + (size_t)iu.s * p.MB + t0b / p.bs);
             const uint32_t dst = (kv ? stage_v(slot) : stage_k(slot)) + h * (kTok * C::kBoxRow) +
                                  b * box_rows * C::kBoxRow;
             tensor_load_2d(dst, kv ? &vmap : &kmap, iu.kvh * D + h * (C::kBoxRow / (FP8 ? 1 : 2)),
-                           pb * p.bs + t0b % p.bs, bar(slot));
+                           pb_box * p.bs + t0b % p.bs, bar(slot));
         }
         ++g_issue;
         ++i_stage;
@@ -400,9 +422,13 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
         if (!have_unit) {
             if (q_head == q_tail) break;
             __syncwarp();
-            const unsigned long long u = queue[q_head % C::kQueue];
+            {
+                const int4* e = reinterpret_cast<const int4*>(queue + q_head % C::kQueue);
+                const int4 a = e[0], b2 = e[1];
+                cu.s = a.x; cu.kvh = a.y; cu.h0 = a.z; cu.nh = a.w;
+                cu.part = b2.x; cu.t0 = b2.y; cu.t1 = b2.z; cu.np = b2.w;
+            }
             ++q_head;
-            unit_of(p, u, nsets, cu);
             c_stage = 0;
             c_nst = (cu.t1 - cu.t0 + kTok - 1) / kTok;
             have_unit = true;
