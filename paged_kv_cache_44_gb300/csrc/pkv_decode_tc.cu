@@ -197,12 +197,16 @@ __device__ __forceinline__ float fast_exp2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-// two E4M3 codes (low byte first) -> two fp16 in one register, exactly
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-    uint32_t r;
-    const uint16_t c = static_cast<uint16_t>(two_codes);
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
-    return r;
+// four E4M3 codes (bytes 0..3 of w) -> two registers of two fp16 each
+// (lo = bytes 0,1; hi = bytes 2,3), exactly; the 16-bit halves of w are
+// taken as register halves, with no shifts
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 l16, h16;\n\t"
+        "mov.b32 {l16, h16}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l16;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h16;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 template <bool FP8>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -492,22 +496,11 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
                 // pi(2i+b) = 4i+b, pi(2i+8+b) = 4i+2+b
                 const int ta = 16 * mt + 4 * (r >> 1) + (r & 1);
                 const int tb = ta + 2;
-                // Load both halves of both rows (odd rows start with the other
-                // half, which spreads a load over all banks), then run the
-                // MMAs in one k-step order common to every lane.
                 uint4 ka[D / 64], kbv[D / 64];
-                if constexpr (D == 128) {
-                    const int first = (r & 1) * 64, second = 64 - first;
-                    const uint4 a0 = lds128(swz<C::kRowBytes, C::kTok>(kb, ta, 16 * c + first));
-                    const uint4 b0 = lds128(swz<C::kRowBytes, C::kTok>(kb, tb, 16 * c + first));
-                    const uint4 a1 = lds128(swz<C::kRowBytes, C::kTok>(kb, ta, 16 * c + second));
-                    const uint4 b1 = lds128(swz<C::kRowBytes, C::kTok>(kb, tb, 16 * c + second));
-                    const bool odd = r & 1;
-                    ka[0] = odd ? a1 : a0;  ka[1] = odd ? a0 : a1;
-                    kbv[0] = odd ? b1 : b0; kbv[1] = odd ? b0 : b1;
-                } else {
-                    ka[0] = lds128(swz<C::kRowBytes, C::kTok>(kb, ta, 16 * c));
-                    kbv[0] = lds128(swz<C::kRowBytes, C::kTok>(kb, tb, 16 * c));
+#pragma unroll
+                for (int hh = 0; hh < D / 64; ++hh) {
+                    ka[hh] = lds128(swz<C::kRowBytes, C::kTok>(kb, ta, 16 * c + 64 * hh));
+                    kbv[hh] = lds128(swz<C::kRowBytes, C::kTok>(kb, tb, 16 * c + 64 * hh));
                 }
 #pragma unroll
                 for (int hh = 0; hh < D / 64; ++hh) {
@@ -516,9 +509,10 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int ks = 4 * hh + j;
-                        mma16816<true>(sacc[mt], e4m3x2_to_f16x2(wa[j]), e4m3x2_to_f16x2(wb[j]),
-                                       e4m3x2_to_f16x2(wa[j] >> 16), e4m3x2_to_f16x2(wb[j] >> 16), qf[ks][0],
-                                       qf[ks][1]);
+                        uint32_t a01, a45, a23, a67;
+                        e4m3x4_to_f16x2x2(wa[j], a01, a45);     // row r: d j=0,1 | j=2,3
+                        e4m3x4_to_f16x2x2(wb[j], a23, a67);     // row r+8
+                        mma16816<true>(sacc[mt], a01, a23, a45, a67, qf[ks][0], qf[ks][1]);
                     }
                 }
             } else {
@@ -615,8 +609,10 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
                     const uint32_t sel = (t & 1) ? 0x7362u : 0x5140u;
                     const uint32_t p01 = __byte_perm(w[0][wi], w[1][wi], sel);   // tokens 4c, 4c+1
                     const uint32_t p23 = __byte_perm(w[2][wi], w[3][wi], sel);   // tokens 4c+2, 4c+3
-                    mma16816<true>(o[t], e4m3x2_to_f16x2(p01), e4m3x2_to_f16x2(p01 >> 16), e4m3x2_to_f16x2(p23),
-                                   e4m3x2_to_f16x2(p23 >> 16), pb[kt][0], pb[kt][1]);
+                    uint32_t a0, a1, a2, a3;
+                    e4m3x4_to_f16x2x2(p01, a0, a1);          // d rows r | r+8, tokens 4c, 4c+1
+                    e4m3x4_to_f16x2x2(p23, a2, a3);          // tokens 4c+2, 4c+3
+                    mma16816<true>(o[t], a0, a1, a2, a3, pb[kt][0], pb[kt][1]);
                 }
             } else {
                 const int mi = lane >> 3;
