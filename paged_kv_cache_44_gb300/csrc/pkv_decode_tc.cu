@@ -71,7 +71,7 @@ constexpr long long kWaitLimitCycles = 4000000000LL;   // ~2 s: a stage that nev
 
 template <int D, bool FP8, int QB>
 struct Cfg {
-    static constexpr int kWarps = FP8 ? PKV_TC_WARPS_FP8 : PKV_TC_WARPS_BF16;     // workers per CTA
+    static constexpr int kWarpsWanted = FP8 ? PKV_TC_WARPS_FP8 : PKV_TC_WARPS_BF16;
     static constexpr int kStages = FP8 ? PKV_TC_STAGES_FP8 : PKV_TC_STAGES_BF16;  // ring depth per worker
     static constexpr int kTok = FP8 ? PKV_TC_TOK_FP8 : PKV_TC_TOK_BF16;          // tokens per stage
     static constexpr int kMT = kTok / 16;                        // 16-token m-tiles per stage
@@ -94,6 +94,9 @@ struct Cfg {
     // the unit queue (32-byte entries, 16-byte aligned)
     static constexpr int kQueueCtlOff = (8 * kStages + 4 * kStages + 15) / 16 * 16;
     static constexpr int kCtlBytes = kQueueCtlOff + 32 * kQueue;
+    // workers per CTA: as many as wanted, up to what fits in shared memory
+    static constexpr int kWarpsFit = (232448 - 1024) / (kWarpBytes + kCtlBytes);
+    static constexpr int kWarps = kWarpsWanted < kWarpsFit ? kWarpsWanted : kWarpsFit;
     static constexpr int kCtlOff = kWarps * kWarpBytes;
     static constexpr int kSmemBytes = kCtlOff + kWarps * kCtlBytes + 1024;   // + room to align the base
     static constexpr int KS = D / 16;     // k-steps of the QK product, m-tiles of the PV product
