@@ -57,7 +57,7 @@ namespace {
 #define PKV_TC_TOK_BF16 32
 #endif
 #ifndef PKV_TC_WARPS_FP8
-#define PKV_TC_WARPS_FP8 8
+#define PKV_TC_WARPS_FP8 10
 #endif
 #ifndef PKV_TC_STAGES_FP8
 #define PKV_TC_STAGES_FP8 2
@@ -228,14 +228,22 @@ struct __align__(16) Unit {
     int s, kvh, h0, nh, part, t0, t1, np;
 };
 
-// Unit id -> coordinates.  Ids run partition-major so that the same
-// partition of every sequence is claimed close together in time (shared
-// prefix blocks are then read while still in L2).  Returns false for ids
-// past a sequence's last partition.
-__device__ __forceinline__ bool unit_of(const DecodeParams& p, unsigned long long u, int nsets, Unit& x) {
+// Unit id -> coordinates.  The ids run over two regions:
+//   A: every full partition (P tokens), partition-major -- the same
+//      partition of every sequence is claimed close together in time, so
+//      shared prefix blocks are read while still in L2;
+//   B: each sequence's last, partial partition (fewer than P tokens, or the
+//      empty one of a sequence with no tokens).
+// Claimed in id order, the long units go first and the short ones last, so
+// the tail of the launch is short.  Returns false for ids that name no
+// work (a partition past the sequence's full ones, or no partial part).
+__device__ __forceinline__ bool unit_of(const DecodeParams& p, unsigned long long u, int nsets,
+                                        unsigned long long region_a, Unit& x) {
     const unsigned long long per_part = (unsigned long long)p.S * p.Hkv * nsets;
-    x.part = (int)(u / per_part);
-    const unsigned long long rem = u - (unsigned long long)x.part * per_part;
+    const bool in_a = u < region_a;
+    const unsigned long long v = in_a ? u : u - region_a;
+    const int part_a = (int)(v / per_part);
+    const unsigned long long rem = v - (unsigned long long)part_a * per_part;
     x.s = (int)(rem / (unsigned)(p.Hkv * nsets));
     const int r2 = (int)(rem - (unsigned long long)x.s * (p.Hkv * nsets));
     x.kvh = r2 / nsets;
@@ -244,13 +252,22 @@ __device__ __forceinline__ bool unit_of(const DecodeParams& p, unsigned long lon
     x.nh = min(kHeadsPerUnit, p.g - set * kHeadsPerUnit);
     int n = __ldg(p.context_lens + x.s);
     if (n < 0 || n > p.max_ctx) {
-        if (x.part == 0 && r2 == 0) report(p.err, PKV_DEVERR_CONTEXT_LEN);
+        if (!in_a && r2 == 0) report(p.err, PKV_DEVERR_CONTEXT_LEN);
         n = n < 0 ? 0 : p.max_ctx;
     }
     x.np = n > 0 ? (n + p.P - 1) / p.P : 1;
-    if (x.part >= x.np) return false;
-    x.t0 = x.part * p.P;
-    x.t1 = min(n, x.t0 + p.P);
+    const int full = n / p.P;
+    if (in_a) {
+        if (part_a >= full) return false;
+        x.part = part_a;
+        x.t0 = part_a * p.P;
+        x.t1 = x.t0 + p.P;
+    } else {
+        if (n > 0 && n == full * p.P) return false;      // no partial partition
+        x.part = full;
+        x.t0 = full * p.P;
+        x.t1 = n;
+    }
     return true;
 }
 
@@ -264,7 +281,8 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, size_t idx, flo
 template <int D, bool FP8, typename QF>
 __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
     decode_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap kmap,
-                     const __grid_constant__ CUtensorMap vmap, unsigned long long total_units, int nsets) {
+                     const __grid_constant__ CUtensorMap vmap, unsigned long long total_units,
+                     unsigned long long region_a, int nsets) {
     using C = Cfg<D, FP8, QF::bytes>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -320,7 +338,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
             static_next += total_warps;
             if (v >= total_units) return false;
             Unit x;
-            if (!unit_of(p, v, nsets, x)) continue;
+            if (!unit_of(p, v, nsets, region_a, x)) continue;
             if (x.t1 <= x.t0) {
                 // a sequence with no tokens: its output is zero
                 for (int i = lane; i < x.nh * D; i += 32)
@@ -348,7 +366,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
                 claiming = false;
                 return false;
             }
-            unit_of(p, u, nsets, iu);
+            unit_of(p, u, nsets, region_a, iu);
             i_qslot = q_tail % C::kQueue;
             if (lane == 0) {
                 int4* e = reinterpret_cast<int4*>(queue + i_qslot);
@@ -751,11 +769,13 @@ cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t st) {
     if (!encode_cache_map<D, FP8>(&kmap, p.kc, p) || !encode_cache_map<D, FP8>(&vmap, p.vc, p))
         return cudaErrorInvalidValue;
     const int nsets = (p.g + kHeadsPerUnit - 1) / kHeadsPerUnit;
-    const unsigned long long units = (unsigned long long)p.Pmax * p.S * p.Hkv * nsets;
+    const unsigned long long per_part = (unsigned long long)p.S * p.Hkv * nsets;
+    const unsigned long long region_a = (unsigned long long)(p.max_ctx / p.P) * per_part;   // full partitions
+    const unsigned long long units = region_a + per_part;                               // + partial ones
     unsigned long long want = (units + C::kWarps - 1) / C::kWarps;
     int grid = (int)(want < (unsigned long long)num_sms ? want : (unsigned long long)num_sms);
     if (grid < 1) grid = 1;
-    kern<<<grid, C::kWarps * 32, C::kSmemBytes, st>>>(p, kmap, vmap, units, nsets);
+    kern<<<grid, C::kWarps * 32, C::kSmemBytes, st>>>(p, kmap, vmap, units, region_a, nsets);
     return cudaGetLastError();
 }
 
