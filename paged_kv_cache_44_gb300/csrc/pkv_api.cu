@@ -18,7 +18,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // finish are short next to the whole launch.  It depends on no dtype, so the
 // workspace size and the launch always agree.
 constexpr long long kTargetUnits = 152LL * 8 * 4;
-constexpr int kMinDefaultPartition = 256;
+constexpr int kMinDefaultPartition = 512;
 constexpr int kHeadSet = 8;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
