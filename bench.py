@@ -218,6 +218,23 @@ def measured_traffic(workload: str, kernel: str):
     return rec.get("dram_bytes_per_launch")
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of `values` over all ranks (the job's time is the
+    slowest rank's); a no-op without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_gbs(world_size: int, bytes_per_rank_step: int, ms_per_step: float) -> float:
+    """Throughput of the whole job: every rank's bytes over the slowest rank's time."""
+    return world_size * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def dist_setup():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -363,11 +380,7 @@ def run_ours(args, w: W.Workload):
     barrier()
     ms_total = t0.elapsed_time(t1)
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(dec0, dec1))
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_total, dec_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total, dec_ms = float(tt[0]), float(tt[1])
+    ms_total, dec_ms = max_over_ranks([ms_total, dec_ms], dev)
     ms_step = ms_total / args.steps
 
     # ---- end to end: host buffers in, host result out, through the public API
@@ -396,16 +409,12 @@ def run_ours(args, w: W.Workload):
     for _ in range(e2e_steps):
         e2e_step()
     e2e_s = (time.perf_counter() - w0) / e2e_steps
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt[0])
+    (e2e_s,) = max_over_ranks([e2e_s], dev)
 
     # ---- numbers
     dbytes = decode_bytes(w)
     sbytes = dbytes + write_bytes(w) + copy_bytes(w)
-    value = ws * sbytes / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(ws, sbytes, ms_step)
     achieved = dbytes / (dec_ms * 1e-3) / 1e9
     peak, peak_kind = peak_hbm()
     traffic = measured_traffic(w.name, args.kernel)
@@ -434,7 +443,7 @@ def run_ours(args, w: W.Workload):
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "traffic": traffic, "kernel": "paged_attention_decode (" + kname + ")",
                      "algorithmic_bytes_per_launch": dbytes, "launch_ms": round(dec_ms, 5)},
-        "e2e": {"value": round(ws * sbytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": round(whole_job_gbs(ws, sbytes, e2e_s * 1e3), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
