@@ -43,33 +43,20 @@ int resolve_partition(int S, int Hq, int Hkv, int d, int bs, int max_ctx, int re
     return P;
 }
 
-}  // namespace
-
-DecodePlan plan_decode(int S, int Hq, int Hkv, int d, int max_ctx, int P) {
+DecodePlan make_plan(int S, int Hq, int d, int max_ctx, int P) {
     DecodePlan pl{};
     pl.P = P;
     pl.Pmax = P > 0 ? (max_ctx > 0 ? (max_ctx + P - 1) / P : 1) : 1;
     pl.split = P > 0 && pl.Pmax > 1;
-    pl.bytes = pl.zero_bytes = kWorkspaceHeaderBytes;
+    pl.bytes = kWorkspaceHeaderBytes;
     if (!pl.split) return pl;
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-    const size_t sets = (size_t)S * Hkv * ((Hq / Hkv + kHeadSet - 1) / kHeadSet);
     const size_t units = (size_t)S * Hq * pl.Pmax;
-    pl.cnt_offset = kWorkspaceHeaderBytes;
-    pl.zero_bytes = up(pl.cnt_offset + sets * sizeof(unsigned));
-    pl.ml_offset = pl.zero_bytes;
+    pl.ml_offset = kWorkspaceHeaderBytes;
     pl.acc_offset = up(pl.ml_offset + units * 2 * sizeof(float));
     pl.bytes = up(pl.acc_offset + units * d * sizeof(float));
     return pl;
 }
-
-size_t decode_zero_bytes(int S, int Hq, int Hkv, int d, int bs, int max_ctx, int partition_request) {
-    const int P = resolve_partition(S, Hq, Hkv, d, bs, max_ctx, partition_request);
-    if (P < 0) return 0;
-    return plan_decode(S, Hq, Hkv, d, max_ctx, P).zero_bytes;
-}
-
-namespace {
 
 pkv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
 
@@ -137,7 +124,7 @@ int pkv_decode_partition_size(int S, int Hq, int Hkv, int d, int bs, int max_con
 size_t pkv_decode_workspace_size(int S, int Hq, int Hkv, int d, int bs, int max_context_len, int partition_size) {
     const int P = resolve_partition(S, Hq, Hkv, d, bs, max_context_len, partition_size);
     if (P < 0) return 0;
-    return plan_decode(S, Hq, Hkv, d, max_context_len, P).bytes;
+    return make_plan(S, Hq, d, max_context_len, P).bytes;
 }
 
 pkv_status pkv_paged_attention_decode_ex(void* out, const void* query, pkv_dtype q_dtype, const void* key_cache,
@@ -172,7 +159,7 @@ pkv_status pkv_paged_attention_decode_ex(void* out, const void* query, pkv_dtype
     if (kernel == PKV_DECODE_AUTO) use_tc = tc_ok;
     else if (kernel == PKV_DECODE_TENSOR_CORES) { if (!tc_ok) return PKV_ERR_UNSUPPORTED; use_tc = true; }
     else use_tc = false;
-    const DecodePlan pl = plan_decode(S, Hq, Hkv, d, max_context_len, P);
+    const DecodePlan pl = make_plan(S, Hq, d, max_context_len, P);
     if (pl.split) {
         if (!workspace || workspace_bytes < pl.bytes) return PKV_ERR_WORKSPACE;
         if (!aligned16(workspace)) return PKV_ERR_INVALID_ARG;
@@ -191,7 +178,6 @@ pkv_status pkv_paged_attention_decode_ex(void* out, const void* query, pkv_dtype
     if (pl.split) {
         char* ws = static_cast<char*>(workspace);
         p.sched = reinterpret_cast<unsigned*>(ws);
-        p.arrive = reinterpret_cast<unsigned*>(ws + pl.cnt_offset);
         p.part_ml = reinterpret_cast<float*>(ws + pl.ml_offset);
         p.part_acc = reinterpret_cast<float*>(ws + pl.acc_offset);
     } else if (workspace && workspace_bytes >= kWorkspaceHeaderBytes && aligned16(workspace)) {
@@ -201,8 +187,7 @@ pkv_status pkv_paged_attention_decode_ex(void* out, const void* query, pkv_dtype
     cudaError_t e = use_tc ? launch_decode_tc(p, q_dtype, cache_dtype, num_sms_current(), st)
                            : launch_decode_simt(p, q_dtype, cache_dtype, st);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
-    // the tensor-core kernel merges partitions itself; the CUDA-core one needs the merge pass
-    if (pl.split && !use_tc) e = launch_decode_reduce(p, q_dtype, st);
+    if (pl.split) e = launch_decode_reduce(p, q_dtype, st);
     return from_cuda(e);
 }
 

@@ -276,55 +276,6 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, size_t idx, flo
     store_elem<QF>(p.out, idx, v);
 }
 
-// Merge of one unit's heads over all partitions of its sequence, by one
-// warp: M = max m_p, L = sum 2^(m_p - M) l_p, O = sum 2^(m_p - M) acc_p / L.
-// Lane i weighs partitions i, i+32, ...; every lane owns D/32 consecutive
-// output elements.  The triples were written by other warps during this
-// launch, so they are read through L2 (ld.global.cg), after the fence that
-// pairs with theirs.
-template <int D, typename QF>
-__device__ __noinline__ void merge_partitions(const DecodeParams& p, const Unit& u, int lane) {
-    constexpr int E = D / 32;
-    for (int hh = 0; hh < u.nh; ++hh) {
-        const size_t u0 = ((size_t)u.s * p.Hq + u.h0 + hh) * p.Pmax;
-        float mx = -CUDART_INF_F;
-        for (int i = lane; i < u.np; i += 32) mx = fmaxf(mx, __ldcg(p.part_ml + 2 * (u0 + i)));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        float lsum = 0.f, o[E];
-#pragma unroll
-        for (int k = 0; k < E; ++k) o[k] = 0.f;
-        for (int c0 = 0; c0 < u.np; c0 += 32) {
-            const int i = c0 + lane;
-            float w = 0.f;
-            if (i < u.np) {
-                const float m = __ldcg(p.part_ml + 2 * (u0 + i));
-                w = m == -CUDART_INF_F ? 0.f : exp2f(m - mx);
-                lsum = fmaf(w, __ldcg(p.part_ml + 2 * (u0 + i) + 1), lsum);
-            }
-            const int cn = min(32, u.np - c0);
-            const float* acc = p.part_acc + (u0 + c0) * D + lane * E;
-            for (int j = 0; j < cn; ++j) {
-                const float wj = __shfl_sync(0xffffffffu, w, j);
-                if constexpr (E == 4) {
-                    const float4 a = __ldcg(reinterpret_cast<const float4*>(acc + (size_t)j * D));
-                    o[0] = fmaf(wj, a.x, o[0]); o[1] = fmaf(wj, a.y, o[1]);
-                    o[2] = fmaf(wj, a.z, o[2]); o[3] = fmaf(wj, a.w, o[3]);
-                } else {
-                    const float2 a = __ldcg(reinterpret_cast<const float2*>(acc + (size_t)j * D));
-                    o[0] = fmaf(wj, a.x, o[0]); o[1] = fmaf(wj, a.y, o[1]);
-                }
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-        const float f = lsum > 0.f ? p.out_scale / lsum : 0.f;
-        const size_t ob = ((size_t)u.s * p.Hq + u.h0 + hh) * D + lane * E;
-#pragma unroll
-        for (int k = 0; k < E; ++k) store_out<QF>(p, ob + k, o[k] * f);
-    }
-}
-
 // ------------------------------------------------------------------ kernel
 
 template <int D, bool FP8, typename QF>
@@ -746,19 +697,6 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
                 if (r == 0) {
                     if (wA) { p.part_ml[2 * uA] = m_run[0]; p.part_ml[2 * uA + 1] = l0; }
                     if (wB) { p.part_ml[2 * uB] = m_run[1]; p.part_ml[2 * uB + 1] = l1; }
-                }
-                // the warp that finishes a sequence's last partition merges them all
-                __threadfence();
-                __syncwarp();
-                const int set = (cu.h0 - cu.kvh * p.g) / kHeadsPerUnit;
-                unsigned* ctr = p.arrive + ((size_t)cu.s * p.Hkv + cu.kvh) * nsets + set;
-                unsigned arrived = 0;
-                if (lane == 0) arrived = atomicAdd(ctr, 1u);
-                arrived = __shfl_sync(0xffffffffu, arrived, 0);
-                if (arrived == (unsigned)cu.np - 1) {
-                    __threadfence();
-                    merge_partitions<D, QF>(p, cu, lane);
-                    if (lane == 0) *ctr = 0u;       // ready for the next launch
                 }
             }
             have_unit = false;

@@ -44,7 +44,6 @@ struct DecodeParams {
     float* part_ml;       // [S][Hq][Pmax][2]: running max (log2 units) and sum
     float* part_acc;      // [S][Hq][Pmax][d]: un-normalised weighted sums of V
     unsigned* sched;      // scheduling counters in the workspace header (or null)
-    unsigned* arrive;     // [S][Hkv][head sets]: partitions finished, for the in-kernel merge (or null)
     int32_t* err;
     int S, MB, Hq, Hkv, g, d, bs, NB;
     int P;                // tokens per partition (> 0)
@@ -54,20 +53,13 @@ struct DecodeParams {
     float out_scale;          // v_scale for E4M3 caches, else 1
 };
 
-// Resolved layout of the decode workspace:
-//   [header 256 B][arrival counters][partition max/sum][partition weighted sums]
-// The header and the counters must be zero when a decode starts; a decode
-// that completes leaves them zero.
+// Resolved layout of the decode workspace.
 struct DecodePlan {
     int P;            // tokens per partition; 0 = one partition per sequence
     int Pmax;
-    bool split;       // partitions must be merged
-    size_t cnt_offset, ml_offset, acc_offset, zero_bytes, bytes;
+    bool split;       // a reduce pass is needed
+    size_t ml_offset, acc_offset, bytes;
 };
-DecodePlan plan_decode(int S, int Hq, int Hkv, int d, int max_ctx, int P);
-// Bytes at the start of the workspace that must be zero before a decode
-// with these arguments (0 for invalid arguments).
-size_t decode_zero_bytes(int S, int Hq, int Hkv, int d, int bs, int max_ctx, int partition_request);
 
 enum class DecodeKernel { Simt = 0, TensorCore = 1 };
 

@@ -54,12 +54,11 @@ extern "C" pkv_status pkv_paged_attention_decode_static(
     void* scratch = nullptr;
     const pkv_status st = scratch_on_current_device(&scratch);
     if (st != PKV_OK) return st;
-    // The array keeps whatever the previous call left.  Its counters (the
-    // work counter and the per-sequence arrival counters at its start) must be
-    // zero; a completed decode leaves them zero, but clear them anyway so
-    // that one interrupted call cannot disturb the next.
-    const size_t zero = pkv::decode_zero_bytes(S, Hq, Hkv, d, bs, max_context_len, partition_size);
-    if (cudaMemsetAsync(scratch, 0, zero, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    // The array keeps whatever the previous call left.  The work counter at
+    // its start must be zero; a completed decode leaves it zero, but clear it
+    // anyway so that one interrupted call cannot disturb the next.
+    if (cudaMemsetAsync(scratch, 0, pkv::kWorkspaceHeaderBytes, reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
         return PKV_ERR_CUDA;
     return pkv_paged_attention_decode(out, query, q_dtype, key_cache, value_cache, cache_dtype, block_tables, MB,
                                       context_lens, S, max_context_len, Hq, Hkv, d, bs, NB, scale, k_scale,

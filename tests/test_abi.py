@@ -47,12 +47,11 @@ def test_status_strings_and_version(pkv):
 
 
 def test_workspace_plan(pkv):
-    # 72B-shaped: header + one arrival counter per (seq, K/V head) + 32 seqs x 64 heads x
-    # 64 partitions x (128 + 2) floats, each region 256-byte aligned
+    # 72B-shaped: 32 seqs x 64 heads x 64 partitions x (128 + 2) floats + header
     n = pkv.decode_workspace_size(32, 64, 8, 128, 16, 32768, 512)
     units = 32 * 64 * 64
-    base = 256 + 32 * 8 * 4 + units * 130 * 4
-    assert base <= n < base + 3 * 256
+    assert n >= 256 + units * 130 * 4
+    assert n < 256 + units * 130 * 4 + 1024
     # no split -> header only
     assert pkv.decode_workspace_size(4, 4, 2, 64, 16, 38, -1) == 256
     assert pkv.decode_partition_size(4, 4, 2, 64, 16, 38, -1) == 0
