@@ -262,6 +262,72 @@ PKV_API pkv_status pkv_paged_attention_decode_static(void* out, const void* quer
                                                      int partition_size,
                                                      int32_t* err_word, pkv_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Host block manager: the bookkeeping that produces the block tables, slot
+ * mappings and copy-on-write pairs the device calls consume.  Host memory
+ * only; nothing here touches the GPU.
+ *
+ * Source: "LLM推論の基礎とvLLMの内部", section 4 "PagedAttentionとブロック
+ * 管理": blocks are handed to a request one at a time as it grows, each
+ * request keeps a block table, block 0 is reserved as the null block, free
+ * blocks wait in a doubly linked queue, and shared blocks carry a reference
+ * count and are copied before a write.  Section 5: a full block's hash
+ * chains its parent's hash, its tokens and extra keys; only full blocks are
+ * cached; the last prompt token is always recomputed; a finished request
+ * returns its blocks tail first with their hashes kept, and the queue is
+ * reused from its front (least recently freed first).  Free blocks without
+ * a hash are handed out before any cached block.
+ *
+ * Errors: PKV_ERR_INVALID_ARG for a null pool, an unknown or duplicate
+ * sequence id, or bad sizes; PKV_ERR_WORKSPACE when the pool has too few
+ * free blocks (nothing is changed then).  A pool is not thread-safe.
+ * ---------------------------------------------------------------------- */
+typedef struct pkv_block_pool pkv_block_pool;
+
+/* A pool of num_blocks blocks of block_size tokens (block 0 reserved, so
+ * num_blocks - 1 usable).  enable_prefix_caching != 0 turns on the hash
+ * chain and reuse of cached blocks. */
+PKV_API pkv_status pkv_pool_create(int num_blocks, int block_size, int enable_prefix_caching,
+                                   pkv_block_pool** out);
+PKV_API void pkv_pool_destroy(pkv_block_pool* pool);
+/* Extra key mixed into every block hash (a LoRA id, a cache salt, ...):
+ * pools with different keys never share cached blocks. */
+PKV_API pkv_status pkv_pool_set_extra_key(pkv_block_pool* pool, uint64_t extra_key);
+PKV_API int pkv_pool_num_free_blocks(const pkv_block_pool* pool);
+PKV_API int pkv_pool_num_cached_blocks(const pkv_block_pool* pool);
+/* Reference count of a physical block (-1 for a bad id). */
+PKV_API int pkv_pool_block_ref_count(const pkv_block_pool* pool, int block);
+
+/* Start sequence seq_id with its prompt tokens[0..n_tokens): reuse the
+ * longest cached prefix of whole blocks (never the block holding the last
+ * token's position if that would leave no token to compute), take new blocks
+ * for the rest.  *num_cached_tokens (optional) receives the tokens found in
+ * the cache.  The prompt's K/V then go to slots block_table[t / bs] * bs +
+ * t % bs for t >= *num_cached_tokens. */
+PKV_API pkv_status pkv_pool_add_sequence(pkv_block_pool* pool, int64_t seq_id, const int32_t* tokens,
+                                         int n_tokens, int* num_cached_tokens);
+
+/* One more token for seq_id.  *slot receives the cache slot of its K/V.  If
+ * the last block was full a new block is taken; if it is shared with another
+ * sequence (after pkv_pool_fork) it is copied first: *cow_src / *cow_dst
+ * receive the (src, dst) pair to pass to pkv_copy_blocks before the write,
+ * else -1. */
+PKV_API pkv_status pkv_pool_append_token(pkv_block_pool* pool, int64_t seq_id, int32_t token, int64_t* slot,
+                                         int64_t* cow_src, int64_t* cow_dst);
+
+/* child_id shares every block of parent_id (reference counts + 1), as for
+ * parallel sampling or beam search. */
+PKV_API pkv_status pkv_pool_fork(pkv_block_pool* pool, int64_t parent_id, int64_t child_id);
+
+/* End seq_id: its blocks lose one reference each, last block first. */
+PKV_API pkv_status pkv_pool_free_sequence(pkv_block_pool* pool, int64_t seq_id);
+
+/* Copy seq_id's block table into table[0..max_blocks), padded with the null
+ * block 0; *num_blocks and *num_tokens (optional) receive its length.  A
+ * NULL table only queries the lengths. */
+PKV_API pkv_status pkv_pool_block_table(const pkv_block_pool* pool, int64_t seq_id, int32_t* table,
+                                        int max_blocks, int* num_blocks, int* num_tokens);
+
 /* Static, human-readable text for a status. */
 PKV_API const char* pkv_status_string(pkv_status status);
 

@@ -34,7 +34,10 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported dtype or shape",
 
 EXPORTED = ("pkv_paged_kv_write", "pkv_decode_workspace_size", "pkv_decode_partition_size",
             "pkv_paged_attention_decode", "pkv_paged_attention_decode_ex", "pkv_copy_blocks",
-            "pkv_status_string", "pkv_version", "pkv_paged_attention_decode_static")
+            "pkv_status_string", "pkv_version", "pkv_paged_attention_decode_static",
+            "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_set_extra_key", "pkv_pool_num_free_blocks",
+            "pkv_pool_num_cached_blocks", "pkv_pool_block_ref_count", "pkv_pool_add_sequence",
+            "pkv_pool_append_token", "pkv_pool_fork", "pkv_pool_free_sequence", "pkv_pool_block_table")
 STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -68,6 +71,29 @@ def _load() -> ctypes.CDLL:
     lib.pkv_paged_attention_decode_static.restype = i32
     lib.pkv_copy_blocks.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32, vp, i32, i32, sz, vp, vp]
     lib.pkv_copy_blocks.restype = i32
+    i64, pi32, pi64 = ctypes.c_int64, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)
+    lib.pkv_pool_create.argtypes = [i32, i32, i32, ctypes.POINTER(vp)]
+    lib.pkv_pool_create.restype = i32
+    lib.pkv_pool_destroy.argtypes = [vp]
+    lib.pkv_pool_destroy.restype = None
+    lib.pkv_pool_set_extra_key.argtypes = [vp, ctypes.c_uint64]
+    lib.pkv_pool_set_extra_key.restype = i32
+    lib.pkv_pool_num_free_blocks.argtypes = [vp]
+    lib.pkv_pool_num_free_blocks.restype = i32
+    lib.pkv_pool_num_cached_blocks.argtypes = [vp]
+    lib.pkv_pool_num_cached_blocks.restype = i32
+    lib.pkv_pool_block_ref_count.argtypes = [vp, i32]
+    lib.pkv_pool_block_ref_count.restype = i32
+    lib.pkv_pool_add_sequence.argtypes = [vp, i64, pi32, i32, pi32]
+    lib.pkv_pool_add_sequence.restype = i32
+    lib.pkv_pool_append_token.argtypes = [vp, i64, ctypes.c_int32, pi64, pi64, pi64]
+    lib.pkv_pool_append_token.restype = i32
+    lib.pkv_pool_fork.argtypes = [vp, i64, i64]
+    lib.pkv_pool_fork.restype = i32
+    lib.pkv_pool_free_sequence.argtypes = [vp, i64]
+    lib.pkv_pool_free_sequence.restype = i32
+    lib.pkv_pool_block_table.argtypes = [vp, i64, pi32, i32, pi32, pi32]
+    lib.pkv_pool_block_table.restype = i32
     lib.pkv_status_string.argtypes = [i32]
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_version.argtypes = []
@@ -219,3 +245,81 @@ def copy_blocks(key_caches: Sequence[torch.Tensor], value_caches: Sequence[torch
     vp = (ctypes.c_void_p * L)(*[_ptr(t) for t in value_caches])
     _check("copy_blocks", lib.pkv_copy_blocks(kp, vp, L, _ptr(block_mapping), P, NB, block_bytes,
                                               _ptr(err_word), _stream(stream)))
+
+
+class BlockPool:
+    """Host block manager (pkv_pool_* in include/pkv.h): block tables, slots
+    and copy-on-write pairs for the device calls.  Block 0 is the null block."""
+
+    def __init__(self, num_blocks: int, block_size: int, prefix_caching: bool = True, extra_key: int = 0):
+        h = ctypes.c_void_p()
+        _check("pkv_pool_create", lib.pkv_pool_create(num_blocks, block_size, int(prefix_caching), ctypes.byref(h)))
+        self._h = h
+        self.block_size = block_size
+        if extra_key:
+            self.set_extra_key(extra_key)
+
+    def set_extra_key(self, extra_key: int) -> None:
+        """Key mixed into later block hashes: blocks cached under one key are
+        never reused under another."""
+        _check("pkv_pool_set_extra_key", lib.pkv_pool_set_extra_key(self._h, extra_key))
+
+    def close(self) -> None:
+        if self._h:
+            lib.pkv_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free(self) -> int:
+        return lib.pkv_pool_num_free_blocks(self._h)
+
+    def num_cached(self) -> int:
+        return lib.pkv_pool_num_cached_blocks(self._h)
+
+    def ref_count(self, block: int) -> int:
+        return lib.pkv_pool_block_ref_count(self._h, block)
+
+    def add_sequence(self, seq_id: int, tokens) -> Optional[int]:
+        """Cached prompt tokens, or None when the pool has too few free blocks."""
+        import numpy as np
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        got = ctypes.c_int32(0)
+        st = lib.pkv_pool_add_sequence(self._h, seq_id, t.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                       t.size, ctypes.byref(got))
+        if st == 3:
+            return None
+        _check("pkv_pool_add_sequence", st)
+        return got.value
+
+    def append_token(self, seq_id: int, token: int):
+        """(slot, cow_src, cow_dst) -- cow_* = -1 without a copy -- or None when no block is free."""
+        slot, src, dst = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        st = lib.pkv_pool_append_token(self._h, seq_id, token, ctypes.byref(slot), ctypes.byref(src),
+                                       ctypes.byref(dst))
+        if st == 3:
+            return None
+        _check("pkv_pool_append_token", st)
+        return slot.value, src.value, dst.value
+
+    def fork(self, parent_id: int, child_id: int) -> None:
+        _check("pkv_pool_fork", lib.pkv_pool_fork(self._h, parent_id, child_id))
+
+    def free_sequence(self, seq_id: int) -> None:
+        _check("pkv_pool_free_sequence", lib.pkv_pool_free_sequence(self._h, seq_id))
+
+    def block_table(self, seq_id: int, max_blocks: Optional[int] = None):
+        """(table as int32 numpy array padded with 0 to max_blocks, number of tokens)."""
+        import numpy as np
+        nb, nt = ctypes.c_int32(), ctypes.c_int32()
+        _check("pkv_pool_block_table", lib.pkv_pool_block_table(self._h, seq_id, None, 0, ctypes.byref(nb),
+                                                                 ctypes.byref(nt)))
+        m = nb.value if max_blocks is None else max_blocks
+        out = np.zeros(max(m, 1), dtype=np.int32)
+        _check("pkv_pool_block_table", lib.pkv_pool_block_table(
+            self._h, seq_id, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), out.size, None, None))
+        return out[:m] if m else out[:0], nt.value

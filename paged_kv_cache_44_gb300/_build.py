@@ -38,7 +38,7 @@ def _newest_header() -> float:
 
 def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     hdr = _newest_header()
     objs, procs = [], []
     for src in srcs:

@@ -49,3 +49,50 @@ def test_pins_catch_mutant(tmp_path, name):
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
+
+
+# ---- the block manager model (oracle/block_pool.py) against the pages' numbers
+
+POOL_MUTANTS = {
+    "return-head-first": ("for b in reversed(self.seqs.pop(sid)[\"table\"]):",
+                          "for b in self.seqs.pop(sid)[\"table\"]:"),
+    "no-last-token-rule": ("and (len(hits) + 1) * self.bs <= n - 1", "and (len(hits) + 1) * self.bs <= n"),
+    "evict-newest-first": ("b = self.queue.pop(0)", "b = self.queue.pop()"),
+    "uncached-reused-last": ("self.queue.insert(0, b)       # nothing worth keeping: reused first",
+                             "self.queue.append(b)"),
+    "cache-partial-blocks": ("for j in range(n // self.bs):", "for j in range(-(-n // self.bs)):"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(POOL_MUTANTS))
+def test_pool_pins_catch_mutant(tmp_path, name):
+    import importlib.util
+    old, new = POOL_MUTANTS[name]
+    src = open(os.path.join(ROOT, "oracle", "block_pool.py"), encoding="utf-8").read()
+    assert src.count(old) == 1, name
+    path = tmp_path / "block_pool_mutant.py"
+    path.write_text(src.replace(old, new), encoding="utf-8")
+    spec = importlib.util.spec_from_file_location("block_pool_mutant", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import test_block_pool as T
+    bs, usable, docs, ntok, passes = T._golden_lru()
+    caught = False
+    try:
+        pool = mod.BlockPoolModel(usable + 1, bs)
+        caught = T._run_lru(pool, docs, ntok, passes) != [p[2] for p in passes]
+    except (AssertionError, IndexError, KeyError, ValueError):
+        caught = True
+    if not caught:
+        caught = not T._full_hit_recomputes_last_token(mod.BlockPoolModel(10, 16))
+    if not caught:
+        # the section 4 diagram: a 38-token request shares its first block with a second one
+        import numpy as np
+        rng = np.random.default_rng(3)
+        a = list(rng.integers(1, 30000, 38))
+        b = a[:16] + list(rng.integers(1, 30000, 10))
+        m = mod.BlockPoolModel(20, 16)
+        m.add_sequence(0, a)
+        caught = m.add_sequence(1, b) != 16 or m.ref[m.block_table(0)[0]] != 2 or len(m.block_table(0)) != 3
+    assert caught, f"pool mutant {name} survived the pins"
