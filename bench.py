@@ -498,6 +498,48 @@ def run_ours(args, w: W.Workload):
         dist.destroy_process_group()
 
 
+def run_block_manager(args):
+    """Host block manager throughput, serving-like: S sequences whose
+    prompts share a system prefix are admitted (prefix-cache lookups and
+    hashing of every full block), each then grows by `steps` tokens (one
+    slot per token, a new block every block_size tokens), then all are freed.
+    Times the C-ABI calls through the binding (ctypes overhead included)."""
+    import paged_kv_cache_44_gb300 as pkv
+    rng = np.random.default_rng(0)
+    S, bs, prompt, steps = 256, 16, 1024, max(1, min(args.steps, 256))
+    system = rng.integers(1, 150_000, 512, dtype=np.int32)
+    prompts = [np.concatenate([system, rng.integers(1, 150_000, prompt - 512, dtype=np.int32)]) for _ in range(S)]
+    nb = S * (prompt + steps) // bs + S + 8
+    pool = pkv.BlockPool(nb, bs)
+    t0 = time.perf_counter()
+    hits = sum(pool.add_sequence(i, prompts[i]) for i in range(S))
+    t1 = time.perf_counter()
+    ids = np.arange(S, dtype=np.int64)
+    toks = np.full(S, 7, np.int32)
+    for _ in range(steps):
+        pool.append_tokens(ids, toks)          # one call per decode step: slots + copy pairs
+    t2 = time.perf_counter()
+    tabs, cl = pool.block_tables(ids, (prompt + steps + bs - 1) // bs)
+    t2b = time.perf_counter()
+    step_us, tables_us = (t2 - t1) / steps * 1e6, (t2b - t2) * 1e6
+    assert int(cl.min()) == prompt + steps
+    t2 = t2b
+    for i in range(S):
+        pool.free_sequence(i)
+    t3 = time.perf_counter()
+    line = {"component": "block-manager", "metric": "host block manager operations/s",
+            "admit_tokens_per_s": round(S * prompt / (t1 - t0), 1),
+            "prefix_hit_tokens": int(hits),
+            "append_tokens_per_s": round(S * steps / (t2 - t1), 1),
+            "decode_step_us": round(step_us, 2),
+            "block_tables_us": round(tables_us, 1),
+            "free_sequences_per_s": round(S / (t3 - t2), 1),
+            "config": {"sequences": S, "prompt_tokens": prompt, "shared_prefix_tokens": 512, "block_size": bs,
+                       "appended_tokens_per_sequence": steps, "blocks": nb},
+            "host": {"cpu_threads": cpu_threads()}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -510,9 +552,14 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--S", type=int, default=None, help="fewer sequences (small profiling cases)")
+    ap.add_argument("--component", default="decode-step", choices=["decode-step", "block-manager"],
+                    help="block-manager: time the host block manager instead (prints its own line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.component == "block-manager":
+        run_block_manager(args)
+        return
     w = W.make(args.workload, S=args.S) if args.S else W.make(args.workload)
     if args.impl == "reference":
         run_reference(args, w)

@@ -322,6 +322,21 @@ PKV_API pkv_status pkv_pool_fork(pkv_block_pool* pool, int64_t parent_id, int64_
 /* End seq_id: its blocks lose one reference each, last block first. */
 PKV_API pkv_status pkv_pool_free_sequence(pkv_block_pool* pool, int64_t seq_id);
 
+/* One decode step for n sequences at once: token tokens[i] is appended to
+ * seq_ids[i] (each id once).  slot_mapping[i] receives its slot -- the input
+ * of pkv_paged_kv_write -- and the copy-on-write pairs go to
+ * block_mapping[0 .. 2 * *num_copies) as (src, dst) -- the input of
+ * pkv_copy_blocks, to run before the write.  block_mapping must have room
+ * for 2 * n entries.  If the pool cannot cover the step, PKV_ERR_WORKSPACE is
+ * returned and nothing changes. */
+PKV_API pkv_status pkv_pool_append_tokens(pkv_block_pool* pool, const int64_t* seq_ids, const int32_t* tokens,
+                                          int n, int64_t* slot_mapping, int64_t* block_mapping, int* num_copies);
+
+/* The decode's inputs for n sequences: tables [n, max_blocks] (padded with
+ * the null block) and context_lens [n]. */
+PKV_API pkv_status pkv_pool_block_tables(const pkv_block_pool* pool, const int64_t* seq_ids, int n,
+                                         int32_t* tables, int max_blocks, int32_t* context_lens);
+
 /* Copy seq_id's block table into table[0..max_blocks), padded with the null
  * block 0; *num_blocks and *num_tokens (optional) receive its length.  A
  * NULL table only queries the lengths. */

@@ -37,7 +37,8 @@ EXPORTED = ("pkv_paged_kv_write", "pkv_decode_workspace_size", "pkv_decode_parti
             "pkv_status_string", "pkv_version", "pkv_paged_attention_decode_static",
             "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_set_extra_key", "pkv_pool_num_free_blocks",
             "pkv_pool_num_cached_blocks", "pkv_pool_block_ref_count", "pkv_pool_add_sequence",
-            "pkv_pool_append_token", "pkv_pool_fork", "pkv_pool_free_sequence", "pkv_pool_block_table")
+            "pkv_pool_append_token", "pkv_pool_fork", "pkv_pool_free_sequence", "pkv_pool_block_table",
+            "pkv_pool_append_tokens", "pkv_pool_block_tables")
 STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -94,6 +95,10 @@ def _load() -> ctypes.CDLL:
     lib.pkv_pool_free_sequence.restype = i32
     lib.pkv_pool_block_table.argtypes = [vp, i64, pi32, i32, pi32, pi32]
     lib.pkv_pool_block_table.restype = i32
+    lib.pkv_pool_append_tokens.argtypes = [vp, pi64, pi32, i32, pi64, pi64, pi32]
+    lib.pkv_pool_append_tokens.restype = i32
+    lib.pkv_pool_block_tables.argtypes = [vp, pi64, i32, pi32, i32, pi32]
+    lib.pkv_pool_block_tables.restype = i32
     lib.pkv_status_string.argtypes = [i32]
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_version.argtypes = []
@@ -305,6 +310,37 @@ class BlockPool:
             return None
         _check("pkv_pool_append_token", st)
         return slot.value, src.value, dst.value
+
+    def append_tokens(self, seq_ids, tokens):
+        """One step for many sequences: (slot_mapping int64 [n], copy pairs
+        int64 [c, 2]) -- the inputs of paged_kv_write and copy_blocks -- or
+        None when the pool cannot cover the step."""
+        import numpy as np
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        tok = np.ascontiguousarray(tokens, dtype=np.int32)
+        n = ids.size
+        slots = np.zeros(n, np.int64)
+        pairs = np.zeros((max(n, 1), 2), np.int64)
+        nc = ctypes.c_int32(0)
+        P64, P32 = ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
+        st = lib.pkv_pool_append_tokens(self._h, ids.ctypes.data_as(P64), tok.ctypes.data_as(P32), n,
+                                        slots.ctypes.data_as(P64), pairs.ctypes.data_as(P64), ctypes.byref(nc))
+        if st == 3:
+            return None
+        _check("pkv_pool_append_tokens", st)
+        return slots, pairs[: nc.value]
+
+    def block_tables(self, seq_ids, max_blocks: int):
+        """(tables int32 [n, max_blocks], context_lens int32 [n]) for the decode."""
+        import numpy as np
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        tabs = np.zeros((ids.size, max_blocks), np.int32)
+        cl = np.zeros(ids.size, np.int32)
+        P64, P32 = ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
+        _check("pkv_pool_block_tables", lib.pkv_pool_block_tables(
+            self._h, ids.ctypes.data_as(P64), ids.size, tabs.ctypes.data_as(P32), max_blocks,
+            cl.ctypes.data_as(P32)))
+        return tabs, cl
 
     def fork(self, parent_id: int, child_id: int) -> None:
         _check("pkv_pool_fork", lib.pkv_pool_fork(self._h, parent_id, child_id))

@@ -38,6 +38,7 @@ struct Seq {
     std::vector<int32_t> table;       // physical block per logical block
     std::vector<int32_t> tokens;      // every token (prompt + appended)
     std::vector<uint64_t> hashes;     // chain hash of each full block
+    uint64_t mark = 0;                // last batch call that named this sequence
 };
 
 // 64-bit mixing (splitmix64 finaliser) for the prefix-hash chain.
@@ -59,6 +60,8 @@ struct pkv_block_pool {
     int nfree = 0;
     std::unordered_map<uint64_t, int> cached;   // hash -> block
     std::unordered_map<int64_t, Seq> seqs;
+    uint64_t batch = 0;                         // batch calls so far
+    std::vector<Seq*> batch_seqs;
 
     // ---- free queue
     void q_remove(int b) {
@@ -115,6 +118,37 @@ struct pkv_block_pool {
         uint64_t h = mix(parent ^ mix(extra_key + 0x51ed27ull));
         for (int i = 0; i < bs; ++i) h = mix(h ^ (uint64_t)(uint32_t)toks[i]);
         return h;
+    }
+
+    // One token more for `s`: its slot, and the copy-on-write pair if its
+    // last block was shared.
+    pkv_status append(Seq& s, int32_t token, int64_t* slot, int64_t* cow_src, int64_t* cow_dst) {
+        const int pos = (int)s.tokens.size();
+        int64_t src = -1, dst = -1;
+        if (pos % bs == 0) {
+            // the last block is full: a new block
+            const int b = take_block();
+            if (b == kNone) return PKV_ERR_WORKSPACE;
+            s.table.push_back(b);
+        } else {
+            // the last block has room; a block that is not full carries no hash
+            const int last = s.table.back();
+            if (blocks[last].ref > 1) {
+                // shared with another sequence (a fork): copy before writing
+                const int b = take_block();
+                if (b == kNone) return PKV_ERR_WORKSPACE;
+                src = last;
+                dst = b;
+                release(last);
+                s.table.back() = b;
+            }
+        }
+        s.tokens.push_back(token);
+        if ((int)s.tokens.size() % bs == 0) seal(s, (int)s.tokens.size() / bs - 1);
+        if (slot) *slot = (int64_t)s.table.back() * bs + pos % bs;
+        if (cow_src) *cow_src = src;
+        if (cow_dst) *cow_dst = dst;
+        return PKV_OK;
     }
 
     // Give full block j of `s` its chain hash and make it findable.
@@ -200,34 +234,7 @@ pkv_status pkv_pool_append_token(pkv_block_pool* p, int64_t seq_id, int32_t toke
     if (!p) return PKV_ERR_INVALID_ARG;
     auto it = p->seqs.find(seq_id);
     if (it == p->seqs.end()) return PKV_ERR_INVALID_ARG;
-    Seq& s = it->second;
-    const int bs = p->bs;
-    const int pos = (int)s.tokens.size();
-    int64_t src = -1, dst = -1;
-    if (pos % bs == 0) {
-        // the last block is full: a new block
-        const int b = p->take_block();
-        if (b == kNone) return PKV_ERR_WORKSPACE;
-        s.table.push_back(b);
-    } else {
-        // the last block has room; a block that is not full carries no hash
-        const int last = s.table.back();
-        if (p->blocks[last].ref > 1) {
-            // shared with another sequence (a fork): copy before writing
-            const int b = p->take_block();
-            if (b == kNone) return PKV_ERR_WORKSPACE;
-            src = last;
-            dst = b;
-            p->release(last);
-            s.table.back() = b;
-        }
-    }
-    s.tokens.push_back(token);
-    if ((int)s.tokens.size() % bs == 0) p->seal(s, (int)s.tokens.size() / bs - 1);
-    if (slot) *slot = (int64_t)s.table.back() * bs + pos % bs;
-    if (cow_src) *cow_src = src;
-    if (cow_dst) *cow_dst = dst;
-    return PKV_OK;
+    return p->append(it->second, token, slot, cow_src, cow_dst);
 }
 
 pkv_status pkv_pool_fork(pkv_block_pool* p, int64_t parent_id, int64_t child_id) {
@@ -263,6 +270,52 @@ pkv_status pkv_pool_block_table(const pkv_block_pool* p, int64_t seq_id, int32_t
         if (max_blocks < n) return PKV_ERR_INVALID_ARG;
         std::memcpy(table, s.table.data(), sizeof(int32_t) * n);
         for (int j = n; j < max_blocks; ++j) table[j] = 0;    // padding: the null block
+    }
+    return PKV_OK;
+}
+
+pkv_status pkv_pool_append_tokens(pkv_block_pool* p, const int64_t* seq_ids, const int32_t* tokens, int n,
+                                  int64_t* slot_mapping, int64_t* block_mapping, int* num_copies) {
+    if (!p || n < 0 || (n > 0 && (!seq_ids || !tokens || !slot_mapping || !block_mapping || !num_copies)))
+        return PKV_ERR_INVALID_ARG;
+    // every id must exist and appear once; enough free blocks for the worst case
+    int worst = 0;
+    const uint64_t mark = ++p->batch;
+    p->batch_seqs.resize((size_t)n);
+    for (int i = 0; i < n; ++i) {
+        auto it = p->seqs.find(seq_ids[i]);
+        if (it == p->seqs.end() || it->second.mark == mark) return PKV_ERR_INVALID_ARG;
+        Seq& s = it->second;
+        s.mark = mark;
+        p->batch_seqs[i] = &s;
+        worst += (s.tokens.size() % p->bs == 0) || p->blocks[s.table.back()].ref > 1;
+    }
+    if (worst > p->nfree) return PKV_ERR_WORKSPACE;
+    int nc = 0;
+    for (int i = 0; i < n; ++i) {
+        int64_t src = -1, dst = -1;
+        const pkv_status st = p->append(*p->batch_seqs[i], tokens[i], slot_mapping + i, &src, &dst);
+        if (st != PKV_OK) return st;   // cannot happen after the checks above
+        if (src >= 0) {
+            block_mapping[2 * nc] = src;
+            block_mapping[2 * nc + 1] = dst;
+            ++nc;
+        }
+    }
+    *num_copies = nc;
+    return PKV_OK;
+}
+
+pkv_status pkv_pool_block_tables(const pkv_block_pool* p, const int64_t* seq_ids, int n, int32_t* tables,
+                                 int max_blocks, int32_t* context_lens) {
+    if (!p || n < 0 || max_blocks < 1 || (n > 0 && (!seq_ids || !tables || !context_lens)))
+        return PKV_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        int nb = 0, nt = 0;
+        const pkv_status st =
+            pkv_pool_block_table(p, seq_ids[i], tables + (size_t)i * max_blocks, max_blocks, &nb, &nt);
+        if (st != PKV_OK) return st;
+        context_lens[i] = nt;
     }
     return PKV_OK;
 }

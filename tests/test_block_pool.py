@@ -208,3 +208,40 @@ def test_block_table_padding_and_errors(pkv):
         pool.free_sequence(99)
     with pytest.raises(pkv.PkvError):
         pool.block_table(3, max_blocks=2)                          # too small
+
+
+def test_batched_step_matches_single_appends(pkv):
+    """pkv_pool_append_tokens gives the same slots and copy pairs as one
+    append per sequence (the model), and the batched tables the same rows."""
+    rng = np.random.default_rng(5)
+    pool, model = pkv.BlockPool(64, 16), BlockPoolModel(64, 16)
+    for sid in range(5):
+        toks = rng.integers(1, 50, int(rng.integers(1, 40)), dtype=np.int32)
+        assert pool.add_sequence(sid, toks) == model.add_sequence(sid, list(toks))
+    pool.fork(2, 5)
+    model.fork(2, 5)
+    ids = np.array([5, 0, 2, 1, 4, 3], np.int64)
+    for _ in range(30):
+        toks = rng.integers(1, 50, ids.size, dtype=np.int32)
+        slots, pairs = pool.append_tokens(ids, toks)
+        want = [model.append_token(int(i), int(t)) for i, t in zip(ids, toks)]
+        assert list(slots) == [w[0] for w in want]
+        assert [tuple(p) for p in pairs] == [(w[1], w[2]) for w in want if w[1] >= 0]
+    tabs, cl = pool.block_tables(ids, 8)
+    for row, sid, n in zip(tabs, ids, cl):
+        t = model.block_table(int(sid))
+        assert list(row[: len(t)]) == t and (row[len(t):] == 0).all() and n == len(model.seqs[int(sid)]["tokens"])
+
+
+def test_batched_step_rejects_without_changing(pkv):
+    pool = pkv.BlockPool(4, 4)                       # 3 usable blocks
+    pool.add_sequence(0, np.arange(1, 5, dtype=np.int32))      # 1 full block
+    pool.add_sequence(1, np.arange(1, 9, dtype=np.int32) + 10)  # 2 full blocks
+    free = pool.num_free()
+    assert free == 0
+    assert pool.append_tokens(np.array([0, 1]), np.array([3, 3])) is None    # needs 2 new blocks
+    assert pool.num_free() == free and pool.block_table(0)[1] == 4 and pool.block_table(1)[1] == 8
+    with pytest.raises(pkv.PkvError):
+        pool.append_tokens(np.array([0, 0]), np.array([1, 2]))               # an id twice
+    with pytest.raises(pkv.PkvError):
+        pool.append_tokens(np.array([7]), np.array([1]))                     # unknown id
