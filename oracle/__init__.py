@@ -76,6 +76,9 @@ def _load():
                                                       c_p, c_i, c_i, c_i, c_i, c_i, c_i, c_f,
                                                       c_f, c_f, c_i, c_i]
         lib.oracle_paged_attention_decode.restype = c_i
+        lib.oracle_paged_attention_prefill.argtypes = [c_p, c_p, c_i, c_p, c_p, c_i, c_p, c_i, c_p, c_p,
+                                                       c_i, c_i, c_i, c_i, c_i, c_i, c_f, c_f, c_f, c_i]
+        lib.oracle_paged_attention_prefill.restype = c_i
         lib.oracle_copy_blocks.argtypes = [ctypes.POINTER(c_p), ctypes.POINTER(c_p), c_i, c_p,
                                            c_i, c_i, ctypes.c_size_t]
         lib.oracle_copy_blocks.restype = c_i
@@ -174,6 +177,32 @@ def paged_attention_decode(query, q_dt, key_cache, value_cache, cache_dt, block_
                                            float(v_scale), int(partition), int(threads))
     if rc != 0:
         raise ValueError(f"oracle decode failed with code {rc}")
+    return out
+
+
+def paged_attention_prefill(query, q_dt, key_cache, value_cache, cache_dt, block_tables, context_lens,
+                            query_start, scale, k_scale=1.0, v_scale=1.0, threads=None) -> np.ndarray:
+    """Several query tokens per sequence, causal: the fp64 output [T, Hq, d].
+    query [T, Hq, d] packs every sequence's queries; query_start [S + 1]."""
+    lib = _load()
+    query = _check(np.ascontiguousarray(query), q_dt, "query")
+    _check(key_cache, cache_dt, "key_cache")
+    _check(value_cache, cache_dt, "value_cache")
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    T, Hq, d = query.shape
+    NB, bs, Hkv, d2 = key_cache.shape
+    S = cl.shape[0]
+    assert d2 == d and qs.shape == (S + 1,) and qs[-1] == T and bt.shape[0] == S
+    out = np.zeros((T, Hq, d), dtype=np.float64)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    rc = lib.oracle_paged_attention_prefill(_ptr(out), _ptr(query), q_dt, _ptr(key_cache), _ptr(value_cache),
+                                            cache_dt, _ptr(bt), bt.shape[1], _ptr(cl), _ptr(qs), S, Hq, Hkv, d,
+                                            bs, NB, float(scale), float(k_scale), float(v_scale), int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle prefill failed with code {rc}")
     return out
 
 

@@ -392,6 +392,140 @@ int oracle_paged_attention_decode(double* out, const void* q, int q_dt,
     return J.status;
 }
 
+/* ---------------------------------------------------------------- prefill */
+
+typedef struct {
+    decode_job base;                /* caches, tables, lengths, sizes */
+    const int32_t* query_start;     /* [S + 1] */
+} prefill_job;
+
+/* Several query tokens per sequence (a prefill chunk, or tokens proposed by
+ * speculative decoding): the sequence's last q_len = query_start[s+1] -
+ * query_start[s] tokens are the queries, their K/V already in the cache.
+ * Query i sits at position p = n - q_len + i and attends to tokens 0..p
+ * (causal).  Same gather-then-textbook-softmax as the decode. */
+static int prefill_one(prefill_job* P, int s, double* Kc, double* Vc, double* x, double* qh)
+{
+    decode_job* J = &P->base;
+    int n = J->context_lens[s];
+    int q0 = P->query_start[s], ql = P->query_start[s + 1] - q0;
+    int g = J->Hq / J->Hkv;
+    int t, h, e, kvh, i;
+    if (n < 0 || n > J->MB * J->bs || ql < 0 || ql > n)
+        return -1;
+    for (t = 0; t < n; ++t) {
+        int pb = J->block_tables[(size_t)s * J->MB + t / J->bs];
+        int off = t % J->bs;
+        if (pb < 0 || pb >= J->NB)
+            return -1;
+        for (kvh = 0; kvh < J->Hkv; ++kvh)
+            for (e = 0; e < J->d; ++e) {
+                size_t src = (((size_t)pb * J->bs + off) * J->Hkv + kvh) * J->d + e;
+                size_t dst = ((size_t)t * J->Hkv + kvh) * J->d + e;
+                Kc[dst] = load_elem(J->kc, J->c_dt, src, J->k_scale);
+                Vc[dst] = load_elem(J->vc, J->c_dt, src, J->v_scale);
+            }
+    }
+    for (i = 0; i < ql; ++i) {
+        int pos = n - ql + i;
+        for (h = 0; h < J->Hq; ++h) {
+            double* o = J->out + ((size_t)(q0 + i) * J->Hq + h) * J->d;
+            double m = -INFINITY, l = 0.0;
+            kvh = h / g;
+            for (e = 0; e < J->d; ++e) {
+                qh[e] = load_elem(J->q, J->q_dt, ((size_t)(q0 + i) * J->Hq + h) * J->d + e, 1.0);
+                o[e] = 0.0;
+            }
+            for (t = 0; t <= pos; ++t) {
+                double acc = 0.0;
+                for (e = 0; e < J->d; ++e)
+                    acc += qh[e] * Kc[((size_t)t * J->Hkv + kvh) * J->d + e];
+                x[t] = J->scale * acc;
+                if (x[t] > m)
+                    m = x[t];
+            }
+            for (t = 0; t <= pos; ++t) {
+                double p = exp(x[t] - m);
+                l += p;
+                for (e = 0; e < J->d; ++e)
+                    o[e] += p * Vc[((size_t)t * J->Hkv + kvh) * J->d + e];
+            }
+            for (e = 0; e < J->d; ++e)
+                o[e] /= l;
+        }
+    }
+    return 0;
+}
+
+static void* prefill_worker(void* arg)
+{
+    prefill_job* P = (prefill_job*)arg;
+    decode_job* J = &P->base;
+    size_t maxtok = (size_t)J->MB * J->bs;
+    double* Kc = malloc(sizeof(double) * (maxtok ? maxtok : 1) * J->Hkv * J->d);
+    double* Vc = malloc(sizeof(double) * (maxtok ? maxtok : 1) * J->Hkv * J->d);
+    double* x = malloc(sizeof(double) * (maxtok ? maxtok : 1));
+    double* qh = malloc(sizeof(double) * J->d);
+    if (!Kc || !Vc || !x || !qh) {
+        pthread_mutex_lock(&J->mu);
+        J->status = -2;
+        pthread_mutex_unlock(&J->mu);
+    } else {
+        for (;;) {
+            int s, rc;
+            pthread_mutex_lock(&J->mu);
+            s = J->next++;
+            pthread_mutex_unlock(&J->mu);
+            if (s >= J->S)
+                break;
+            rc = prefill_one(P, s, Kc, Vc, x, qh);
+            if (rc) {
+                pthread_mutex_lock(&J->mu);
+                J->status = rc;
+                pthread_mutex_unlock(&J->mu);
+            }
+        }
+    }
+    free(Kc); free(Vc); free(x); free(qh);
+    return NULL;
+}
+
+/* out: fp64 [T, Hq, d] with T = query_start[S]; q: [T, Hq, d]. */
+int oracle_paged_attention_prefill(double* out, const void* q, int q_dt, const void* key_cache,
+                                   const void* value_cache, int cache_dt, const int32_t* block_tables,
+                                   int MB, const int32_t* context_lens, const int32_t* query_start, int S,
+                                   int Hq, int Hkv, int d, int bs, int NB, float scale, float k_scale,
+                                   float v_scale, int threads)
+{
+    prefill_job P;
+    pthread_t* tid;
+    int i, nt = threads > 0 ? threads : 1;
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || bs <= 0)
+        return -1;
+    memset(&P, 0, sizeof P);
+    P.base.q = q; P.base.q_dt = q_dt; P.base.kc = key_cache; P.base.vc = value_cache;
+    P.base.c_dt = cache_dt; P.base.block_tables = block_tables; P.base.MB = MB;
+    P.base.context_lens = context_lens; P.base.S = S; P.base.Hq = Hq; P.base.Hkv = Hkv;
+    P.base.d = d; P.base.bs = bs; P.base.NB = NB; P.base.scale = (double)scale;
+    P.base.k_scale = cache_dt == OR_E4M3 ? (double)k_scale : 1.0;
+    P.base.v_scale = cache_dt == OR_E4M3 ? (double)v_scale : 1.0;
+    P.base.out = out;
+    P.query_start = query_start;
+    pthread_mutex_init(&P.base.mu, NULL);
+    if (nt > S)
+        nt = S > 0 ? S : 1;
+    tid = malloc(sizeof(pthread_t) * nt);
+    if (!tid)
+        return -2;
+    for (i = 0; i < nt; ++i)
+        pthread_create(&tid[i], NULL, prefill_worker, &P);
+    for (i = 0; i < nt; ++i)
+        pthread_join(tid[i], NULL);
+    free(tid);
+    pthread_mutex_destroy(&P.base.mu);
+    return P.base.status;
+}
+
 /* ------------------------------------------------------------ copy_blocks */
 
 /* Copy-on-write duplication: for every layer and every (src, dst) pair of

@@ -28,6 +28,9 @@ MUTANTS = {
                                "                   (const char*)key_caches[l] + src * block_bytes",
                                "memcpy((char*)key_caches[l] + src * block_bytes,\n"
                                "                   (const char*)key_caches[l] + dst * block_bytes"),
+    "prefill-causal-excludes-self": ("for (t = 0; t <= pos; ++t) {\n                double acc = 0.0;",
+                                     "for (t = 0; t < pos; ++t) {\n                double acc = 0.0;"),
+    "prefill-positions-from-start": ("int pos = n - ql + i;", "int pos = i;"),
     "softmax-sum-skips-last": ("for (t = 0; t < n; ++t) {\n                double p = exp(x[t] - m);",
                                "for (t = 0; t < n; ++t) {\n                double p = t + 1 < n ? exp(x[t] - m) : 0.0;"),
 }

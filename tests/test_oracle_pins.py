@@ -383,3 +383,58 @@ def test_copy_on_write_then_repoint_keeps_outputs(oracle):
                                          w.scale, hv.k_scale, hv.v_scale)
     np.testing.assert_array_equal(out, out2)
     assert args
+
+
+# ------------------------------------------------------------------ prefill
+
+def _sdpa_causal_chunk(q, k_ctx, v_ctx, scale):
+    """Brute force for a chunk of q_len queries at the end of an n-token
+    sequence: torch's fp64 SDPA with an explicit mask (query i sees tokens
+    0 .. n - q_len + i).  q [q_len, Hq, d]; k_ctx/v_ctx [n, Hkv, d]."""
+    ql, Hq, d = q.shape
+    n, Hkv, _ = k_ctx.shape
+    g = Hq // Hkv
+    qt = torch.from_numpy(q.astype(np.float64)).permute(1, 0, 2)                 # [Hq, ql, d]
+    kt = torch.from_numpy(k_ctx.astype(np.float64)).permute(1, 0, 2).repeat_interleave(g, dim=0)
+    vt = torch.from_numpy(v_ctx.astype(np.float64)).permute(1, 0, 2).repeat_interleave(g, dim=0)
+    pos = torch.arange(n - ql, n)[:, None]
+    mask = torch.arange(n)[None, :] <= pos                                          # [ql, n]
+    out = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=scale)
+    return out.permute(1, 0, 2).numpy()
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (8, 1), (6, 6)])
+def test_prefill_brute_force(oracle, Hq, Hkv):
+    rng = np.random.default_rng(200 + Hq + Hkv)
+    d, bs = 64, 16
+    lens = [1, 16, 17, 40, 70, 33]
+    qlens = [1, 3, 17, 40, 5, 0]                    # a whole-sequence chunk, ragged chunks, an empty one
+    _, kp, vp, tabs, cl, kctx, vctx = _scatter_case(rng, lens, Hq, Hkv, d, bs)
+    qs = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    q = rng.standard_normal((int(qs[-1]), Hq, d)).astype(np.float32)
+    out = oracle.paged_attention_prefill(q, oracle.F32, kp, vp, oracle.F32, tabs, cl, qs, 0.125)
+    for s in range(len(lens)):
+        if qlens[s] == 0:
+            continue
+        ref = _sdpa_causal_chunk(q[qs[s]:qs[s + 1]], kctx[s], vctx[s], 0.125)
+        np.testing.assert_allclose(out[qs[s]:qs[s + 1]], ref, atol=1e-12, rtol=0)
+
+
+def test_prefill_whole_sequence_is_causal_attention(oracle):
+    rng = np.random.default_rng(7)
+    _, kp, vp, tabs, cl, kctx, vctx = _scatter_case(rng, [50], 4, 2, 64, 16)
+    q = rng.standard_normal((50, 4, 64)).astype(np.float32)
+    out = oracle.paged_attention_prefill(q, oracle.F32, kp, vp, oracle.F32, tabs, cl, np.array([0, 50]), 0.125)
+    qt = torch.from_numpy(q.astype(np.float64)).permute(1, 0, 2)
+    kt = torch.from_numpy(kctx[0].astype(np.float64)).permute(1, 0, 2).repeat_interleave(2, dim=0)
+    vt = torch.from_numpy(vctx[0].astype(np.float64)).permute(1, 0, 2).repeat_interleave(2, dim=0)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=True, scale=0.125)
+    np.testing.assert_allclose(out, ref.permute(1, 0, 2).numpy(), atol=1e-12, rtol=0)
+
+
+def test_prefill_one_query_is_decode(oracle):
+    rng = np.random.default_rng(8)
+    q, kp, vp, tabs, cl, _, _ = _scatter_case(rng, [1, 30, 99], 8, 2, 64, 16)
+    dec = oracle.paged_attention_decode(q, oracle.F32, kp, vp, oracle.F32, tabs, cl, 0.125)
+    pre = oracle.paged_attention_prefill(q, oracle.F32, kp, vp, oracle.F32, tabs, cl, np.arange(4), 0.125)
+    np.testing.assert_array_equal(dec, pre)
