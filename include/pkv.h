@@ -70,7 +70,8 @@ enum {
     PKV_DEVERR_CONTEXT_LEN = 2,   /* context_lens[s] < 0 or > max_context_len (clamped) */
     PKV_DEVERR_SLOT = 3,          /* slot_mapping[i] >= NB * bs */
     PKV_DEVERR_COPY_PAIR = 4,     /* a copy pair with an id outside [0, NB) */
-    PKV_DEVERR_TIMEOUT = 5        /* a staged copy did not land within ~2 s; the kernel gave up */
+    PKV_DEVERR_TIMEOUT = 5,       /* a staged copy did not land within ~2 s; the kernel gave up */
+    PKV_DEVERR_QUERY_LEN = 6      /* prefill: a sequence's query count is < 0 or > its length (skipped) */
 };
 
 /*
@@ -261,6 +262,42 @@ PKV_API pkv_status pkv_paged_attention_decode_static(void* out, const void* quer
                                                      float scale, float k_scale, float v_scale,
                                                      int partition_size,
                                                      int32_t* err_word, pkv_stream_t stream);
+
+/*
+ * paged_attention_prefill -- several query tokens per sequence, causal: a
+ * chunk of a prompt (chunked prefill) or the tokens a speculative decoder
+ * proposes, attending through the same block tables.
+ *
+ * Source: "LLM推論の基礎とvLLMの内部", section 6: chunked prefill runs a
+ * long prompt in per-step pieces next to other requests' decodes; section 3:
+ * the V1 scheduler gives every request the tokens it still has to compute,
+ * speculative ones included, without separate prefill and decode phases.
+ *
+ * query/out [T, Hq, d] pack every sequence's queries: those of sequence s
+ * are rows query_start[s] .. query_start[s+1] (int32 [S+1], device, rising,
+ * query_start[S] = T).  They are the sequence's last q_len tokens, whose
+ * K/V are already in the cache (pkv_paged_kv_write first): query i sits at
+ * position p = context_lens[s] - q_len + i and attends to tokens 0..p.
+ * partition_size splits long key ranges like the decode's (0 = library
+ * choice, -1 = never, > 0 = that many tokens, a multiple of bs); then
+ * `workspace` must hold pkv_prefill_workspace_size(...) bytes, its first
+ * 256 bytes zero before first use.  max_query_len >= every q_len and
+ * max_context_len >= every length (host values that size the launch).
+ * Supported: bf16 query and bf16 cache (tensor cores), d in {64, 128}, bs in
+ * {16, 32}; anything else returns PKV_ERR_UNSUPPORTED.
+ */
+PKV_API size_t pkv_prefill_workspace_size(int S, int num_query_tokens, int max_query_len, int Hq, int Hkv, int d,
+                                          int bs, int max_context_len, int partition_size);
+PKV_API pkv_status pkv_paged_attention_prefill(void* out, const void* query, pkv_dtype q_dtype,
+                                               const void* key_cache, const void* value_cache,
+                                               pkv_dtype cache_dtype,
+                                               const int32_t* block_tables, int MB,
+                                               const int32_t* context_lens, const int32_t* query_start,
+                                               int S, int num_query_tokens, int max_query_len,
+                                               int max_context_len, int Hq, int Hkv, int d, int bs, int NB,
+                                               float scale, int partition_size,
+                                               void* workspace, size_t workspace_bytes,
+                                               int32_t* err_word, pkv_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Host block manager: the bookkeeping that produces the block tables, slot

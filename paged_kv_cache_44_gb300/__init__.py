@@ -38,7 +38,8 @@ EXPORTED = ("pkv_paged_kv_write", "pkv_decode_workspace_size", "pkv_decode_parti
             "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_set_extra_key", "pkv_pool_num_free_blocks",
             "pkv_pool_num_cached_blocks", "pkv_pool_block_ref_count", "pkv_pool_add_sequence",
             "pkv_pool_append_token", "pkv_pool_fork", "pkv_pool_free_sequence", "pkv_pool_block_table",
-            "pkv_pool_append_tokens", "pkv_pool_block_tables")
+            "pkv_pool_append_tokens", "pkv_pool_block_tables", "pkv_prefill_workspace_size",
+            "pkv_paged_attention_prefill")
 STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -99,6 +100,11 @@ def _load() -> ctypes.CDLL:
     lib.pkv_pool_append_tokens.restype = i32
     lib.pkv_pool_block_tables.argtypes = [vp, pi64, i32, pi32, i32, pi32]
     lib.pkv_pool_block_tables.restype = i32
+    lib.pkv_prefill_workspace_size.argtypes = [i32] * 9
+    lib.pkv_prefill_workspace_size.restype = sz
+    lib.pkv_paged_attention_prefill.argtypes = [vp, vp, i32, vp, vp, i32, vp, i32, vp, vp, i32, i32, i32, i32,
+                                                i32, i32, i32, i32, i32, f32, i32, vp, sz, vp, vp]
+    lib.pkv_paged_attention_prefill.restype = i32
     lib.pkv_status_string.argtypes = [i32]
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_version.argtypes = []
@@ -228,6 +234,41 @@ def paged_attention_decode_static(out: torch.Tensor, query: torch.Tensor, key_ca
         dtype_code(key_cache.dtype), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), S,
         int(max_context_len), Hq, Hkv, d, bs, NB, float(scale), float(k_scale), float(v_scale),
         int(partition_size), _ptr(err_word), _stream(stream)))
+    return out
+
+
+def prefill_workspace_size(S: int, num_query_tokens: int, max_query_len: int, Hq: int, Hkv: int, d: int,
+                           bs: int, max_context_len: int, partition_size: int = 0) -> int:
+    return int(lib.pkv_prefill_workspace_size(S, num_query_tokens, max_query_len, Hq, Hkv, d, bs, max_context_len,
+                                              partition_size))
+
+
+def paged_attention_prefill(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                            value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                            query_start: torch.Tensor, max_query_len: int, max_context_len: int,
+                            scale: Optional[float] = None, partition_size: int = 0,
+                            workspace: Optional[torch.Tensor] = None, err_word: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    """Several query tokens per sequence, causal.  query/out [T, Hq, d];
+    query_start int32 [S+1] (device); caches [NB, bs, Hkv, d]."""
+    T, Hq, d = query.shape
+    NB, bs, Hkv, d2 = key_cache.shape
+    S = context_lens.numel()
+    if d2 != d or out.shape != query.shape or out.dtype != query.dtype or query_start.numel() != S + 1:
+        raise ValueError("shape or dtype mismatch")
+    if query_start.dtype != torch.int32 or context_lens.dtype != torch.int32 or block_tables.dtype != torch.int32:
+        raise ValueError("query_start, context_lens and block_tables must be int32")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        n = prefill_workspace_size(S, T, max_query_len, Hq, Hkv, d, bs, max_context_len, partition_size)
+        workspace = torch.zeros(max(n, 256), dtype=torch.uint8, device=query.device)
+    _check("paged_attention_prefill", lib.pkv_paged_attention_prefill(
+        _ptr(out), _ptr(query), dtype_code(query.dtype), _ptr(key_cache), _ptr(value_cache),
+        dtype_code(key_cache.dtype), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+        _ptr(query_start), S, T, int(max_query_len), int(max_context_len), Hq, Hkv, d, bs, NB, float(scale),
+        int(partition_size), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err_word),
+        _stream(stream)))
     return out
 
 

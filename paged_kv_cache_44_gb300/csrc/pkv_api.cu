@@ -203,6 +203,107 @@ pkv_status pkv_paged_attention_decode(void* out, const void* query, pkv_dtype q_
                                          PKV_DECODE_AUTO);
 }
 
+}  // extern "C"
+
+namespace pkv {
+namespace {
+
+// Prefill partition size (0 = no split; -1 = invalid): tiles of 16 (query,
+// head) rows already give parallelism, so split only when there are few.
+int resolve_prefill_partition(int S, int max_q_len, int Hq, int Hkv, int d, int bs, int max_ctx, int req) {
+    if (!decode_shape_ok(S, Hq, Hkv, d, bs, max_ctx) || max_q_len < 0 || max_q_len > max_ctx) return -1;
+    if (req > 0) return req % bs == 0 ? req : -1;
+    if (req == -1) return 0;
+    if (req != 0) return -1;
+    const long long tiles = (long long)S * Hkv * ((max_q_len * (Hq / Hkv) + 15) / 16);
+    if (tiles == 0 || tiles >= kTargetUnits / 2 || max_ctx <= kMinDefaultPartition) return 0;
+    int P = 1 << 20;
+    while (P > kMinDefaultPartition && tiles * ((max_ctx + P - 1) / P) < kTargetUnits / 2) P >>= 1;
+    return P >= max_ctx ? 0 : P;
+}
+
+struct PrefillPlan {
+    int P, Pmax;
+    bool split;
+    size_t ml_offset, acc_offset, bytes;
+};
+
+PrefillPlan plan_prefill(int T, int Hq, int d, int max_ctx, int P) {
+    PrefillPlan pl{};
+    pl.P = P;
+    pl.Pmax = P > 0 ? (max_ctx > 0 ? (max_ctx + P - 1) / P : 1) : 1;
+    pl.split = P > 0 && pl.Pmax > 1;
+    pl.bytes = kWorkspaceHeaderBytes;
+    if (!pl.split) return pl;
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t units = (size_t)T * Hq * pl.Pmax;
+    pl.ml_offset = kWorkspaceHeaderBytes;
+    pl.acc_offset = up(pl.ml_offset + units * 2 * sizeof(float));
+    pl.bytes = up(pl.acc_offset + units * d * sizeof(float));
+    return pl;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+size_t pkv_prefill_workspace_size(int S, int num_query_tokens, int max_query_len, int Hq, int Hkv, int d, int bs,
+                                  int max_context_len, int partition_size) {
+    if (num_query_tokens < 0) return 0;
+    const int P = resolve_prefill_partition(S, max_query_len, Hq, Hkv, d, bs, max_context_len, partition_size);
+    if (P < 0) return 0;
+    return plan_prefill(num_query_tokens, Hq, d, max_context_len, P).bytes;
+}
+
+pkv_status pkv_paged_attention_prefill(void* out, const void* query, pkv_dtype q_dtype, const void* key_cache,
+                                       const void* value_cache, pkv_dtype cache_dtype, const int32_t* block_tables,
+                                       int MB, const int32_t* context_lens, const int32_t* query_start, int S,
+                                       int num_query_tokens, int max_query_len, int max_context_len, int Hq,
+                                       int Hkv, int d, int bs, int NB, float scale, int partition_size,
+                                       void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                       pkv_stream_t stream) {
+    if (S < 0 || MB < 1 || NB < 1 || Hkv < 1 || Hq < 1 || max_context_len < 0 || num_query_tokens < 0 ||
+        max_query_len < 0 || max_query_len > max_context_len)
+        return PKV_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return PKV_ERR_INVALID_ARG;
+    if (q_dtype != PKV_BF16 || cache_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (!(d == 64 || d == 128) || !(bs == 16 || bs == 32)) return PKV_ERR_UNSUPPORTED;
+    if (S > 65535 || (long long)NB * bs >= (1LL << 31)) return PKV_ERR_UNSUPPORTED;
+    if ((long long)max_context_len > (long long)MB * bs) return PKV_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    if (partition_size < -1 || (partition_size > 0 && partition_size % bs != 0)) return PKV_ERR_INVALID_ARG;
+    if (S == 0 || num_query_tokens == 0) return PKV_OK;
+    if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens || !query_start)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
+        (reinterpret_cast<uintptr_t>(query_start) & 3u))
+        return PKV_ERR_INVALID_ARG;
+    const int P = resolve_prefill_partition(S, max_query_len, Hq, Hkv, d, bs, max_context_len, partition_size);
+    if (P < 0) return PKV_ERR_INVALID_ARG;
+    const PrefillPlan pl = plan_prefill(num_query_tokens, Hq, d, max_context_len, P);
+    if (pl.split && (!workspace || workspace_bytes < pl.bytes)) return PKV_ERR_WORKSPACE;
+    if (workspace && !aligned16(workspace)) return PKV_ERR_INVALID_ARG;
+    DecodeParams p{};
+    p.out = out; p.q = query; p.kc = key_cache; p.vc = value_cache;
+    p.block_tables = block_tables; p.context_lens = context_lens; p.err = err_word;
+    p.S = S; p.MB = MB; p.Hq = Hq; p.Hkv = Hkv; p.g = Hq / Hkv; p.d = d; p.bs = bs; p.NB = NB;
+    p.P = pl.P > 0 ? pl.P : MB * bs;
+    p.Pmax = pl.Pmax;
+    p.max_ctx = max_context_len;
+    p.logit_scale_log2 = scale * kLog2e;
+    p.out_scale = 1.f;
+    if (workspace && workspace_bytes >= kWorkspaceHeaderBytes) p.sched = reinterpret_cast<unsigned*>(workspace);
+    if (pl.split) {
+        char* ws = static_cast<char*>(workspace);
+        p.part_ml = reinterpret_cast<float*>(ws + pl.ml_offset);
+        p.part_acc = reinterpret_cast<float*>(ws + pl.acc_offset);
+    }
+    return from_cuda(launch_prefill_tc(p, query_start, num_query_tokens, max_query_len, num_sms_current(), pl.split,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
 pkv_status pkv_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
                            const int64_t* block_mapping, int P, int NB, size_t block_bytes, int32_t* err_word,
                            pkv_stream_t stream) {

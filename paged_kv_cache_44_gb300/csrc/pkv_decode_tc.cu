@@ -40,9 +40,12 @@
 
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
+#include "pkv_tc_common.cuh"
 
 namespace pkv {
 namespace {
+
+using namespace tc;
 
 // Tuning knobs: workers per CTA, stages per worker, tokens per stage, for
 // bf16 and for E4M3 caches (E4M3 does more arithmetic per byte and wants
@@ -105,122 +108,6 @@ struct Cfg {
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
     static_assert(kCtlOff % 1024 == 0 && kCtlBytes % 16 == 0, "trailer alignment");
 };
-
-// Shared-memory byte address of logical byte `x` (a multiple of 16, plus an
-// offset inside the 16-byte chunk) of token row `tok` in a stage part laid
-// out by the tensor copies: rows of kBoxRow bytes, one region of kTok rows
-// per 128-byte half, 16-byte chunks permuted by the swizzle (128-byte mode:
-// chunk ^= row % 8; 64-byte mode: chunk ^= (row / 2) % 4).
-template <int RB, int TOK>
-__device__ __forceinline__ uint32_t swz(uint32_t part, int tok, int x) {
-    if constexpr (RB >= 128) {
-        const int h = x >> 7, j = (x >> 4) & 7;
-        return part + h * (TOK * 128) + tok * 128 + ((j ^ (tok & 7)) << 4) + (x & 15);
-    } else {
-        const int j = (x >> 4) & 3;
-        return part + tok * 64 + ((j ^ ((tok >> 1) & 3)) << 4) + (x & 15);
-    }
-}
-
-// ------------------------------------------------------------- PTX wrappers
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void tensor_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void fence_barrier_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
-    uint32_t d;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
-    return d;
-}
-template <bool FP8>
-__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-    if constexpr (FP8) {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-            "{%0,%1,%2,%3};"
-            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-    } else {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-            "{%0,%1,%2,%3};"
-            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-    }
-}
-__device__ __forceinline__ float fast_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-// four E4M3 codes (bytes 0..3 of w) -> two registers of two fp16 each
-// (lo = bytes 0,1; hi = bytes 2,3), exactly; the 16-bit halves of w are
-// taken as register halves, with no shifts
-__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    asm("{\n\t.reg .b16 l16, h16;\n\t"
-        "mov.b32 {l16, h16}, %2;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %0, l16;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %1, h16;\n\t}"
-        : "=r"(lo), "=r"(hi)
-        : "r"(w));
-}
-template <bool FP8>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-    if constexpr (FP8) {
-        __half2 h = __floats2half2_rn(lo, hi);
-        return *reinterpret_cast<uint32_t*>(&h);
-    } else {
-        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-        return *reinterpret_cast<uint32_t*>(&h);
-    }
-}
 
 // ------------------------------------------------------------------- units
 

@@ -68,5 +68,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, pkv_dtype q_dt, pkv_dtype c_
                              cudaStream_t st);
 cudaError_t launch_decode_reduce(const DecodeParams& p, pkv_dtype q_dt, cudaStream_t st);
 bool decode_tc_supports(pkv_dtype q_dt, pkv_dtype c_dt, int d, int bs, int NB);
+cudaError_t launch_prefill_tc(const DecodeParams& p, const int32_t* query_start, int T, int max_q_len, int num_sms,
+                              bool merge, cudaStream_t st);
 
 }  // namespace pkv

@@ -1,0 +1,105 @@
+"""Paged attention for several query tokens per sequence (chunked prefill,
+speculative-decoding verification) through the C ABI, against the oracle."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import oracle as O
+    import paged_kv_cache_44_gb300 as pkv
+    from tests.gpu_cases import assert_close, to_device
+
+
+def _case(name, lens, qlens, Hq=None, Hkv=None, d=None, seed=7):
+    w = W.make(name, S=len(lens), lengths=np.array(lens), seed=seed)
+    if Hq is not None:
+        w = dataclasses.replace(w, Hq=Hq, Hkv=Hkv, d=d)
+    hv = W.host_values(w)
+    qs = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    q32 = W.host_normal(seed, "prefill-query", (int(qs[-1]), w.Hq, w.d))
+    return w, hv, qs, q32
+
+
+def _run(w, hv, qs, q32, partition, dev="cuda", query_start=None, err=None):
+    kc = to_device(hv.k_pool, W.DT_BF16, dev)
+    vc = to_device(hv.v_pool, W.DT_BF16, dev)
+    q = to_device(q32, W.DT_BF16, dev)
+    out = torch.full_like(q, float("nan"))
+    qs_dev = torch.from_numpy(qs if query_start is None else query_start).to(dev)
+    pkv.paged_attention_prefill(out, q, kc, vc, torch.from_numpy(w.block_tables).to(dev),
+                                torch.from_numpy(w.context_lens).to(dev), qs_dev, int(np.diff(qs).max()),
+                                w.max_context_len, scale=w.scale, partition_size=partition, err_word=err)
+    return out
+
+
+def _ref(w, hv, qs, q32):
+    return O.paged_attention_prefill(W.bf16_bits(q32), O.BF16, W.bf16_bits(hv.k_pool), W.bf16_bits(hv.v_pool),
+                                     O.BF16, w.block_tables, w.context_lens, qs, w.scale)
+
+
+CASES = [
+    # (workload for bs, lens, qlens, Hq, Hkv, d)
+    ("qwen2.5-1.5b", [1, 17, 40, 300, 64, 1000], [1, 17, 5, 128, 0, 33], 8, 2, 128),
+    ("qwen2.5-1.5b", [2048, 100, 513], [7, 100, 1], 28, 4, 128),
+    ("qwen2.5-1.5b", [77, 500], [77, 250], 8, 8, 64),
+    ("fp8-bs32", [33, 700, 64], [16, 65, 64], 16, 2, 128),
+    ("fp8-bs32", [1500, 31], [4, 31], 8, 1, 64),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-g{c[3] // c[4]}-d{c[5]}" for c in CASES])
+@pytest.mark.parametrize("partition", [-1, 0, 64])
+def test_prefill_matches_oracle(case, partition):
+    name, lens, qlens, Hq, Hkv, d = case
+    w, hv, qs, q32 = _case(name, lens, qlens, Hq, Hkv, d)
+    if partition > 0 and partition % w.bs:
+        partition = 2 * w.bs
+    out = _run(w, hv, qs, q32, partition)
+    assert_close(out, _ref(w, hv, qs, q32), W.DT_BF16, f"prefill P={partition}")
+
+
+def test_prefill_one_query_equals_decode():
+    w, hv, qs, q32 = _case("qwen2.5-1.5b", [5, 200, 1025], [1, 1, 1], 12, 2, 128)
+    out = _run(w, hv, qs, q32, 0)
+    q = to_device(q32, W.DT_BF16, "cuda")
+    dec = torch.empty_like(q)
+    ws = pkv.make_workspace(w.S, w.Hq, w.Hkv, w.d, w.bs, w.max_context_len, -1)
+    pkv.paged_attention_decode(dec, q, to_device(hv.k_pool, W.DT_BF16, "cuda"),
+                               to_device(hv.v_pool, W.DT_BF16, "cuda"), torch.from_numpy(w.block_tables).cuda(),
+                               torch.from_numpy(w.context_lens).cuda(), w.max_context_len, scale=w.scale,
+                               partition_size=-1, workspace=ws)
+    ref = _ref(w, hv, qs, q32)
+    assert_close(out, ref, W.DT_BF16, "prefill q_len=1")
+    assert_close(dec, ref, W.DT_BF16, "decode")
+
+
+def test_prefill_chunked_long_prompt():
+    """A Qwen2.5-7B-shaped batch: 8 sequences with 512-token chunks at the
+    end of 1,024 .. 4,096-token contexts, and 24 decoding sequences (one
+    query) next to them, as one call."""
+    rng = np.random.default_rng(12)
+    lens = list(rng.integers(1024, 4097, 8)) + list(rng.integers(16, 3000, 24))
+    qlens = [512] * 8 + [1] * 24
+    w, hv, qs, q32 = _case("qwen2.5-1.5b", lens, qlens, 28, 4, 128, seed=13)
+    out = _run(w, hv, qs, q32, 0)
+    assert_close(out, _ref(w, hv, qs, q32), W.DT_BF16, "mixed chunk + decode batch")
+
+
+def test_prefill_bad_query_count_reported():
+    w, hv, qs, q32 = _case("qwen2.5-1.5b", [20, 30], [4, 4], 8, 2, 128)
+    bad = np.array([0, 4, 40], np.int32)            # second sequence: 36 queries > 30 tokens
+    q32 = W.host_normal(7, "prefill-query-bad", (40, w.Hq, w.d))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = _run(w, hv, bad, q32, -1, query_start=bad, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 6
+    ref = O.paged_attention_prefill(W.bf16_bits(q32[:4]), O.BF16, W.bf16_bits(hv.k_pool), W.bf16_bits(hv.v_pool),
+                                    O.BF16, w.block_tables[:1], w.context_lens[:1], np.array([0, 4], np.int32),
+                                    w.scale)
+    assert_close(out[:4], ref, W.DT_BF16, "valid sequence of a batch with a bad one")
