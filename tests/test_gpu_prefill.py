@@ -26,14 +26,15 @@ def _case(name, lens, qlens, Hq=None, Hkv=None, d=None, seed=7):
     return w, hv, qs, q32
 
 
-def _run(w, hv, qs, q32, partition, dev="cuda", query_start=None, err=None):
+def _run(w, hv, qs, q32, partition, dev="cuda", query_start=None, err=None, max_query_len=None):
     kc = to_device(hv.k_pool, W.DT_BF16, dev)
     vc = to_device(hv.v_pool, W.DT_BF16, dev)
     q = to_device(q32, W.DT_BF16, dev)
     out = torch.full_like(q, float("nan"))
     qs_dev = torch.from_numpy(qs if query_start is None else query_start).to(dev)
+    mq = int(np.diff(qs).max()) if max_query_len is None else max_query_len
     pkv.paged_attention_prefill(out, q, kc, vc, torch.from_numpy(w.block_tables).to(dev),
-                                torch.from_numpy(w.context_lens).to(dev), qs_dev, int(np.diff(qs).max()),
+                                torch.from_numpy(w.context_lens).to(dev), qs_dev, mq,
                                 w.max_context_len, scale=w.scale, partition_size=partition, err_word=err)
     return out
 
@@ -96,7 +97,7 @@ def test_prefill_bad_query_count_reported():
     bad = np.array([0, 4, 40], np.int32)            # second sequence: 36 queries > 30 tokens
     q32 = W.host_normal(7, "prefill-query-bad", (40, w.Hq, w.d))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = _run(w, hv, bad, q32, -1, query_start=bad, err=err)
+    out = _run(w, hv, bad, q32, -1, query_start=bad, err=err, max_query_len=4)   # what the host believes
     torch.cuda.synchronize()
     assert int(err.item()) == 6
     ref = O.paged_attention_prefill(W.bf16_bits(q32[:4]), O.BF16, W.bf16_bits(hv.k_pool), W.bf16_bits(hv.v_pool),

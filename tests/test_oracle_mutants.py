@@ -45,7 +45,7 @@ def test_pins_catch_mutant(tmp_path, name):
     for f in ("__init__.py", "pkv_oracle.c"):
         shutil.copy(os.path.join(src_dir, f), dst / f)
     c = (dst / "pkv_oracle.c").read_text()
-    assert c.count(old) == 1, name
+    assert c.count(old) >= 1, name              # a mistake in shared logic is planted everywhere
     (dst / "pkv_oracle.c").write_text(c.replace(old, new))
     env = dict(os.environ, PKV_ORACLE_DIR=str(dst))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
