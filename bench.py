@@ -79,6 +79,27 @@ def copy_bytes(w: W.Workload) -> int:
     return len(w.cow_pairs) * (2 * 2 * blk + 16)
 
 
+def prefill_flops(w: W.Workload, qlens: np.ndarray) -> int:
+    """Algorithmic FLOPs of paged attention over query chunks: every (query,
+    head) with the keys its causal range allows (the chunk's query i of a
+    sequence of n tokens sees n - q_len + i + 1 keys), 2 d for the logit and
+    2 d for the weighted sum per key."""
+    n = w.context_lens.astype(np.int64)
+    ql = qlens.astype(np.int64)
+    keys = ql * (n - ql) + ql * (ql + 1) // 2          # sum over the chunk of (pos + 1)
+    return int(keys.sum()) * w.Hq * 4 * w.d
+
+
+def prefill_bytes(w: W.Workload, qlens: np.ndarray) -> int:
+    """Algorithmic bytes: every query read and output written once, the K/V
+    of each sequence's tokens once, table entries and lengths."""
+    T = int(qlens.sum())
+    bq = ELEM[w.q_dtype]
+    kv = int(w.context_lens.astype(np.int64).sum()) * w.Hkv * w.d * 2 * ELEM[w.cache_dtype]
+    nblk = -(-w.context_lens.astype(np.int64) // w.bs)
+    return 2 * T * w.Hq * w.d * bq + kv + int(nblk.sum()) * 4 + w.S * 8
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -311,24 +332,16 @@ def run_reference(args, w: W.Workload):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, w: W.Workload):
+def device_caches(w: W.Workload, seed: int, dev, stream):
+    """K and V pools of workload `w` filled on the device from seeded draws
+    (bf16: the draws' upper halves; fp8: the library's own write with a
+    per-tensor scale amax / 448).  Returns (key_cache, value_cache,
+    k_scale, v_scale)."""
     import torch
     import paged_kv_cache_44_gb300 as pkv
-
-    ws, rank, local = dist_setup()
-    if ws > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local if ws > 1 else 0)
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.Stream(device=dev)
-
-    # ---- inputs, resident in HBM before timing
     tdt = {W.DT_F32: torch.float32, W.DT_BF16: torch.bfloat16, W.DT_E4M3: torch.uint8}
     shape = (w.NB, w.bs, w.Hkv, w.d)
     numel = int(np.prod(shape))
-    seed = w.seed + 7919 * rank
     k_scale = v_scale = 1.0
     caches = []
     with torch.cuda.stream(stream):
@@ -355,7 +368,26 @@ def run_ours(args, w: W.Workload):
                     cache[c0:c0 + x.numel()] = W.device_bf16_from_draws(x) if w.cache_dtype == W.DT_BF16 else x
                 cache = cache.view(shape)
             caches.append(cache)
-        kc, vc = caches
+    return caches[0], caches[1], k_scale, v_scale
+
+
+def run_ours(args, w: W.Workload):
+    import torch
+    import paged_kv_cache_44_gb300 as pkv
+
+    ws, rank, local = dist_setup()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    # ---- inputs, resident in HBM before timing
+    seed = w.seed + 7919 * rank
+    kc, vc, k_scale, v_scale = device_caches(w, seed, dev, stream)
+    with torch.cuda.stream(stream):
 
         def dev_vals(tag, shp):
             x = W.device_normal(seed, tag, int(np.prod(shp)), dev).view(shp)
@@ -498,6 +530,192 @@ def run_ours(args, w: W.Workload):
         dist.destroy_process_group()
 
 
+def peak_bf16(sustained: bool):
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)
+        return float(rec["bf16_tflops_sustained" if sustained else "bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return (1700.0 if sustained else 1900.0), "fallback"
+
+
+def run_prefill(args, w: W.Workload):
+    """Paged attention over query chunks: a step is one call over the
+    workload's packed queries (chunked prefill next to decodes, or
+    speculative verification), the K/V pools resident in HBM.  Reports both
+    TFLOP/s and GB/s; the roofline takes the bound the arithmetic intensity
+    selects (FLOPs per byte above the ratio of the measured peaks: tensor)."""
+    import torch
+    import paged_kv_cache_44_gb300 as pkv
+
+    ws, rank, local = dist_setup()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    if w.cache_dtype != W.DT_BF16 or w.q_dtype != W.DT_BF16:
+        raise SystemExit("query chunks: bf16 query and cache only")
+    seed = w.seed + 7919 * rank
+    qlens = W.query_lens(w)
+    qs_host = W.query_start(qlens)
+    T, mq, mc = int(qs_host[-1]), int(qlens.max()), w.max_context_len
+    kc, vc, _, _ = device_caches(w, seed, dev, stream)
+    with torch.cuda.stream(stream):
+        q = W.device_bf16_from_draws(W.device_normal(seed, 21, T * w.Hq * w.d, dev)).view(T, w.Hq, w.d)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    qs = torch.from_numpy(qs_host).to(dev)
+    out = torch.empty_like(q)
+    P = args.partition if args.partition is not None else 0
+    wsb = pkv.prefill_workspace_size(w.S, T, mq, w.Hq, w.Hkv, w.d, w.bs, mc, P)
+    wsp = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+    split = wsb > 256
+    torch.cuda.synchronize(dev)
+
+    def step(qq=q, btab=bt, clen=cl, qst=qs):
+        pkv.paged_attention_prefill(out, qq, kc, vc, btab, clen, qst, mq, mc, scale=w.scale, partition_size=P,
+                                    workspace=wsp, stream=stream)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier(device_ids=[dev.index])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(uuid) as clk:
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    (ms_total,) = max_over_ranks([t0.elapsed_time(t1)], dev)
+    ms_step = ms_total / args.steps
+
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    h_in = {k: pin(v) for k, v in dict(q=q, bt=bt, cl=cl, qs=qs).items()}
+    d_in = {k: torch.empty_like(v, device=dev) for k, v in h_in.items()}
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    d2h = h_out.numel() * h_out.element_size()
+    e2e_steps = max(3, min(args.steps, 100))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for k in h_in:
+                d_in[k].copy_(h_in[k], non_blocking=True)
+        step(qq=d_in["q"], btab=d_in["bt"], clen=d_in["cl"], qst=d_in["qs"])
+        with torch.cuda.stream(stream):
+            h_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    w0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    (e2e_s,) = max_over_ranks([(time.perf_counter() - w0) / e2e_steps], dev)
+
+    flops, nbytes = prefill_flops(w, qlens), prefill_bytes(w, qlens)
+    tflops = ws * flops / (ms_step * 1e-3) / 1e12
+    gbs = whole_job_gbs(ws, nbytes, ms_step)
+    hbm, hbm_kind = peak_hbm()
+    tc, tc_kind = peak_bf16(sustained=ms_total > 2000.0)
+    tensor_bound = flops / nbytes > tc * 1e12 / (hbm * 1e9)
+    per_launch_tf, per_launch_gbs = flops / (ms_step * 1e-3) / 1e12, nbytes / (ms_step * 1e-3) / 1e9
+    if tensor_bound:
+        metric, value, unit = "paged attention over query chunks, TFLOP/s", tflops, "TFLOP/s"
+        roof = {"bound": "tensor", "achieved": round(per_launch_tf, 2), "peak": tc, "unit": "TFLOP/s",
+                "frac": round(per_launch_tf / tc, 4),
+                "peak_kind": tc_kind + (" bf16 sustained" if ms_total > 2000.0 else " bf16 burst"),
+                "note": "mma.sync m16n8k16 (legacy tensor path) against a cuBLAS bf16 peak"}
+        e2e_v = ws * flops / e2e_s / 1e12
+    else:
+        metric, value, unit = "paged attention over query chunks, KV GB/s", gbs, "GB/s"
+        roof = {"bound": "hbm", "achieved": round(per_launch_gbs, 2), "peak": hbm, "unit": "GB/s",
+                "frac": round(per_launch_gbs / hbm, 4), "peak_kind": hbm_kind}
+        e2e_v = whole_job_gbs(ws, nbytes, e2e_s * 1e3)
+    roof.update({"traffic": None, "kernel": "paged_attention_prefill", "algorithmic_flops_per_launch": flops,
+                 "algorithmic_bytes_per_launch": nbytes, "launch_ms": round(ms_step, 5)})
+    line = {
+        "component": "prefill", "metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "bs": w.bs,
+                   "query_tokens": T, "max_query_len": mq, "max_context_len": mc,
+                   "kv_tokens": int(w.context_lens.astype(np.int64).sum()),
+                   "partition_size": P, "split": bool(split),
+                   "l2": "inputs larger than L2" if nbytes > 2 * 129e6 else "not flushed: inputs near L2 size",
+                   "step": "paged_attention_prefill over every sequence's query chunk"},
+        "tflops": round(tflops, 2), "kv_gbs": round(gbs, 2),
+        "query_tokens_per_s": round(ws * T / (ms_step * 1e-3), 1),
+        "roofline": roof,
+        "e2e": {"value": round(e2e_v, 2), "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_s * 1e3, 4)},
+        "gpu_launches": (2 if split else 1) * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = prefill_cpu_baseline(w, qlens, args.cpu_seconds, tensor_bound)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def prefill_cpu_baseline(w: W.Workload, qlens: np.ndarray, budget: float, tensor_bound: bool):
+    """The oracle on a bounded sample of the workload: batches of one
+    sequence per host thread (the oracle's unit of parallel work), each
+    keeping the last min(q_len, 16) queries of its chunk (the same keys per
+    query as in the full chunk), until about `budget` seconds."""
+    import oracle as O
+    threads = cpu_threads()
+    rng = np.random.default_rng(w.seed)
+    order = list(rng.permutation(w.S))
+    flops = nbytes = 0
+    spent, seqs, queries, keys, calls = 0.0, 0, 0, 0, 0
+    used = 1
+    while order and spent < budget:
+        take, tok = 0, 0                         # at most 2^17 K/V tokens of host draws per call
+        while take < min(threads, len(order)) and (take == 0 or tok + int(w.context_lens[order[take]]) <= 1 << 17):
+            tok += int(w.context_lens[order[take]])
+            take += 1
+        batch = np.array(sorted(order[:take]), np.int64)
+        order = order[take:]
+        used = max(used, take)
+        sw = W.sub_workload(w, batch)
+        hv = W.host_values(sw)
+        ql = np.minimum(qlens[batch], 16).astype(np.int32)
+        qst = W.query_start(ql)
+        q = W.bf16_bits(W.host_normal(w.seed, "chunk-query:%d" % calls, (int(qst[-1]), w.Hq, w.d)))
+        t0 = time.perf_counter()
+        O.paged_attention_prefill(q, O.BF16, W.bf16_bits(hv.k_pool), W.bf16_bits(hv.v_pool), O.BF16,
+                                  sw.block_tables, sw.context_lens, qst, w.scale, threads=threads)
+        spent += time.perf_counter() - t0
+        flops += prefill_flops(sw, ql)
+        nbytes += prefill_bytes(sw, ql)
+        seqs, queries, keys, calls = seqs + len(batch), queries + int(ql.sum()), keys + int(sw.context_lens.sum()), \
+            calls + 1
+    value = flops / spent / 1e12 if tensor_bound else nbytes / spent / 1e9
+    return {"value": round(value, 6), "unit": "TFLOP/s" if tensor_bound else "GB/s", "cores": used,
+            "kind": "oracle",
+            "sample": "%d sequences in %d calls, the last <=16 queries of each chunk (%d query tokens, %d K/V "
+                      "tokens), %.1f s" % (seqs, calls, queries, keys, spent)}
+
+
 def run_block_manager(args):
     """Host block manager throughput, serving-like: S sequences whose
     prompts share a system prefix are admitted (prefix-cache lookups and
@@ -545,22 +763,31 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="qwen2.5-72b-long", choices=sorted(W.SHAPES))
+    ap.add_argument("--workload", default=None, choices=sorted(W.SHAPES),
+                    help="default: qwen2.5-72b-long (decode-step), qwen2.5-7b-chunked (prefill)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "cuda_cores", "tensor_cores"])
     ap.add_argument("--partition", type=int, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--S", type=int, default=None, help="fewer sequences (small profiling cases)")
-    ap.add_argument("--component", default="decode-step", choices=["decode-step", "block-manager"],
-                    help="block-manager: time the host block manager instead (prints its own line)")
+    ap.add_argument("--component", default="decode-step", choices=["decode-step", "prefill", "block-manager"],
+                    help="prefill: paged attention over query chunks; block-manager: the host block "
+                         "manager (each prints its own line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.component == "block-manager":
         run_block_manager(args)
         return
+    if args.workload is None:
+        args.workload = "qwen2.5-7b-chunked" if args.component == "prefill" else "qwen2.5-72b-long"
     w = W.make(args.workload, S=args.S) if args.S else W.make(args.workload)
+    if args.component == "prefill":
+        if args.impl == "reference":
+            ap.error("--impl reference times the decode step")
+        run_prefill(args, w)
+        return
     if args.impl == "reference":
         run_reference(args, w)
     else:

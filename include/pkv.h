@@ -71,7 +71,8 @@ enum {
     PKV_DEVERR_SLOT = 3,          /* slot_mapping[i] >= NB * bs */
     PKV_DEVERR_COPY_PAIR = 4,     /* a copy pair with an id outside [0, NB) */
     PKV_DEVERR_TIMEOUT = 5,       /* a staged copy did not land within ~2 s; the kernel gave up */
-    PKV_DEVERR_QUERY_LEN = 6      /* prefill: a sequence's query count is < 0 or > its length (skipped) */
+    PKV_DEVERR_QUERY_LEN = 6      /* prefill: a sequence's queries are < 0, more than its length or
+                                     than max_query_len, or outside [0, T) (the sequence is skipped) */
 };
 
 /*

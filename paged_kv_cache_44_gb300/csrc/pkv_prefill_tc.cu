@@ -72,8 +72,8 @@ struct __align__(16) PUnit {
 // Unit id -> coordinates; false for ids that name no work.  Ids run
 // partition-major, then sequence, K/V head, row tile: the tiles of one key
 // range are claimed together, so they share the K/V reads in L2.
-__device__ __forceinline__ bool punit_of(const DecodeParams& p, const int32_t* query_start, unsigned long long u,
-                                         int rt_max, PUnit& x) {
+__device__ __forceinline__ bool punit_of(const DecodeParams& p, const int32_t* query_start, int T,
+                                         unsigned long long u, int rt_max, PUnit& x) {
     const unsigned long long per_part = (unsigned long long)p.S * p.Hkv * rt_max;
     x.part = (int)(u / per_part);
     const unsigned long long rem = u - (unsigned long long)x.part * per_part;
@@ -84,7 +84,10 @@ __device__ __forceinline__ bool punit_of(const DecodeParams& p, const int32_t* q
     int n = __ldg(p.context_lens + x.s);
     x.q0 = __ldg(query_start + x.s);
     x.ql = __ldg(query_start + x.s + 1) - x.q0;
-    if (n < 0 || n > p.max_ctx || x.ql < 0 || x.ql > n) {
+    // a length above the host bound, a query count outside [0, n], queries
+    // outside [0, T) or more rows than the launch has tiles for: skipped
+    if (n < 0 || n > p.max_ctx || x.ql < 0 || x.ql > n || x.q0 < 0 || x.q0 + x.ql > T ||
+        x.ql * p.g > rt_max * kRows) {
         if (x.part == 0 && r2 == 0) report(p.err, PKV_DEVERR_QUERY_LEN);
         return false;
     }
@@ -102,7 +105,7 @@ __device__ __forceinline__ bool punit_of(const DecodeParams& p, const int32_t* q
 
 template <int D>
 __global__ void __launch_bounds__(kPWarps * 32, 1)
-    prefill_tc_kernel(const __grid_constant__ DecodeParams p, const int32_t* __restrict__ query_start,
+    prefill_tc_kernel(const __grid_constant__ DecodeParams p, const int32_t* __restrict__ query_start, int T,
                       const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       unsigned long long total_units, int rt_max) {
     using C = PCfg<D>;
@@ -152,7 +155,7 @@ __global__ void __launch_bounds__(kPWarps * 32, 1)
             static_next += total_warps;
             if (v >= total_units) return false;
             PUnit x;
-            if (!punit_of(p, query_start, v, rt_max, x)) continue;
+            if (!punit_of(p, query_start, T, v, rt_max, x)) continue;
             u = v;
             return true;
         }
@@ -165,7 +168,7 @@ __global__ void __launch_bounds__(kPWarps * 32, 1)
                 claiming = false;
                 return false;
             }
-            punit_of(p, query_start, u, rt_max, iu);
+            punit_of(p, query_start, T, u, rt_max, iu);
             if (lane == 0) {
                 int4* e = queue + 3 * (q_tail % C::kQueue);
                 e[0] = make_int4(iu.s, iu.kvh, iu.rt, iu.part);
@@ -445,7 +448,7 @@ __global__ void __launch_bounds__(kPWarps * 32, 1)
 // programmatic dependent of the prefill kernel.
 template <int D>
 __global__ void __launch_bounds__(256) prefill_merge_kernel(DecodeParams p, const int32_t* __restrict__ query_start,
-                                                            int T) {
+                                                            int T, int row_cap) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr int E = D / 32;
     const int lane = threadIdx.x & 31;
@@ -459,7 +462,9 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(DecodeParams p, cons
     }
     const int s = lo;
     const int n = p.context_lens[s], q0 = query_start[s], ql = query_start[s + 1] - q0;
-    if (n < 0 || n > p.max_ctx || ql < 0 || ql > n || tq >= q0 + ql) return;
+    if (n < 0 || n > p.max_ctx || ql < 0 || ql > n || q0 < 0 || q0 + ql > T || ql * p.g > row_cap ||
+        tq >= q0 + ql)
+        return;                                // the sequence the main kernel skipped
     const int kvh = h / p.g, row = (tq - q0) * p.g + (h - kvh * p.g);
     const int rows = ql * p.g, rt = row / kRows;
     const int last_row = min(rt * kRows + kRows - 1, rows - 1);
@@ -547,7 +552,7 @@ cudaError_t launch_prefill_d(const DecodeParams& p, const int32_t* query_start, 
     const unsigned long long want = (units + kPWarps - 1) / kPWarps;
     int grid = (int)(want < (unsigned long long)num_sms ? want : (unsigned long long)num_sms);
     if (grid < 1) grid = 1;
-    kern<<<grid, kPWarps * 32, C::kSmemBytes, st>>>(p, query_start, kmap, vmap, units, rt_max > 0 ? rt_max : 1);
+    kern<<<grid, kPWarps * 32, C::kSmemBytes, st>>>(p, query_start, T, kmap, vmap, units, rt_max > 0 ? rt_max : 1);
     e = cudaGetLastError();
     if (e != cudaSuccess || !merge) return e;
     cudaLaunchConfig_t cfg = {};
@@ -560,7 +565,7 @@ cudaError_t launch_prefill_d(const DecodeParams& p, const int32_t* query_start, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_merge_kernel<D>, p, query_start, T);
+    return cudaLaunchKernelEx(&cfg, prefill_merge_kernel<D>, p, query_start, T, (rt_max > 0 ? rt_max : 1) * kRows);
 }
 
 }  // namespace

@@ -104,3 +104,63 @@ def test_prefill_bad_query_count_reported():
                                     O.BF16, w.block_tables[:1], w.context_lens[:1], np.array([0, 4], np.int32),
                                     w.scale)
     assert_close(out[:4], ref, W.DT_BF16, "valid sequence of a batch with a bad one")
+
+
+def test_prefill_queries_outside_the_batch_are_skipped():
+    """query_start naming rows past T, or more queries than max_query_len
+    covers: skipped and reported, nothing written out of bounds."""
+    w, hv, qs, q32 = _case("qwen2.5-1.5b", [20, 30, 25], [4, 4, 4], 8, 2, 128)
+    cases = [(bad, mq, part) for bad, mq in ((np.array([0, 4, 8, 40], np.int32), 4),
+                                             (np.array([0, 4, 12, 12], np.int32), 4)) for part in (-1, 16)]
+    for bad, mq, part in cases:
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = _run(w, hv, qs, q32, part, query_start=bad, err=err, max_query_len=mq)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 6
+        ref = _ref(w, hv, qs, q32)
+        assert_close(out[:4], ref[:4], W.DT_BF16, "the valid first sequence")
+
+
+FULL = [("qwen2.5-7b-chunked", 4, 6), ("qwen2.5-72b-spec", 3, 5)]
+
+
+@pytest.mark.parametrize("name,nseq,nq", FULL, ids=[f[0] for f in FULL])
+def test_full_size_query_chunks(name, nseq, nq):
+    """The query-chunk workloads at full size, in the launch configuration
+    the benchmark times (default partitioning).  Sampled sequences hold host
+    draws; for each, a few of its queries (first, last, random) are
+    recomputed by the oracle as one-query sequences ending at the query's
+    position, which is the causal rule itself.  Every output is finite and
+    bounded by max |V| (a convex combination)."""
+    from tests.gpu_cases import build_case
+    w = W.make(name)
+    c = build_case(w, sample=nseq)
+    qlens = W.query_lens(w)
+    qs = W.query_start(qlens)
+    T = int(qs[-1])
+    q32 = W.host_normal(w.seed, "chunk-query", (T, w.Hq, w.d))
+    q = to_device(q32, W.DT_BF16)
+    out = torch.empty_like(q)
+    P = 0
+    wsb = pkv.prefill_workspace_size(w.S, T, int(qlens.max()), w.Hq, w.Hkv, w.d, w.bs, w.max_context_len, P)
+    wsp = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    pkv.paged_attention_prefill(out, q, c.k_cache, c.v_cache, c.block_tables, c.context_lens,
+                                torch.from_numpy(qs).cuda(), int(qlens.max()), w.max_context_len, scale=w.scale,
+                                partition_size=P, workspace=wsp)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    rows, tabs, lens = [], [], []
+    for j, s in enumerate(c.seqs):
+        ql, n = int(qlens[s]), int(w.context_lens[s])
+        pick = sorted({0, ql - 1} | set(rng.integers(0, ql, max(0, nq - 2)).tolist()))
+        for i in pick:
+            rows.append(int(qs[s]) + i)
+            tabs.append(c.ow.block_tables[j])
+            lens.append(n - ql + i + 1)
+    rows_a = np.array(rows)
+    ref = O.paged_attention_prefill(W.bf16_bits(q32[rows_a]), O.BF16, c.o_k, c.o_v, O.BF16, np.stack(tabs),
+                                    np.array(lens, np.int32), np.arange(len(rows) + 1, dtype=np.int32), w.scale)
+    assert_close(out[torch.from_numpy(rows_a).cuda()], ref, W.DT_BF16, f"{name} sampled queries")
+    of = out.float()
+    assert torch.isfinite(of).all()
+    assert float(of.abs().max()) <= float(c.v_cache.float().abs().max()) * 1.01 + 1e-3

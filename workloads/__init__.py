@@ -102,7 +102,31 @@ def _lengths(name: str, rng: np.random.Generator, S: int) -> np.ndarray:
         return np.full(S, 32768, np.int64)
     if name.startswith("fp8"):
         return rng.integers(256, 16384, size=S, endpoint=True)
+    if name == "qwen2.5-7b-chunked":
+        p = min(S, CHUNKED_PROMPTS)
+        chunk_end = CHUNK_TOKENS * rng.integers(1, 8192 // CHUNK_TOKENS, size=p, endpoint=True)
+        dec = np.clip(np.rint(rng.lognormal(mean=math.log(1024.0), sigma=1.0, size=S - p)), 1, 8192)
+        return np.concatenate([chunk_end, dec]).astype(np.int64)
+    if name == "qwen2.5-72b-spec":
+        return np.full(S, 32768, np.int64)
     raise KeyError(name)
+
+
+def query_lens(w: "Workload") -> np.ndarray:
+    """Queries per sequence: the chunk of the chunked workload's prompts,
+    the speculative tokens of the verification workload, else one."""
+    if w.name == "qwen2.5-7b-chunked":
+        q = np.ones(w.S, np.int64)
+        q[: min(w.S, CHUNKED_PROMPTS)] = CHUNK_TOKENS
+        return np.minimum(q, w.context_lens).astype(np.int32)
+    if w.name == "qwen2.5-72b-spec":
+        return np.minimum(SPEC_QUERIES, w.context_lens).astype(np.int32)
+    return np.minimum(1, w.context_lens).astype(np.int32)
+
+
+def query_start(qlens: np.ndarray) -> np.ndarray:
+    """Offsets of each sequence's queries in the packed query array [S + 1]."""
+    return np.concatenate([[0], np.cumsum(np.asarray(qlens, np.int64))]).astype(np.int32)
 
 
 SHAPES: Dict[str, dict] = {
@@ -124,7 +148,22 @@ SHAPES: Dict[str, dict] = {
                      cache_dtype=DT_E4M3, partition_size=0, seed=5),
     "fp8-bs32": dict(S=128, Hq=28, Hkv=4, d=128, bs=32, q_dtype=DT_BF16,
                      cache_dtype=DT_E4M3, partition_size=0, seed=5),
+    # Several queries per sequence.  Chunked prefill next to decodes
+    # ("LLM推論の基礎とvLLMの内部", section 6): 16 prompts each computing a
+    # 512-token chunk that ends at a multiple of 512 up to 8,192, beside 48
+    # decoding sequences (one query each) -- 8,240 query tokens in one step.
+    "qwen2.5-7b-chunked": dict(S=64, Hq=28, Hkv=4, d=128, bs=16, q_dtype=DT_BF16,
+                               cache_dtype=DT_BF16, partition_size=0, seed=6),
+    # Speculative verification at long context (same page, section 3: a
+    # request's tokens to compute include its speculative ones): the
+    # accepted token plus 4 proposed ones, 5 queries per sequence.
+    "qwen2.5-72b-spec": dict(S=32, Hq=64, Hkv=8, d=128, bs=16, q_dtype=DT_BF16,
+                             cache_dtype=DT_BF16, partition_size=0, seed=8),
 }
+
+CHUNK_TOKENS = 512          # prefill chunk of the chunked workload
+CHUNKED_PROMPTS = 16        # sequences of that workload computing a chunk
+SPEC_QUERIES = 5            # 1 accepted + 4 proposed tokens
 
 COW_PAIRS = 64
 
