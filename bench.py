@@ -578,7 +578,7 @@ def run_prefill(args, w: W.Workload):
 
     def step(qq=q, btab=bt, clen=cl, qst=qs):
         pkv.paged_attention_prefill(out, qq, kc, vc, btab, clen, qst, mq, mc, scale=w.scale, partition_size=P,
-                                    workspace=wsp, stream=stream)
+                                    workspace=wsp, stream=stream, kernel=args.prefill_kernel)
 
     def barrier():
         if ws > 1:
@@ -639,15 +639,16 @@ def run_prefill(args, w: W.Workload):
         metric, value, unit = "paged attention over query chunks, TFLOP/s", tflops, "TFLOP/s"
         roof = {"bound": "tensor", "achieved": round(per_launch_tf, 2), "peak": tc, "unit": "TFLOP/s",
                 "frac": round(per_launch_tf / tc, 4),
-                "peak_kind": tc_kind + (" bf16 sustained" if ms_total > 2000.0 else " bf16 burst"),
-                "note": "mma.sync m16n8k16 (legacy tensor path) against a cuBLAS bf16 peak"}
+                "peak_kind": tc_kind + (" bf16 sustained" if ms_total > 2000.0 else " bf16 burst")}
         e2e_v = ws * flops / e2e_s / 1e12
     else:
         metric, value, unit = "paged attention over query chunks, KV GB/s", gbs, "GB/s"
         roof = {"bound": "hbm", "achieved": round(per_launch_gbs, 2), "peak": hbm, "unit": "GB/s",
                 "frac": round(per_launch_gbs / hbm, 4), "peak_kind": hbm_kind}
         e2e_v = whole_job_gbs(ws, nbytes, e2e_s * 1e3)
-    roof.update({"traffic": None, "kernel": "paged_attention_prefill", "algorithmic_flops_per_launch": flops,
+    kname = "tcgen05" if args.prefill_kernel == "auto" else args.prefill_kernel
+    roof.update({"traffic": None, "kernel": "paged_attention_prefill (%s)" % kname,
+                 "algorithmic_flops_per_launch": flops,
                  "algorithmic_bytes_per_launch": nbytes, "launch_ms": round(ms_step, 5)})
     line = {
         "component": "prefill", "metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": ws,
@@ -656,7 +657,7 @@ def run_prefill(args, w: W.Workload):
         "config": {"workload": w.name, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "bs": w.bs,
                    "query_tokens": T, "max_query_len": mq, "max_context_len": mc,
                    "kv_tokens": int(w.context_lens.astype(np.int64).sum()),
-                   "partition_size": P, "split": bool(split),
+                   "partition_size": P, "split": bool(split), "prefill_kernel": kname,
                    "l2": "inputs larger than L2" if nbytes > 2 * 129e6 else "not flushed: inputs near L2 size",
                    "step": "paged_attention_prefill over every sequence's query chunk"},
         "tflops": round(tflops, 2), "kv_gbs": round(gbs, 2),
@@ -767,6 +768,7 @@ def main():
                     help="default: qwen2.5-72b-long (decode-step), qwen2.5-7b-chunked (prefill)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "cuda_cores", "tensor_cores"])
     ap.add_argument("--partition", type=int, default=None)
+    ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "tcgen05", "mma_sync"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -285,7 +285,8 @@ PKV_API pkv_status pkv_paged_attention_decode_static(void* out, const void* quer
  * 256 bytes zero before first use.  max_query_len >= every q_len and
  * max_context_len >= every length (host values that size the launch).
  * Supported: bf16 query and bf16 cache (tensor cores), d in {64, 128}, bs in
- * {16, 32}; anything else returns PKV_ERR_UNSUPPORTED.
+ * {16, 32}; anything else returns PKV_ERR_UNSUPPORTED.  Runs the tcgen05
+ * kernel (PKV_PREFILL_AUTO of pkv_paged_attention_prefill_ex).
  */
 PKV_API size_t pkv_prefill_workspace_size(int S, int num_query_tokens, int max_query_len, int Hq, int Hkv, int d,
                                           int bs, int max_context_len, int partition_size);
@@ -299,6 +300,31 @@ PKV_API pkv_status pkv_paged_attention_prefill(void* out, const void* query, pkv
                                                float scale, int partition_size,
                                                void* workspace, size_t workspace_bytes,
                                                int32_t* err_word, pkv_stream_t stream);
+
+/* Kernel choice for pkv_paged_attention_prefill_ex. */
+typedef enum {
+    PKV_PREFILL_AUTO = 0,         /* the tcgen05 kernel */
+    PKV_PREFILL_MMA_SYNC = 1,     /* warp-level mma.sync: tiles of 16 (query, head) rows, one warp each */
+    PKV_PREFILL_TCGEN05 = 2       /* tcgen05.mma with tensor-memory accumulators: tiles of 128 rows,
+                                     one CTA each */
+} pkv_prefill_kernel;
+
+/*
+ * Same as pkv_paged_attention_prefill, with an explicit kernel choice
+ * (`kernel` is a pkv_prefill_kernel).  Both kernels compute the same
+ * function with the same partitioning and workspace; the choice exists so
+ * the two can be measured against each other.
+ */
+PKV_API pkv_status pkv_paged_attention_prefill_ex(void* out, const void* query, pkv_dtype q_dtype,
+                                                  const void* key_cache, const void* value_cache,
+                                                  pkv_dtype cache_dtype,
+                                                  const int32_t* block_tables, int MB,
+                                                  const int32_t* context_lens, const int32_t* query_start,
+                                                  int S, int num_query_tokens, int max_query_len,
+                                                  int max_context_len, int Hq, int Hkv, int d, int bs, int NB,
+                                                  float scale, int partition_size,
+                                                  void* workspace, size_t workspace_bytes,
+                                                  int32_t* err_word, pkv_stream_t stream, int kernel);
 
 /* ------------------------------------------------------------------------
  * Host block manager: the bookkeeping that produces the block tables, slot

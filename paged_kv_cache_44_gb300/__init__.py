@@ -39,7 +39,7 @@ EXPORTED = ("pkv_paged_kv_write", "pkv_decode_workspace_size", "pkv_decode_parti
             "pkv_pool_num_cached_blocks", "pkv_pool_block_ref_count", "pkv_pool_add_sequence",
             "pkv_pool_append_token", "pkv_pool_fork", "pkv_pool_free_sequence", "pkv_pool_block_table",
             "pkv_pool_append_tokens", "pkv_pool_block_tables", "pkv_prefill_workspace_size",
-            "pkv_paged_attention_prefill")
+            "pkv_paged_attention_prefill", "pkv_paged_attention_prefill_ex")
 STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -105,6 +105,8 @@ def _load() -> ctypes.CDLL:
     lib.pkv_paged_attention_prefill.argtypes = [vp, vp, i32, vp, vp, i32, vp, i32, vp, vp, i32, i32, i32, i32,
                                                 i32, i32, i32, i32, i32, f32, i32, vp, sz, vp, vp]
     lib.pkv_paged_attention_prefill.restype = i32
+    lib.pkv_paged_attention_prefill_ex.argtypes = lib.pkv_paged_attention_prefill.argtypes + [i32]
+    lib.pkv_paged_attention_prefill_ex.restype = i32
     lib.pkv_status_string.argtypes = [i32]
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_version.argtypes = []
@@ -237,6 +239,9 @@ def paged_attention_decode_static(out: torch.Tensor, query: torch.Tensor, key_ca
     return out
 
 
+PREFILL_KERNELS = {"auto": 0, "mma_sync": 1, "tcgen05": 2}
+
+
 def prefill_workspace_size(S: int, num_query_tokens: int, max_query_len: int, Hq: int, Hkv: int, d: int,
                            bs: int, max_context_len: int, partition_size: int = 0) -> int:
     return int(lib.pkv_prefill_workspace_size(S, num_query_tokens, max_query_len, Hq, Hkv, d, bs, max_context_len,
@@ -248,9 +253,12 @@ def paged_attention_prefill(out: torch.Tensor, query: torch.Tensor, key_cache: t
                             query_start: torch.Tensor, max_query_len: int, max_context_len: int,
                             scale: Optional[float] = None, partition_size: int = 0,
                             workspace: Optional[torch.Tensor] = None, err_word: Optional[torch.Tensor] = None,
-                            stream=None) -> torch.Tensor:
+                            stream=None, kernel: str = "auto") -> torch.Tensor:
     """Several query tokens per sequence, causal.  query/out [T, Hq, d];
-    query_start int32 [S+1] (device); caches [NB, bs, Hkv, d]."""
+    query_start int32 [S+1] (device); caches [NB, bs, Hkv, d].  kernel:
+    "auto" / "tcgen05" (tensor-memory accumulators) or "mma_sync"."""
+    if kernel not in PREFILL_KERNELS:
+        raise ValueError(f"kernel must be one of {sorted(PREFILL_KERNELS)}")
     T, Hq, d = query.shape
     NB, bs, Hkv, d2 = key_cache.shape
     S = context_lens.numel()
@@ -263,12 +271,12 @@ def paged_attention_prefill(out: torch.Tensor, query: torch.Tensor, key_cache: t
     if workspace is None:
         n = prefill_workspace_size(S, T, max_query_len, Hq, Hkv, d, bs, max_context_len, partition_size)
         workspace = torch.zeros(max(n, 256), dtype=torch.uint8, device=query.device)
-    _check("paged_attention_prefill", lib.pkv_paged_attention_prefill(
+    _check("paged_attention_prefill", lib.pkv_paged_attention_prefill_ex(
         _ptr(out), _ptr(query), dtype_code(query.dtype), _ptr(key_cache), _ptr(value_cache),
         dtype_code(key_cache.dtype), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
         _ptr(query_start), S, T, int(max_query_len), int(max_context_len), Hq, Hkv, d, bs, NB, float(scale),
         int(partition_size), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err_word),
-        _stream(stream)))
+        _stream(stream), PREFILL_KERNELS[kernel]))
     return out
 
 

@@ -19,6 +19,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // workspace size and the launch always agree.
 constexpr long long kTargetUnits = 152LL * 8 * 4;
 constexpr int kMinDefaultPartition = 512;
+constexpr long long kPrefillTargetUnits = 152LL * 4;
 constexpr int kHeadSet = 8;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -215,10 +216,12 @@ int resolve_prefill_partition(int S, int max_q_len, int Hq, int Hkv, int d, int 
     if (req > 0) return req % bs == 0 ? req : -1;
     if (req == -1) return 0;
     if (req != 0) return -1;
-    const long long tiles = (long long)S * Hkv * ((max_q_len * (Hq / Hkv) + 15) / 16);
-    if (tiles == 0 || tiles >= kTargetUnits / 2 || max_ctx <= kMinDefaultPartition) return 0;
+    // counted in tiles of 128 rows (the tcgen05 kernel's unit); about four
+    // units per SM keep the persistent CTAs busy to the end
+    const long long tiles = (long long)S * Hkv * ((max_q_len * (long long)(Hq / Hkv) + 127) / 128);
+    if (tiles == 0 || tiles >= kPrefillTargetUnits || max_ctx <= kMinDefaultPartition) return 0;
     int P = 1 << 20;
-    while (P > kMinDefaultPartition && tiles * ((max_ctx + P - 1) / P) < kTargetUnits / 2) P >>= 1;
+    while (P > kMinDefaultPartition && tiles * ((max_ctx + P - 1) / P) < kPrefillTargetUnits) P >>= 1;
     return P >= max_ctx ? 0 : P;
 }
 
@@ -263,6 +266,21 @@ pkv_status pkv_paged_attention_prefill(void* out, const void* query, pkv_dtype q
                                        int Hkv, int d, int bs, int NB, float scale, int partition_size,
                                        void* workspace, size_t workspace_bytes, int32_t* err_word,
                                        pkv_stream_t stream) {
+    return pkv_paged_attention_prefill_ex(out, query, q_dtype, key_cache, value_cache, cache_dtype, block_tables, MB,
+                                          context_lens, query_start, S, num_query_tokens, max_query_len,
+                                          max_context_len, Hq, Hkv, d, bs, NB, scale, partition_size, workspace,
+                                          workspace_bytes, err_word, stream, PKV_PREFILL_AUTO);
+}
+
+pkv_status pkv_paged_attention_prefill_ex(void* out, const void* query, pkv_dtype q_dtype, const void* key_cache,
+                                          const void* value_cache, pkv_dtype cache_dtype,
+                                          const int32_t* block_tables, int MB, const int32_t* context_lens,
+                                          const int32_t* query_start, int S, int num_query_tokens,
+                                          int max_query_len, int max_context_len, int Hq, int Hkv, int d, int bs,
+                                          int NB, float scale, int partition_size, void* workspace,
+                                          size_t workspace_bytes, int32_t* err_word, pkv_stream_t stream,
+                                          int kernel) {
+    if (kernel < PKV_PREFILL_AUTO || kernel > PKV_PREFILL_TCGEN05) return PKV_ERR_INVALID_ARG;
     if (S < 0 || MB < 1 || NB < 1 || Hkv < 1 || Hq < 1 || max_context_len < 0 || num_query_tokens < 0 ||
         max_query_len < 0 || max_query_len > max_context_len)
         return PKV_ERR_INVALID_ARG;
@@ -300,8 +318,12 @@ pkv_status pkv_paged_attention_prefill(void* out, const void* query, pkv_dtype q
         p.part_ml = reinterpret_cast<float*>(ws + pl.ml_offset);
         p.part_acc = reinterpret_cast<float*>(ws + pl.acc_offset);
     }
-    return from_cuda(launch_prefill_tc(p, query_start, num_query_tokens, max_query_len, num_sms_current(), pl.split,
-                                       reinterpret_cast<cudaStream_t>(stream)));
+    auto st = reinterpret_cast<cudaStream_t>(stream);
+    if (kernel == PKV_PREFILL_MMA_SYNC)
+        return from_cuda(launch_prefill_tc(p, query_start, num_query_tokens, max_query_len, num_sms_current(),
+                                           pl.split, st));
+    return from_cuda(launch_prefill_umma(p, query_start, num_query_tokens, max_query_len, num_sms_current(),
+                                         pl.split, st));
 }
 
 pkv_status pkv_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,

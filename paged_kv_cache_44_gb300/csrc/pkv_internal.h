@@ -1,6 +1,7 @@
 // Internal launch interface between the C ABI (pkv_api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -70,5 +71,12 @@ cudaError_t launch_decode_reduce(const DecodeParams& p, pkv_dtype q_dt, cudaStre
 bool decode_tc_supports(pkv_dtype q_dt, pkv_dtype c_dt, int d, int bs, int NB);
 cudaError_t launch_prefill_tc(const DecodeParams& p, const int32_t* query_start, int T, int max_q_len, int num_sms,
                               bool merge, cudaStream_t st);
+cudaError_t launch_prefill_umma(const DecodeParams& p, const int32_t* query_start, int T, int max_q_len, int num_sms,
+                                bool merge, cudaStream_t st);
+cudaError_t launch_prefill_merge(const DecodeParams& p, const int32_t* query_start, int T, int tile_rows,
+                                 int max_q, cudaStream_t st);
+// 2-D tensor map over a bf16 K or V cache [NB * bs tokens, Hkv * d]: boxes of
+// 64 values by min(bs, 32) tokens, 128-byte swizzle
+bool prefill_encode_kv_map(CUtensorMap* map, const void* base, const DecodeParams& p);
 
 }  // namespace pkv

@@ -30,6 +30,7 @@
 
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
+#include "pkv_qtile.cuh"
 #include "pkv_tc_common.cuh"
 
 namespace pkv {
@@ -62,51 +63,10 @@ struct PCfg {
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
-struct __align__(16) PUnit {
-    int s, kvh, rt, part;      // sequence, K/V head, row tile, key partition
-    int k0, k1;                // key tokens [k0, k1)
-    int n, ql;                 // sequence length, queries in the chunk
-    int q0, np, rows, pad;     // first query token, partitions of the tile, rows of the sequence
-};
-
-// Unit id -> coordinates; false for ids that name no work.  Ids run
-// partition-major, then sequence, K/V head, row tile: the tiles of one key
-// range are claimed together, so they share the K/V reads in L2.
-__device__ __forceinline__ bool punit_of(const DecodeParams& p, const int32_t* query_start, int T,
-                                         unsigned long long u, int rt_max, PUnit& x) {
-    const unsigned long long per_part = (unsigned long long)p.S * p.Hkv * rt_max;
-    x.part = (int)(u / per_part);
-    const unsigned long long rem = u - (unsigned long long)x.part * per_part;
-    x.s = (int)(rem / ((unsigned long long)p.Hkv * rt_max));
-    const int r2 = (int)(rem - (unsigned long long)x.s * p.Hkv * rt_max);
-    x.kvh = r2 / rt_max;
-    x.rt = r2 - x.kvh * rt_max;
-    int n = __ldg(p.context_lens + x.s);
-    x.q0 = __ldg(query_start + x.s);
-    x.ql = __ldg(query_start + x.s + 1) - x.q0;
-    // a length above the host bound, a query count outside [0, n], queries
-    // outside [0, T) or more rows than the launch has tiles for: skipped
-    if (n < 0 || n > p.max_ctx || x.ql < 0 || x.ql > n || x.q0 < 0 || x.q0 + x.ql > T ||
-        x.ql * p.g > rt_max * kRows) {
-        if (x.part == 0 && r2 == 0) report(p.err, PKV_DEVERR_QUERY_LEN);
-        return false;
-    }
-    x.n = n;
-    x.rows = x.ql * p.g;
-    if (x.rt * kRows >= x.rows) return false;
-    const int last_row = min(x.rt * kRows + kRows - 1, x.rows - 1);
-    const int key_end = n - x.ql + last_row / p.g + 1;          // keys of the tile's last query
-    x.np = (key_end + p.P - 1) / p.P;
-    if (x.part >= x.np) return false;
-    x.k0 = x.part * p.P;
-    x.k1 = min(key_end, x.k0 + p.P);
-    return true;
-}
-
 template <int D>
 __global__ void __launch_bounds__(kPWarps * 32, 1)
     prefill_tc_kernel(const __grid_constant__ DecodeParams p, const int32_t* __restrict__ query_start, int T,
-                      const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                      int max_q, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       unsigned long long total_units, int rt_max) {
     using C = PCfg<D>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -138,7 +98,7 @@ __global__ void __launch_bounds__(kPWarps * 32, 1)
 
     // ---- issue side
     bool claiming = true, i_have = false;
-    PUnit iu{};
+    QTile iu{};
     int i_stage = 0, i_nst = 0;
     unsigned g_issue = 0, q_tail = 0;
     int tab = 0, tab_next = 0, tab_chunk = 0, tab_blocks = 0;
@@ -154,8 +114,8 @@ __global__ void __launch_bounds__(kPWarps * 32, 1)
             v = __shfl_sync(0xffffffffu, v, 0);
             static_next += total_warps;
             if (v >= total_units) return false;
-            PUnit x;
-            if (!punit_of(p, query_start, T, v, rt_max, x)) continue;
+            QTile x;
+            if (!qtile_of<kRows>(p, query_start, T, max_q, v, rt_max, x)) continue;
             u = v;
             return true;
         }
@@ -168,7 +128,7 @@ __global__ void __launch_bounds__(kPWarps * 32, 1)
                 claiming = false;
                 return false;
             }
-            punit_of(p, query_start, T, u, rt_max, iu);
+            qtile_of<kRows>(p, query_start, T, max_q, u, rt_max, iu);
             if (lane == 0) {
                 int4* e = queue + 3 * (q_tail % C::kQueue);
                 e[0] = make_int4(iu.s, iu.kvh, iu.rt, iu.part);
@@ -226,7 +186,7 @@ __global__ void __launch_bounds__(kPWarps * 32, 1)
     // ---- consume side
     unsigned g_cons = 0, q_head = 0;
     bool have_unit = false;
-    PUnit cu{};
+    QTile cu{};
     int c_stage = 0, c_nst = 0;
     uint32_t qa[C::KS][4];           // Q A-fragments: rows r, r+8 of the tile
     float o[C::DT][4];               // O accumulators, 8-wide tiles of d
@@ -448,7 +408,7 @@ __global__ void __launch_bounds__(kPWarps * 32, 1)
 // programmatic dependent of the prefill kernel.
 template <int D>
 __global__ void __launch_bounds__(256) prefill_merge_kernel(DecodeParams p, const int32_t* __restrict__ query_start,
-                                                            int T, int row_cap) {
+                                                            int T, int tile_rows, int max_q) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr int E = D / 32;
     const int lane = threadIdx.x & 31;
@@ -462,12 +422,11 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(DecodeParams p, cons
     }
     const int s = lo;
     const int n = p.context_lens[s], q0 = query_start[s], ql = query_start[s + 1] - q0;
-    if (n < 0 || n > p.max_ctx || ql < 0 || ql > n || q0 < 0 || q0 + ql > T || ql * p.g > row_cap ||
-        tq >= q0 + ql)
+    if (n < 0 || n > p.max_ctx || ql < 0 || ql > n || ql > max_q || q0 < 0 || q0 + ql > T || tq >= q0 + ql)
         return;                                // the sequence the main kernel skipped
     const int kvh = h / p.g, row = (tq - q0) * p.g + (h - kvh * p.g);
-    const int rows = ql * p.g, rt = row / kRows;
-    const int last_row = min(rt * kRows + kRows - 1, rows - 1);
+    const int rows = ql * p.g, rt = row / tile_rows;
+    const int last_row = min(rt * tile_rows + tile_rows - 1, rows - 1);
     const int key_end = n - ql + last_row / p.g + 1;
     const int np = (key_end + p.P - 1) / p.P;
     if (np <= 1) return;
@@ -503,34 +462,6 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(DecodeParams p, cons
     for (int k = 0; k < E; ++k) out[k] = __float2bfloat16_rn(acc[k] * f);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 p_encode_fn() {
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
-template <int D>
-bool p_encode_map(CUtensorMap* map, const void* base, const DecodeParams& p) {
-    using C = PCfg<D>;
-    auto fn = p_encode_fn();
-    if (fn == nullptr) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)p.Hkv * D, (cuuint64_t)p.NB * p.bs};
-    const cuuint64_t strides[1] = {(cuuint64_t)p.Hkv * D * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)(C::kBoxRow / 2), (cuuint32_t)(p.bs < kPTok ? p.bs : kPTok)};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 cudaError_t launch_prefill_d(const DecodeParams& p, const int32_t* query_start, int T, int max_q_len,
                              int num_sms, bool merge, cudaStream_t st) {
@@ -546,15 +477,46 @@ cudaError_t launch_prefill_d(const DecodeParams& p, const int32_t* query_start, 
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
     CUtensorMap kmap, vmap;
-    if (!p_encode_map<D>(&kmap, p.kc, p) || !p_encode_map<D>(&vmap, p.vc, p)) return cudaErrorInvalidValue;
+    if (!prefill_encode_kv_map(&kmap, p.kc, p) || !prefill_encode_kv_map(&vmap, p.vc, p)) return cudaErrorInvalidValue;
     const int rt_max = (max_q_len * p.g + kRows - 1) / kRows;
     const unsigned long long units = (unsigned long long)p.Pmax * p.S * p.Hkv * (rt_max > 0 ? rt_max : 1);
     const unsigned long long want = (units + kPWarps - 1) / kPWarps;
     int grid = (int)(want < (unsigned long long)num_sms ? want : (unsigned long long)num_sms);
     if (grid < 1) grid = 1;
-    kern<<<grid, kPWarps * 32, C::kSmemBytes, st>>>(p, query_start, T, kmap, vmap, units, rt_max > 0 ? rt_max : 1);
+    kern<<<grid, kPWarps * 32, C::kSmemBytes, st>>>(p, query_start, T, max_q_len, kmap, vmap, units,
+                                                    rt_max > 0 ? rt_max : 1);
     e = cudaGetLastError();
     if (e != cudaSuccess || !merge) return e;
+    return launch_prefill_merge(p, query_start, T, kRows, max_q_len, st);
+}
+
+}  // namespace
+
+bool prefill_encode_kv_map(CUtensorMap* map, const void* base, const DecodeParams& p) {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    if (fn == nullptr) return false;
+    // rows of one K/V head (d bf16 values), boxes of 64 values x one block
+    // of at most 32 tokens, 128-byte swizzle
+    const cuuint64_t dims[2] = {(cuuint64_t)p.Hkv * p.d, (cuuint64_t)p.NB * p.bs};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.Hkv * p.d * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)(p.bs < 32 ? p.bs : 32)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_prefill_merge(const DecodeParams& p, const int32_t* query_start, int T, int tile_rows,
+                                 int max_q, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     const long long warps = (long long)T * p.Hq;
     cfg.gridDim = dim3((unsigned)((warps + 7) / 8));
@@ -565,10 +527,9 @@ cudaError_t launch_prefill_d(const DecodeParams& p, const int32_t* query_start, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_merge_kernel<D>, p, query_start, T, (rt_max > 0 ? rt_max : 1) * kRows);
+    return p.d == 64 ? cudaLaunchKernelEx(&cfg, prefill_merge_kernel<64>, p, query_start, T, tile_rows, max_q)
+                     : cudaLaunchKernelEx(&cfg, prefill_merge_kernel<128>, p, query_start, T, tile_rows, max_q);
 }
-
-}  // namespace
 
 cudaError_t launch_prefill_tc(const DecodeParams& p, const int32_t* query_start, int T, int max_q_len, int num_sms,
                               bool merge, cudaStream_t st) {

@@ -1,0 +1,559 @@
+// Paged attention over query chunks (chunked prefill, speculative
+// verification) on the fifth-generation tensor cores: tcgen05.mma with the
+// accumulators in tensor memory.
+//
+// "LLM推論の基礎とvLLMの内部", section 6: chunked prefill computes a long
+// prompt in per-step pieces next to other requests' decodes; section 3: the
+// scheduler counts a request's tokens to compute, speculative ones included.
+// Query i of a sequence's chunk of q_len (at position n - q_len + i) attends
+// to tokens 0 .. n - q_len + i, read through the block table.
+//
+// Work unit: (sequence, K/V head, tile of 128 (query, head) rows, partition
+// of P key tokens); one persistent CTA per SM claims units in order.  Roles:
+//   warp 4      producer: claims units, writes the Q tile (128 rows x d,
+//               128-byte swizzled) into one of two buffers, and fills a ring
+//               of two K/V stages of 128 tokens with TMA tensor copies (one
+//               box per block and 64-value half row);
+//   warp 5      one thread issues the MMAs:
+//                 S_j  = Q . K_j^T        M 128, N 128, K d  (TMEM, 2 buffers)
+//                 O   (+)= P_j . V_j      M 128, N d,   K 128 (TMEM)
+//               S_{j+1} is issued before P_j . V_j, so the tensor core works
+//               on the next logits while the softmax of stage j runs;
+//   warps 0-3   softmax, one thread per row (TMEM lane): read S_j, causal
+//               mask, running maximum in base 2, P_j = 2^(x - m) as bf16 into
+//               shared memory (over the K part of stage j once S_j no longer
+//               needs it, when it fits), running sum; at the end O / l.
+// The reference maximum m of a row changes only when a stage's maximum
+// exceeds it by more than 2^8; O and l are then rescaled (O in TMEM, after
+// the previous product has completed).  Every exponent stays <= 2^8, and the
+// final O / l is the same softmax whatever reference was used.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "pkv_common.cuh"
+#include "pkv_internal.h"
+#include "pkv_qtile.cuh"
+#include "pkv_tc_common.cuh"
+#include "pkv_umma.cuh"
+
+namespace pkv {
+namespace {
+
+using namespace tc;
+
+constexpr int kTok = 128;            // key tokens per stage
+constexpr int kURows = 128;          // (query, head) rows per tile: M of both products
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4, kMmaWarp = 5;
+constexpr float kRescaleLog2 = 8.f;
+constexpr long long kUWaitLimit = 4000000000LL;   // ~2 s: a barrier that never completes
+constexpr uint32_t kTmemCols = 512;               // S buffers at 0 and 128, O at 256
+constexpr uint32_t kTmemO = 256;
+
+template <int D>
+struct UCfg {
+    static constexpr int kHalves = D / 64;                 // 128-byte halves of a Q/K/V row
+    static constexpr int kPartBytes = kTok * 2 * D;        // K or V of one stage
+    static constexpr int kStageBytes = 2 * kPartBytes;
+    static constexpr int kQBytes = kURows * 2 * D;
+    static constexpr int kPBytes = kURows * kTok * 2;
+    static constexpr bool kPInK = kPartBytes >= kPBytes;   // P_j overwrites K_j
+    static constexpr int kQOff = 2 * kStageBytes;
+    static constexpr int kPOff = kQOff + 2 * kQBytes;
+    static constexpr int kCtlOff = kPOff + (kPInK ? 0 : 2 * kPBytes);
+    static constexpr int kSmemBytes = kCtlOff + 512 + 1024;
+    static constexpr int KS = D / 16;
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
+
+// control block offsets (bytes from the control base)
+constexpr uint32_t kBarKvFull = 0, kBarKvEmpty = 16, kBarSFull = 32, kBarSFree = 48, kBarPFull = 64,
+                   kBarODone = 80, kBarFin = 88, kBarQFull = 96, kBarQEmpty = 112, kBarUFull = 128,
+                   kBarUEmpty = 144, kTmemSlot = 160, kAbort = 164, kMasks = 176, kRing = 256;
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_umma_kernel(const __grid_constant__ DecodeParams p, const int32_t* __restrict__ query_start, int T,
+                        int max_q, const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, unsigned long long total_units, int rt_max) {
+    using C = UCfg<D>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    unsigned char* smem = smem_raw + (base - raw_addr);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t ctl = base + C::kCtlOff;
+    unsigned char* ctlp = smem + C::kCtlOff;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(ctlp + kAbort);
+    uint32_t* masks = reinterpret_cast<uint32_t*>(ctlp + kMasks);      // [2 stages][4 words]: tokens present
+    int4* ring = reinterpret_cast<int4*>(ctlp + kRing);                // [2 units][4 int4]
+    auto kpart = [&](int s) { return base + s * C::kStageBytes; };
+    auto vpart = [&](int s) { return base + s * C::kStageBytes + C::kPartBytes; };
+    auto qbuf = [&](int b) { return base + C::kQOff + b * C::kQBytes; };
+    auto pbuf = [&](int s) { return C::kPInK ? kpart(s) : base + C::kPOff + s * C::kPBytes; };
+    auto bar = [&](uint32_t off, int i) { return ctl + off + 8 * i; };
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(kBarKvFull, i), 1);
+            mbar_init(bar(kBarKvEmpty, i), 1);
+            mbar_init(bar(kBarSFull, i), 1);
+            mbar_init(bar(kBarSFree, i), 4);
+            mbar_init(bar(kBarPFull, i), 4);
+            mbar_init(bar(kBarQFull, i), 1);
+            mbar_init(bar(kBarQEmpty, i), 1);
+            mbar_init(bar(kBarUFull, i), 1);
+            mbar_init(bar(kBarUEmpty, i), 5);
+        }
+        mbar_init(bar(kBarODone, 0), 1);
+        mbar_init(bar(kBarFin, 0), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) umma::tmem_alloc(ctl + kTmemSlot, kTmemCols);
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(ctlp + kTmemSlot);
+
+    // bounded wait; false once the limit passes or another role gave up
+    auto wait = [&](uint32_t b, uint32_t parity, bool abortable) -> bool {
+        if (mbar_try_wait(b, parity)) return true;
+        const long long t0 = clock64();
+        while (!mbar_try_wait(b, parity)) {
+            if (abortable && *abort_flag) return false;
+            if (clock64() - t0 > kUWaitLimit) {
+                report(p.err, PKV_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+        return true;
+    };
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ producer
+        unsigned long long static_next = blockIdx.x;
+        uint32_t g = 0, un = 0;
+        const uint32_t box_bytes = (uint32_t)(p.bs < 32 ? p.bs : 32) * 128u;
+        bool ok = true, bad = false;          // bad: warp-uniform
+        for (;;) {
+            QTile x;
+            bool have = false;
+            for (;;) {
+                unsigned long long v = 0;
+                if (lane == 0)
+                    v = p.sched != nullptr ? atomicAdd(reinterpret_cast<unsigned long long*>(p.sched), 1ull)
+                                           : static_next;
+                v = __shfl_sync(0xffffffffu, v, 0);
+                static_next += gridDim.x;
+                if (v >= total_units) break;
+                if (qtile_of<kURows>(p, query_start, T, max_q, v, rt_max, x)) {
+                    have = true;
+                    break;
+                }
+            }
+            const int slot = un & 1;
+            if (un >= 2) ok = wait(bar(kBarUEmpty, slot), ((un >> 1) - 1) & 1, true);
+            if (__any_sync(0xffffffffu, !ok)) break;
+            if (lane == 0) {
+                int4* e = ring + 4 * slot;
+                if (have) {
+                    e[0] = make_int4(x.s, x.kvh, x.rt, x.part);
+                    e[1] = make_int4(x.k0, x.k1, x.n, x.ql);
+                    e[2] = make_int4(x.q0, x.np, x.rows, 1);
+                } else {
+                    e[2] = make_int4(0, 0, 0, 0);
+                }
+                umma::mbar_arrive(bar(kBarUFull, slot));
+            }
+            if (!have) break;
+
+            // Q tile: rows (query, head) of this tile, zero past the last row
+            const int qb = un & 1;
+            if (un >= 2) ok = wait(bar(kBarQEmpty, qb), ((un >> 1) - 1) & 1, true);
+            if (__any_sync(0xffffffffu, !ok)) break;
+            {
+                constexpr int CH = 2 * D / 16;              // 16-byte chunks per row
+                const int rows_here = min(kURows, x.rows - x.rt * kURows);
+                const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
+                const uint32_t qdst = qbuf(qb);
+#pragma unroll 4
+                for (int it = 0; it < kURows * CH / 32; ++it) {
+                    const int idx = it * 32 + lane;
+                    const int r = idx / CH, c = idx % CH;
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (r < rows_here) {
+                        const int row = x.rt * kURows + r;
+                        const int qi = row / p.g, hh = row - qi * p.g;
+                        const size_t off = ((size_t)(x.q0 + qi) * p.Hq + x.kvh * p.g + hh) * D + c * 8;
+                        v = __ldg(reinterpret_cast<const uint4*>(q + off));
+                    }
+                    st_shared_v4(qdst + (c >> 3) * (kURows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4), v);
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) umma::mbar_arrive(bar(kBarQFull, qb));
+            }
+
+            // K/V stages; block-table entries come 32 at a time, one chunk ahead
+            const int nst = (x.k1 - x.k0 + kTok - 1) / kTok;
+            const int bps = kTok / p.bs;                      // blocks per stage: 8 or 4
+            const int unit_blocks = (x.k1 - x.k0 + p.bs - 1) / p.bs;
+            const int32_t* trow = p.block_tables + (size_t)x.s * p.MB + x.k0 / p.bs;
+            auto load_chunk = [&](int c) -> int {
+                const int rb = 32 * c + lane;
+                return rb < unit_blocks ? __ldg(trow + rb) : 0;
+            };
+            int tab = load_chunk(0), tab_next = load_chunk(1), tab_chunk = 0;
+            for (int j = 0; j < nst; ++j, ++g) {
+                const int s = g & 1;
+                if (g >= 2) ok = wait(bar(kBarKvEmpty, s), ((g >> 1) - 1) & 1, true);
+                if (__any_sync(0xffffffffu, !ok)) {
+                    bad = true;
+                    break;
+                }
+                const int ts = x.k0 + j * kTok;
+                const int tn = min(kTok, x.k1 - ts);
+                const int nb = (tn + p.bs - 1) / p.bs;
+                const int idx0 = j * bps;
+                if ((idx0 >> 5) != tab_chunk) {
+                    tab_chunk = idx0 >> 5;
+                    tab = tab_next;
+                    tab_next = load_chunk(tab_chunk + 1);
+                }
+                const int pb = __shfl_sync(0xffffffffu, tab, (idx0 + (lane & (bps - 1))) & 31);
+                const bool bok = lane < nb && pb >= 0 && pb < p.NB;
+                if (lane < nb && !bok) report(p.err, PKV_DEVERR_BLOCK_ID);
+                const uint32_t bm = __ballot_sync(0xffffffffu, bok);
+                if (lane < 4) {
+                    // tokens 32 lane .. 32 lane + 31: present where their block is valid and t < tn
+                    uint32_t w;
+                    if (p.bs == 16) {
+                        const uint32_t b2 = (bm >> (2 * lane)) & 3u;
+                        w = ((b2 & 1u) ? 0x0000ffffu : 0u) | ((b2 & 2u) ? 0xffff0000u : 0u);
+                    } else {
+                        w = ((bm >> lane) & 1u) ? 0xffffffffu : 0u;
+                    }
+                    const int lo = 32 * lane;
+                    const uint32_t tm = tn >= lo + 32 ? 0xffffffffu : (tn <= lo ? 0u : ((1u << (tn - lo)) - 1u));
+                    masks[4 * s + lane] = w & tm;
+                }
+                constexpr int kPer = 2 * C::kHalves;       // boxes per block: K and V, each half
+                const int bi = lane / kPer, kv = (lane / C::kHalves) & 1, h = lane % C::kHalves;
+                const int pbb = __shfl_sync(0xffffffffu, pb, bi & 31);
+                const bool live = bi < nb && ((bm >> bi) & 1u);
+                const uint32_t nlive = __popc(__ballot_sync(0xffffffffu, live));
+                __syncwarp();
+                if (lane == 0) mbar_arrive_expect_tx(bar(kBarKvFull, s), nlive * box_bytes);
+                __syncwarp();
+                if (live) {
+                    const uint32_t dst = (kv ? vpart(s) : kpart(s)) + h * (kTok * 128) + bi * p.bs * 128;
+                    tensor_load_2d(dst, kv ? &vmap : &kmap, x.kvh * D + h * 64, pbb * p.bs, bar(kBarKvFull, s));
+                }
+            }
+            if (bad) break;
+            ++un;
+        }
+        // copies still in flight land before the CTA leaves
+        if (g >= 1) wait(bar(kBarKvFull, (g - 1) & 1), ((g - 1) >> 1) & 1, false);
+        if (g >= 2) wait(bar(kBarKvFull, g & 1), ((g - 2) >> 1) & 1, false);
+        if (p.sched != nullptr && lane == 0) {
+            unsigned long long* ctr = reinterpret_cast<unsigned long long*>(p.sched);
+            __threadfence();
+            const unsigned long long done = atomicAdd(ctr + 1, 1ull);
+            if (done == gridDim.x - 1) {
+                atomicExch(ctr, 0ull);
+                atomicExch(ctr + 1, 0ull);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idS = umma::idesc_bf16_f32(kURows, kTok, false);
+            constexpr uint32_t idPV = umma::idesc_bf16_f32(kURows, D, true);
+            uint32_t g = 0, un = 0;
+            long long pv_pending = -1;
+            bool pv_first = false, ok = true;
+            auto issue_pv = [&](uint32_t gp, bool first) -> bool {
+                const int s = gp & 1;
+                if (!wait(bar(kBarPFull, s), (gp >> 1) & 1, true)) return false;
+                umma::fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < kTok / 16; ++kk) {
+                    const uint64_t a = umma::desc_sw128(pbuf(s) + (kk >> 2) * (kURows * 128) + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = umma::desc_sw128(vpart(s) + kk * 2048, kTok * 128, 1024);
+                    umma::mma_bf16(tmem + kTmemO, a, b, idPV, !(first && kk == 0));
+                }
+                umma::commit(bar(kBarODone, 0));
+                umma::commit(bar(kBarKvEmpty, s));
+                return true;
+            };
+            for (;;) {
+                const int slot = un & 1;
+                if (!wait(bar(kBarUFull, slot), (un >> 1) & 1, true)) break;
+                const int4 e1 = ring[4 * slot + 1], e2 = ring[4 * slot + 2];
+                umma::mbar_arrive(bar(kBarUEmpty, slot));
+                if (e2.w == 0) break;
+                const int nst = (e1.y - e1.x + kTok - 1) / kTok;
+                const int qb = un & 1;
+                if (!wait(bar(kBarQFull, qb), (un >> 1) & 1, true)) break;
+                for (int j = 0; j < nst; ++j, ++g) {
+                    const int s = g & 1;
+                    if (!wait(bar(kBarKvFull, s), (g >> 1) & 1, true) ||
+                        (g >= 2 && !wait(bar(kBarSFree, s), ((g >> 1) - 1) & 1, true))) {
+                        ok = false;
+                        break;
+                    }
+                    umma::fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < C::KS; ++kk) {
+                        const uint64_t a =
+                            umma::desc_sw128(qbuf(qb) + (kk >> 2) * (kURows * 128) + (kk & 3) * 32, 16, 1024);
+                        const uint64_t b =
+                            umma::desc_sw128(kpart(s) + (kk >> 2) * (kTok * 128) + (kk & 3) * 32, 16, 1024);
+                        umma::mma_bf16(tmem + s * kTok, a, b, idS, kk > 0);
+                    }
+                    umma::commit(bar(kBarSFull, s));
+                    if (j == nst - 1) umma::commit(bar(kBarQEmpty, qb));
+                    if (pv_pending >= 0 && !issue_pv((uint32_t)pv_pending, pv_first)) {
+                        ok = false;
+                        break;
+                    }
+                    pv_pending = g;
+                    pv_first = j == 0;
+                }
+                if (!ok) break;
+                ++un;
+            }
+            if (ok && pv_pending >= 0) issue_pv((uint32_t)pv_pending, pv_first);
+            // every product issued here completes before the CTA releases TMEM
+            umma::commit(bar(kBarFin, 0));
+            wait(bar(kBarFin, 0), 0, false);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------- softmax
+        const int i = tid;                                    // row of the tile, TMEM lane
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const float scl = p.logit_scale_log2;
+        uint32_t g = 0, un = 0;
+        bool ok = true, bad = false;          // bad: warp-uniform
+        for (;;) {
+            const int slot = un & 1;
+            ok = wait(bar(kBarUFull, slot), (un >> 1) & 1, true);
+            if (__any_sync(0xffffffffu, !ok)) break;
+            const int4 e0 = ring[4 * slot], e1 = ring[4 * slot + 1], e2 = ring[4 * slot + 2];
+            __syncwarp();
+            if (lane == 0) umma::mbar_arrive(bar(kBarUEmpty, slot));
+            if (e2.w == 0) break;
+            const int kvh = e0.y, rt = e0.z, part = e0.w, k0 = e1.x, k1 = e1.y, n = e1.z, ql = e1.w;
+            const int q0 = e2.x, np = e2.y, rows = e2.z;
+            const int row = rt * kURows + i;
+            const bool rv = row < rows;
+            const int qi = rv ? row / p.g : 0;
+            const int hh = rv ? row - qi * p.g : 0;
+            const int pos = rv ? n - ql + qi : -1;
+            float m_ref = -CUDART_INF_F, l = 0.f;
+            const int nst = (k1 - k0 + kTok - 1) / kTok;
+            for (int j = 0; j < nst; ++j, ++g) {
+                const int s = g & 1;
+                ok = wait(bar(kBarSFull, s), (g >> 1) & 1, true) && wait(bar(kBarKvFull, s), (g >> 1) & 1, true);
+                if (__any_sync(0xffffffffu, !ok)) {
+                    bad = true;
+                    break;
+                }
+                umma::fence_after_sync();
+                uint32_t sr[4][32];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) umma::tmem_ld32(tmem + lane_base + s * kTok + 32 * q, sr[q]);
+                umma::tmem_wait_ld();
+                umma::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) umma::mbar_arrive(bar(kBarSFree, s));
+
+                const int lim = pos - (k0 + j * kTok);           // tokens t <= lim are visible to this row
+                uint32_t mw[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) mw[q] = masks[4 * s + q];
+                const bool whole = lim >= kTok - 1 && (mw[0] & mw[1] & mw[2] & mw[3]) == 0xffffffffu;
+                float mx8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mx8[k] = -CUDART_INF_F;
+                if (whole) {                                     // every token present and visible
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+#pragma unroll
+                        for (int b = 0; b < 32; ++b) {
+                            const float xv = __uint_as_float(sr[q][b]) * scl;
+                            sr[q][b] = __float_as_uint(xv);
+                            mx8[b & 7] = fmaxf(mx8[b & 7], xv);
+                        }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+#pragma unroll
+                        for (int b = 0; b < 32; ++b) {
+                            const bool live = ((mw[q] >> b) & 1u) && (32 * q + b) <= lim;
+                            const float xv = live ? __uint_as_float(sr[q][b]) * scl : -CUDART_INF_F;
+                            sr[q][b] = __float_as_uint(xv);
+                            mx8[b & 7] = fmaxf(mx8[b & 7], xv);
+                        }
+                }
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                float alpha = 1.f;
+                bool resc = false;
+                if (j == 0) {
+                    m_ref = mx;
+                } else if (mx > m_ref + kRescaleLog2) {
+                    if (m_ref != -CUDART_INF_F) {
+                        alpha = fast_exp2(m_ref - mx);
+                        resc = true;
+                    }
+                    m_ref = mx;
+                }
+                l *= alpha;
+                if (__any_sync(0xffffffffu, resc)) {
+                    // O holds P_{j-1} . V_{j-1}: wait for that product, then scale in place
+                    ok = wait(bar(kBarODone, 0), (g - 1) & 1, true);
+                    if (__any_sync(0xffffffffu, !ok)) {
+                        bad = true;
+                        break;
+                    }
+                    umma::fence_after_sync();
+#pragma unroll
+                    for (int c0 = 0; c0 < D / 32; ++c0) {
+                        uint32_t ov[32];
+                        umma::tmem_ld32(tmem + lane_base + kTmemO + 32 * c0, ov);
+                        umma::tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
+                        umma::tmem_st32(tmem + lane_base + kTmemO + 32 * c0, ov);
+                    }
+                    umma::tmem_wait_st();
+                }
+                // V rows of tokens that were not loaded are zeroed (0 * garbage could be NaN)
+                if (!((mw[i >> 5] >> (i & 31)) & 1u)) {
+#pragma unroll
+                    for (int h = 0; h < C::kHalves; ++h)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            st_shared_v4(vpart(s) + h * (kTok * 128) + i * 128 + c * 16, make_uint4(0u, 0u, 0u, 0u));
+                }
+                // P row: 2^(x - m), bf16, 128-byte swizzled K-major rows of 64 tokens
+                const float mb = m_ref == -CUDART_INF_F ? 0.f : m_ref;
+                float ls[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+                const uint32_t prow = pbuf(s) + i * 128;
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int t = 8 * c + 2 * k;
+                        const float a0 = fast_exp2(__uint_as_float(sr[t >> 5][t & 31]) - mb);
+                        const float a1 = fast_exp2(__uint_as_float(sr[(t + 1) >> 5][(t + 1) & 31]) - mb);
+                        ls[2 * k] += a0;
+                        ls[2 * k + 1] += a1;
+                        w[k] = pack2<false>(a0, a1);
+                    }
+                    st_shared_v4(prow + (c >> 3) * (kURows * 128) + (((c & 7) ^ (i & 7)) << 4),
+                                 make_uint4(w[0], w[1], w[2], w[3]));
+                }
+                l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                fence_proxy_async();
+                umma::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) umma::mbar_arrive(bar(kBarPFull, s));
+            }
+            if (bad) break;
+
+            // epilogue: O / l, or the partition's (m, l, O)
+            ok = wait(bar(kBarODone, 0), (g - 1) & 1, true);
+            if (__any_sync(0xffffffffu, !ok)) break;
+            umma::fence_after_sync();
+            const size_t hrow = (size_t)(q0 + qi) * p.Hq + kvh * p.g + hh;
+            const float f = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < D / 32; ++c0) {
+                uint32_t ov[32];
+                umma::tmem_ld32(tmem + lane_base + kTmemO + 32 * c0, ov);
+                umma::tmem_wait_ld();
+                if (!rv) continue;
+                if (np == 1) {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + hrow * D + 32 * c0);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        dst[k] = make_uint4(pack2<false>(__uint_as_float(ov[8 * k]) * f, __uint_as_float(ov[8 * k + 1]) * f),
+                                            pack2<false>(__uint_as_float(ov[8 * k + 2]) * f, __uint_as_float(ov[8 * k + 3]) * f),
+                                            pack2<false>(__uint_as_float(ov[8 * k + 4]) * f, __uint_as_float(ov[8 * k + 5]) * f),
+                                            pack2<false>(__uint_as_float(ov[8 * k + 6]) * f, __uint_as_float(ov[8 * k + 7]) * f));
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(p.part_acc + (hrow * p.Pmax + part) * D + 32 * c0);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) dst[k] = make_uint4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
+                }
+            }
+            if (rv && np > 1) {
+                const size_t u = hrow * p.Pmax + part;
+                p.part_ml[2 * u] = m_ref;
+                p.part_ml[2 * u + 1] = l;
+            }
+            umma::fence_before_sync();
+            ++un;
+        }
+    }
+
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        umma::fence_after_sync();
+        umma::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int D>
+cudaError_t launch_umma_d(const DecodeParams& p, const int32_t* query_start, int T, int max_q_len, int num_sms,
+                          bool merge, cudaStream_t st) {
+    using C = UCfg<D>;
+    auto kern = prefill_umma_kernel<D>;
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = true;
+    }
+    CUtensorMap kmap, vmap;
+    if (!prefill_encode_kv_map(&kmap, p.kc, p) || !prefill_encode_kv_map(&vmap, p.vc, p)) return cudaErrorInvalidValue;
+    int rt_max = (max_q_len * p.g + kURows - 1) / kURows;
+    if (rt_max < 1) rt_max = 1;
+    const unsigned long long units = (unsigned long long)p.Pmax * p.S * p.Hkv * rt_max;
+    int grid = (int)(units < (unsigned long long)num_sms ? units : (unsigned long long)num_sms);
+    if (grid < 1) grid = 1;
+    kern<<<grid, kThreads, C::kSmemBytes, st>>>(p, query_start, T, max_q_len, kmap, vmap, units, rt_max);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || !merge) return e;
+    return launch_prefill_merge(p, query_start, T, kURows, max_q_len, st);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_umma(const DecodeParams& p, const int32_t* query_start, int T, int max_q_len, int num_sms,
+                                bool merge, cudaStream_t st) {
+    if (p.S == 0 || T == 0) return cudaSuccess;
+    return p.d == 64 ? launch_umma_d<64>(p, query_start, T, max_q_len, num_sms, merge, st)
+                     : launch_umma_d<128>(p, query_start, T, max_q_len, num_sms, merge, st);
+}
+
+}  // namespace pkv

@@ -26,7 +26,10 @@ def _case(name, lens, qlens, Hq=None, Hkv=None, d=None, seed=7):
     return w, hv, qs, q32
 
 
-def _run(w, hv, qs, q32, partition, dev="cuda", query_start=None, err=None, max_query_len=None):
+KERNELS = ["tcgen05", "mma_sync"]
+
+
+def _run(w, hv, qs, q32, partition, dev="cuda", query_start=None, err=None, max_query_len=None, kernel="auto"):
     kc = to_device(hv.k_pool, W.DT_BF16, dev)
     vc = to_device(hv.v_pool, W.DT_BF16, dev)
     q = to_device(q32, W.DT_BF16, dev)
@@ -35,7 +38,8 @@ def _run(w, hv, qs, q32, partition, dev="cuda", query_start=None, err=None, max_
     mq = int(np.diff(qs).max()) if max_query_len is None else max_query_len
     pkv.paged_attention_prefill(out, q, kc, vc, torch.from_numpy(w.block_tables).to(dev),
                                 torch.from_numpy(w.context_lens).to(dev), qs_dev, mq,
-                                w.max_context_len, scale=w.scale, partition_size=partition, err_word=err)
+                                w.max_context_len, scale=w.scale, partition_size=partition, err_word=err,
+                                kernel=kernel)
     return out
 
 
@@ -54,20 +58,83 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-g{c[3] // c[4]}-d{c[5]}" for c in CASES])
 @pytest.mark.parametrize("partition", [-1, 0, 64])
-def test_prefill_matches_oracle(case, partition):
+def test_prefill_matches_oracle(case, partition, kernel):
     name, lens, qlens, Hq, Hkv, d = case
     w, hv, qs, q32 = _case(name, lens, qlens, Hq, Hkv, d)
     if partition > 0 and partition % w.bs:
         partition = 2 * w.bs
-    out = _run(w, hv, qs, q32, partition)
-    assert_close(out, _ref(w, hv, qs, q32), W.DT_BF16, f"prefill P={partition}")
+    out = _run(w, hv, qs, q32, partition, kernel=kernel)
+    assert_close(out, _ref(w, hv, qs, q32), W.DT_BF16, f"prefill {kernel} P={partition}")
 
 
-def test_prefill_one_query_equals_decode():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_prefill_wide_groups_and_tile_edges(kernel):
+    """Rows that cross 128-row tiles mid-query (g = 12, 40 and 64 heads per
+    K/V head), a query count that is not a multiple of anything, and
+    sequences whose key range ends inside a block."""
+    for (Hq, Hkv, lens, qlens) in ((24, 2, [300, 77, 1200], [23, 77, 130]),
+                                   (40, 1, [129, 64], [7, 64]),
+                                   (64, 1, [513, 1000], [3, 2])):
+        w, hv, qs, q32 = _case("qwen2.5-1.5b", lens, qlens, Hq, Hkv, 128, seed=Hq)
+        for partition in (-1, 96):
+            out = _run(w, hv, qs, q32, partition, kernel=kernel)
+            assert_close(out, _ref(w, hv, qs, q32), W.DT_BF16, f"g={Hq // Hkv} P={partition} {kernel}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_prefill_bad_block_id_reported(kernel):
+    """A block-table entry outside the pool: that block is skipped (its keys
+    count as absent) and error word 1 is reported; nothing faults."""
+    w, hv, qs, q32 = _case("qwen2.5-1.5b", [40, 50], [8, 8], 8, 2, 128)
+    bt = w.block_tables.copy()
+    bt[1, 1] = w.NB + 5
+    w2 = dataclasses.replace(w, block_tables=bt)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = _run(w2, hv, qs, q32, -1, err=err, kernel=kernel)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 1
+    assert_close(out[:8], _ref(w, hv, qs, q32)[:8], W.DT_BF16, "the sequence with a valid table")
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_prefill_graph_replay_reuses_workspace(kernel):
+    """The call is capturable and its scheduling counters reset themselves:
+    several replays of one captured call give identical outputs."""
+    w, hv, qs, q32 = _case("qwen2.5-1.5b", [600, 1500, 90], [40, 100, 90], 12, 2, 128)
+    out = _run(w, hv, qs, q32, 128, kernel=kernel)
+    ref = out.clone()
+    kc = to_device(hv.k_pool, W.DT_BF16)
+    vc = to_device(hv.v_pool, W.DT_BF16)
+    q = to_device(q32, W.DT_BF16)
+    o2 = torch.empty_like(q)
+    bt, cl, qd = (torch.from_numpy(a).cuda() for a in (w.block_tables, w.context_lens, qs))
+    mq = int(np.diff(qs).max())
+    n = pkv.prefill_workspace_size(w.S, q.shape[0], mq, w.Hq, w.Hkv, w.d, w.bs, w.max_context_len, 128)
+    ws = torch.zeros(max(n, 256), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        pkv.paged_attention_prefill(o2, q, kc, vc, bt, cl, qd, mq, w.max_context_len, scale=w.scale,
+                                    partition_size=128, workspace=ws, stream=s, kernel=kernel)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pkv.paged_attention_prefill(o2, q, kc, vc, bt, cl, qd, mq, w.max_context_len, scale=w.scale,
+                                    partition_size=128, workspace=ws, stream=s, kernel=kernel)
+    for _ in range(3):
+        o2.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o2, ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_prefill_one_query_equals_decode(kernel):
     w, hv, qs, q32 = _case("qwen2.5-1.5b", [5, 200, 1025], [1, 1, 1], 12, 2, 128)
-    out = _run(w, hv, qs, q32, 0)
+    out = _run(w, hv, qs, q32, 0, kernel=kernel)
     q = to_device(q32, W.DT_BF16, "cuda")
     dec = torch.empty_like(q)
     ws = pkv.make_workspace(w.S, w.Hq, w.Hkv, w.d, w.bs, w.max_context_len, -1)
@@ -80,7 +147,8 @@ def test_prefill_one_query_equals_decode():
     assert_close(dec, ref, W.DT_BF16, "decode")
 
 
-def test_prefill_chunked_long_prompt():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_prefill_chunked_long_prompt(kernel):
     """A Qwen2.5-7B-shaped batch: 8 sequences with 512-token chunks at the
     end of 1,024 .. 4,096-token contexts, and 24 decoding sequences (one
     query) next to them, as one call."""
@@ -88,16 +156,17 @@ def test_prefill_chunked_long_prompt():
     lens = list(rng.integers(1024, 4097, 8)) + list(rng.integers(16, 3000, 24))
     qlens = [512] * 8 + [1] * 24
     w, hv, qs, q32 = _case("qwen2.5-1.5b", lens, qlens, 28, 4, 128, seed=13)
-    out = _run(w, hv, qs, q32, 0)
-    assert_close(out, _ref(w, hv, qs, q32), W.DT_BF16, "mixed chunk + decode batch")
+    out = _run(w, hv, qs, q32, 0, kernel=kernel)
+    assert_close(out, _ref(w, hv, qs, q32), W.DT_BF16, f"mixed chunk + decode batch {kernel}")
 
 
-def test_prefill_bad_query_count_reported():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_prefill_bad_query_count_reported(kernel):
     w, hv, qs, q32 = _case("qwen2.5-1.5b", [20, 30], [4, 4], 8, 2, 128)
     bad = np.array([0, 4, 40], np.int32)            # second sequence: 36 queries > 30 tokens
     q32 = W.host_normal(7, "prefill-query-bad", (40, w.Hq, w.d))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = _run(w, hv, bad, q32, -1, query_start=bad, err=err, max_query_len=4)   # what the host believes
+    out = _run(w, hv, bad, q32, -1, query_start=bad, err=err, max_query_len=4, kernel=kernel)   # host's view
     torch.cuda.synchronize()
     assert int(err.item()) == 6
     ref = O.paged_attention_prefill(W.bf16_bits(q32[:4]), O.BF16, W.bf16_bits(hv.k_pool), W.bf16_bits(hv.v_pool),
@@ -106,7 +175,8 @@ def test_prefill_bad_query_count_reported():
     assert_close(out[:4], ref, W.DT_BF16, "valid sequence of a batch with a bad one")
 
 
-def test_prefill_queries_outside_the_batch_are_skipped():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_prefill_queries_outside_the_batch_are_skipped(kernel):
     """query_start naming rows past T, or more queries than max_query_len
     covers: skipped and reported, nothing written out of bounds."""
     w, hv, qs, q32 = _case("qwen2.5-1.5b", [20, 30, 25], [4, 4, 4], 8, 2, 128)
@@ -114,7 +184,7 @@ def test_prefill_queries_outside_the_batch_are_skipped():
                                              (np.array([0, 4, 12, 12], np.int32), 4)) for part in (-1, 16)]
     for bad, mq, part in cases:
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
-        out = _run(w, hv, qs, q32, part, query_start=bad, err=err, max_query_len=mq)
+        out = _run(w, hv, qs, q32, part, query_start=bad, err=err, max_query_len=mq, kernel=kernel)
         torch.cuda.synchronize()
         assert int(err.item()) == 6
         ref = _ref(w, hv, qs, q32)
@@ -124,8 +194,9 @@ def test_prefill_queries_outside_the_batch_are_skipped():
 FULL = [("qwen2.5-7b-chunked", 4, 6), ("qwen2.5-72b-spec", 3, 5)]
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("name,nseq,nq", FULL, ids=[f[0] for f in FULL])
-def test_full_size_query_chunks(name, nseq, nq):
+def test_full_size_query_chunks(name, nseq, nq, kernel):
     """The query-chunk workloads at full size, in the launch configuration
     the benchmark times (default partitioning).  Sampled sequences hold host
     draws; for each, a few of its queries (first, last, random) are
@@ -146,7 +217,7 @@ def test_full_size_query_chunks(name, nseq, nq):
     wsp = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
     pkv.paged_attention_prefill(out, q, c.k_cache, c.v_cache, c.block_tables, c.context_lens,
                                 torch.from_numpy(qs).cuda(), int(qlens.max()), w.max_context_len, scale=w.scale,
-                                partition_size=P, workspace=wsp)
+                                partition_size=P, workspace=wsp, kernel=kernel)
     torch.cuda.synchronize()
     rng = np.random.default_rng(5)
     rows, tabs, lens = [], [], []
@@ -160,7 +231,7 @@ def test_full_size_query_chunks(name, nseq, nq):
     rows_a = np.array(rows)
     ref = O.paged_attention_prefill(W.bf16_bits(q32[rows_a]), O.BF16, c.o_k, c.o_v, O.BF16, np.stack(tabs),
                                     np.array(lens, np.int32), np.arange(len(rows) + 1, dtype=np.int32), w.scale)
-    assert_close(out[torch.from_numpy(rows_a).cuda()], ref, W.DT_BF16, f"{name} sampled queries")
+    assert_close(out[torch.from_numpy(rows_a).cuda()], ref, W.DT_BF16, f"{name} {kernel} sampled queries")
     of = out.float()
     assert torch.isfinite(of).all()
     assert float(of.abs().max()) <= float(c.v_cache.float().abs().max()) * 1.01 + 1e-3
