@@ -1,6 +1,6 @@
 // Paged attention over query chunks (chunked prefill, speculative
 // verification) on the fifth-generation tensor cores: tcgen05.mma with the
-// accumulators in tensor memory.
+// accumulators and the probabilities in tensor memory (TMEM).
 //
 // "LLM推論の基礎とvLLMの内部", section 6: chunked prefill computes a long
 // prompt in per-step pieces next to other requests' decodes; section 3: the
@@ -10,19 +10,20 @@
 //
 // Work unit: (sequence, K/V head, tile of 128 (query, head) rows, partition
 // of P key tokens); one persistent CTA per SM claims units in order.  Roles:
-//   warp 4      producer: claims units, writes the Q tile (128 rows x d,
-//               128-byte swizzled) into one of two buffers, and fills a ring
-//               of two K/V stages of 128 tokens with TMA tensor copies (one
-//               box per block and 64-value half row);
+//   warp 4      producer: claims units and streams 128-token tiles, K_j then
+//               V_j, into one ring of shared-memory items by TMA tensor
+//               copies (one box per block and 64-value half row, 128-byte
+//               swizzle).  K_j's item is released as soon as S_j is done.
+//   warp 6      Q loader: the tile's 128 rows of Q into one of two buffers.
 //   warp 5      one thread issues the MMAs:
-//                 S_j  = Q . K_j^T        M 128, N 128, K d  (TMEM, 2 buffers)
-//                 O   (+)= P_j . V_j      M 128, N d,   K 128 (TMEM)
+//                 S_j = Q . K_j^T        M 128, N 128, K d   (TMEM, 3 buffers)
+//                 O  (+)= P_j . V_j      M 128, N d,   K 128 (A = P_j in TMEM)
 //               S_{j+1} is issued before P_j . V_j, so the tensor core works
-//               on the next logits while the softmax of stage j runs;
+//               on the next logits while the softmax of stage j runs.
 //   warps 0-3   softmax, one thread per row (TMEM lane): read S_j, causal
-//               mask, running maximum in base 2, P_j = 2^(x - m) as bf16 into
-//               shared memory (over the K part of stage j once S_j no longer
-//               needs it, when it fits), running sum; at the end O / l.
+//               mask, running maximum in base 2, P_j = 2^(x - m) packed as
+//               bf16 over the first half of S_j's columns, running sum; at
+//               the end O / l, or the partition's (m, l, O).
 // The reference maximum m of a row changes only when a stage's maximum
 // exceeds it by more than 2^8; O and l are then rescaled (O in TMEM, after
 // the previous product has completed).  Every exponent stays <= 2^8, and the
@@ -44,37 +45,56 @@ using namespace tc;
 
 constexpr int kTok = 128;            // key tokens per stage
 constexpr int kURows = 128;          // (query, head) rows per tile: M of both products
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4, kMmaWarp = 5;
+constexpr int kSBufs = 3;            // S (and P) buffers in TMEM
+constexpr int kThreads = 224;
+constexpr int kProducerWarp = 4, kMmaWarp = 5, kQWarp = 6;
 constexpr float kRescaleLog2 = 8.f;
 constexpr long long kUWaitLimit = 4000000000LL;   // ~2 s: a barrier that never completes
-constexpr uint32_t kTmemCols = 512;               // S buffers at 0 and 128, O at 256
-constexpr uint32_t kTmemO = 256;
+constexpr uint32_t kTmemCols = 512;               // S buffers at 0, 128, 256; O at 384
+constexpr uint32_t kTmemO = 384;
 
 template <int D>
 struct UCfg {
     static constexpr int kHalves = D / 64;                 // 128-byte halves of a Q/K/V row
-    static constexpr int kPartBytes = kTok * 2 * D;        // K or V of one stage
-    static constexpr int kStageBytes = 2 * kPartBytes;
+    static constexpr int kItemBytes = kTok * 2 * D;        // one K or V tile of a stage
+    static constexpr int kItems = D == 128 ? 5 : 8;        // ring of K/V tiles
     static constexpr int kQBytes = kURows * 2 * D;
-    static constexpr int kPBytes = kURows * kTok * 2;
-    static constexpr bool kPInK = kPartBytes >= kPBytes;   // P_j overwrites K_j
-    static constexpr int kQOff = 2 * kStageBytes;
-    static constexpr int kPOff = kQOff + 2 * kQBytes;
-    static constexpr int kCtlOff = kPOff + (kPInK ? 0 : 2 * kPBytes);
-    static constexpr int kSmemBytes = kCtlOff + 512 + 1024;
+    static constexpr int kQOff = kItems * kItemBytes;
+    static constexpr int kCtlOff = kQOff + 2 * kQBytes;
+    static constexpr int kCtlBytes = 1024;
+    static constexpr int kSmemBytes = kCtlOff + kCtlBytes + 1024;
     static constexpr int KS = D / 16;
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
-// control block offsets (bytes from the control base)
-constexpr uint32_t kBarKvFull = 0, kBarKvEmpty = 16, kBarSFull = 32, kBarSFree = 48, kBarPFull = 64,
-                   kBarODone = 80, kBarFin = 88, kBarQFull = 96, kBarQEmpty = 112, kBarUFull = 128,
-                   kBarUEmpty = 144, kTmemSlot = 160, kAbort = 164, kMasks = 176, kRing = 256;
+// control block (byte offsets): mbarriers, then the TMEM slot, the abort
+// flag, the token masks of four stages and the ring of two unit records
+constexpr uint32_t kBarItemFull = 0;      // [8]
+constexpr uint32_t kBarItemEmpty = 64;    // [8]
+constexpr uint32_t kBarSFull = 128;       // [3]
+constexpr uint32_t kBarPFull = 152;       // [3]
+constexpr uint32_t kBarSFree = 176;       // [3]: P_j . V_j done (S buffer j % 3 free; O complete to stage j)
+constexpr uint32_t kBarFin = 208;
+constexpr uint32_t kBarQFull = 216;       // [2]
+constexpr uint32_t kBarQEmpty = 232;      // [2]
+constexpr uint32_t kBarUFull = 248;       // [2]
+constexpr uint32_t kBarUEmpty = 264;      // [2]
+constexpr uint32_t kTmemSlot = 280, kAbort = 284, kMasks = 288 /* [4][4] words */, kRing = 352 /* [2][4] int4 */;
+constexpr uint32_t kBarMaskFull = 512;    // [4]: masks of stage j published (slot j % 4)
+constexpr uint32_t kBarMaskEmpty = 544;   // [4]: masks of stage j read by the softmax warps
+static_assert(kRing + 128 <= kBarMaskFull && kBarMaskEmpty + 32 <= 1024, "control block");
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
+}
+// D[tmem] (+)= A[tmem] . B[smem]: the A operand read from tensor memory
+__device__ __forceinline__ void mma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
+                                            bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate ? 1u : 0u));
 }
 
 template <int D>
@@ -83,6 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         int max_q, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, unsigned long long total_units, int rt_max) {
     using C = UCfg<D>;
+    constexpr int NI = C::kItems;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -91,27 +112,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t ctl = base + C::kCtlOff;
     unsigned char* ctlp = smem + C::kCtlOff;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(ctlp + kAbort);
-    uint32_t* masks = reinterpret_cast<uint32_t*>(ctlp + kMasks);      // [2 stages][4 words]: tokens present
+    uint32_t* masks = reinterpret_cast<uint32_t*>(ctlp + kMasks);      // [4 stages][4 words]: tokens present
     int4* ring = reinterpret_cast<int4*>(ctlp + kRing);                // [2 units][4 int4]
-    auto kpart = [&](int s) { return base + s * C::kStageBytes; };
-    auto vpart = [&](int s) { return base + s * C::kStageBytes + C::kPartBytes; };
+    auto item = [&](uint32_t it) { return base + (it % NI) * C::kItemBytes; };
     auto qbuf = [&](int b) { return base + C::kQOff + b * C::kQBytes; };
-    auto pbuf = [&](int s) { return C::kPInK ? kpart(s) : base + C::kPOff + s * C::kPBytes; };
     auto bar = [&](uint32_t off, int i) { return ctl + off + 8 * i; };
 
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(kBarKvFull, i), 1);
-            mbar_init(bar(kBarKvEmpty, i), 1);
+        for (int i = 0; i < NI; ++i) {
+            mbar_init(bar(kBarItemFull, i), 1);
+            mbar_init(bar(kBarItemEmpty, i), 1);
+        }
+        for (int i = 0; i < kSBufs; ++i) {
             mbar_init(bar(kBarSFull, i), 1);
-            mbar_init(bar(kBarSFree, i), 4);
             mbar_init(bar(kBarPFull, i), 4);
+            mbar_init(bar(kBarSFree, i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(bar(kBarQFull, i), 1);
             mbar_init(bar(kBarQEmpty, i), 1);
             mbar_init(bar(kBarUFull, i), 1);
-            mbar_init(bar(kBarUEmpty, i), 5);
+            mbar_init(bar(kBarUEmpty, i), 6);
         }
-        mbar_init(bar(kBarODone, 0), 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(bar(kBarMaskFull, i), 1);
+            mbar_init(bar(kBarMaskEmpty, i), 4);
+        }
         mbar_init(bar(kBarFin, 0), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -136,6 +162,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
     };
+    // A parity wait is exact only while the barrier is within one phase of
+    // the awaited one, neither behind nor ahead; every wait below has that
+    // bound by construction (e.g. "P_j . V_j done" is waited on its S
+    // buffer's barrier, since S_j itself required P_{j-3} . V_{j-3} done).
+    // item `it` of the K/V ring: K_j is item 2j, V_j item 2j + 1 (j counted over the CTA's stages)
+    auto item_full_parity = [&](uint32_t it) { return (it / NI) & 1u; };
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
@@ -175,34 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!have) break;
 
-            // Q tile: rows (query, head) of this tile, zero past the last row
-            const int qb = un & 1;
-            if (un >= 2) ok = wait(bar(kBarQEmpty, qb), ((un >> 1) - 1) & 1, true);
-            if (__any_sync(0xffffffffu, !ok)) break;
-            {
-                constexpr int CH = 2 * D / 16;              // 16-byte chunks per row
-                const int rows_here = min(kURows, x.rows - x.rt * kURows);
-                const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-                const uint32_t qdst = qbuf(qb);
-#pragma unroll 4
-                for (int it = 0; it < kURows * CH / 32; ++it) {
-                    const int idx = it * 32 + lane;
-                    const int r = idx / CH, c = idx % CH;
-                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                    if (r < rows_here) {
-                        const int row = x.rt * kURows + r;
-                        const int qi = row / p.g, hh = row - qi * p.g;
-                        const size_t off = ((size_t)(x.q0 + qi) * p.Hq + x.kvh * p.g + hh) * D + c * 8;
-                        v = __ldg(reinterpret_cast<const uint4*>(q + off));
-                    }
-                    st_shared_v4(qdst + (c >> 3) * (kURows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4), v);
-                }
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) umma::mbar_arrive(bar(kBarQFull, qb));
-            }
-
-            // K/V stages; block-table entries come 32 at a time, one chunk ahead
+            // K/V tiles; block-table entries come 32 at a time, one chunk ahead
             const int nst = (x.k1 - x.k0 + kTok - 1) / kTok;
             const int bps = kTok / p.bs;                      // blocks per stage: 8 or 4
             const int unit_blocks = (x.k1 - x.k0 + p.bs - 1) / p.bs;
@@ -213,12 +218,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             int tab = load_chunk(0), tab_next = load_chunk(1), tab_chunk = 0;
             for (int j = 0; j < nst; ++j, ++g) {
-                const int s = g & 1;
-                if (g >= 2) ok = wait(bar(kBarKvEmpty, s), ((g >> 1) - 1) & 1, true);
-                if (__any_sync(0xffffffffu, !ok)) {
-                    bad = true;
-                    break;
-                }
                 const int ts = x.k0 + j * kTok;
                 const int tn = min(kTok, x.k1 - ts);
                 const int nb = (tn + p.bs - 1) / p.bs;
@@ -232,38 +231,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool bok = lane < nb && pb >= 0 && pb < p.NB;
                 if (lane < nb && !bok) report(p.err, PKV_DEVERR_BLOCK_ID);
                 const uint32_t bm = __ballot_sync(0xffffffffu, bok);
-                if (lane < 4) {
-                    // tokens 32 lane .. 32 lane + 31: present where their block is valid and t < tn
-                    uint32_t w;
-                    if (p.bs == 16) {
-                        const uint32_t b2 = (bm >> (2 * lane)) & 3u;
-                        w = ((b2 & 1u) ? 0x0000ffffu : 0u) | ((b2 & 2u) ? 0xffff0000u : 0u);
-                    } else {
-                        w = ((bm >> lane) & 1u) ? 0xffffffffu : 0u;
-                    }
-                    const int lo = 32 * lane;
-                    const uint32_t tm = tn >= lo + 32 ? 0xffffffffu : (tn <= lo ? 0u : ((1u << (tn - lo)) - 1u));
-                    masks[4 * s + lane] = w & tm;
-                }
-                constexpr int kPer = 2 * C::kHalves;       // boxes per block: K and V, each half
-                const int bi = lane / kPer, kv = (lane / C::kHalves) & 1, h = lane % C::kHalves;
+                const int bi = lane / C::kHalves, h = lane % C::kHalves;
                 const int pbb = __shfl_sync(0xffffffffu, pb, bi & 31);
                 const bool live = bi < nb && ((bm >> bi) & 1u);
                 const uint32_t nlive = __popc(__ballot_sync(0xffffffffu, live));
-                __syncwarp();
-                if (lane == 0) mbar_arrive_expect_tx(bar(kBarKvFull, s), nlive * box_bytes);
-                __syncwarp();
-                if (live) {
-                    const uint32_t dst = (kv ? vpart(s) : kpart(s)) + h * (kTok * 128) + bi * p.bs * 128;
-                    tensor_load_2d(dst, kv ? &vmap : &kmap, x.kvh * D + h * 64, pbb * p.bs, bar(kBarKvFull, s));
+                for (int kv = 0; kv < 2; ++kv) {
+                    const uint32_t it = 2 * g + kv;
+                    if (it >= (uint32_t)NI) ok = wait(bar(kBarItemEmpty, it % NI), ((it / NI) - 1) & 1, true);
+                    if (kv == 0 && g >= 4) ok = ok && wait(bar(kBarMaskEmpty, g & 3), ((g >> 2) - 1) & 1, true);
+                    if (__any_sync(0xffffffffu, !ok)) {
+                        bad = true;
+                        break;
+                    }
+                    if (kv == 0 && lane < 4) {
+                        // tokens 32 lane .. 32 lane + 31: present where their block is valid and t < tn
+                        uint32_t w;
+                        if (p.bs == 16) {
+                            const uint32_t b2 = (bm >> (2 * lane)) & 3u;
+                            w = ((b2 & 1u) ? 0x0000ffffu : 0u) | ((b2 & 2u) ? 0xffff0000u : 0u);
+                        } else {
+                            w = ((bm >> lane) & 1u) ? 0xffffffffu : 0u;
+                        }
+                        const int lo = 32 * lane;
+                        const uint32_t tm =
+                            tn >= lo + 32 ? 0xffffffffu : (tn <= lo ? 0u : ((1u << (tn - lo)) - 1u));
+                        masks[4 * (g & 3) + lane] = w & tm;
+                    }
+                    __syncwarp();
+                    if (kv == 0 && lane == 0) umma::mbar_arrive(bar(kBarMaskFull, g & 3));
+                    if (lane == 0) mbar_arrive_expect_tx(bar(kBarItemFull, it % NI), nlive * box_bytes);
+                    __syncwarp();
+                    if (live)
+                        tensor_load_2d(item(it) + h * (kTok * 128) + bi * p.bs * 128, kv ? &vmap : &kmap,
+                                       x.kvh * D + h * 64, pbb * p.bs, bar(kBarItemFull, it % NI));
                 }
+                if (bad) break;
             }
             if (bad) break;
             ++un;
         }
         // copies still in flight land before the CTA leaves
-        if (g >= 1) wait(bar(kBarKvFull, (g - 1) & 1), ((g - 1) >> 1) & 1, false);
-        if (g >= 2) wait(bar(kBarKvFull, g & 1), ((g - 2) >> 1) & 1, false);
+        for (uint32_t k = 1; k <= (uint32_t)NI && k <= 2 * g; ++k) {
+            const uint32_t it = 2 * g - k;
+            wait(bar(kBarItemFull, it % NI), item_full_parity(it), false);
+        }
         if (p.sched != nullptr && lane == 0) {
             unsigned long long* ctr = reinterpret_cast<unsigned long long*>(p.sched);
             __threadfence();
@@ -272,6 +283,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atomicExch(ctr, 0ull);
                 atomicExch(ctr + 1, 0ull);
             }
+        }
+    } else if (warp == kQWarp) {
+        // ------------------------------------------------------------ Q loader
+        uint32_t un = 0;
+        bool ok = true;
+        const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
+        for (;;) {
+            const int slot = un & 1;
+            ok = wait(bar(kBarUFull, slot), (un >> 1) & 1, true);
+            if (__any_sync(0xffffffffu, !ok)) break;
+            const int4 e0 = ring[4 * slot], e2 = ring[4 * slot + 2];
+            __syncwarp();
+            if (lane == 0) umma::mbar_arrive(bar(kBarUEmpty, slot));
+            if (e2.w == 0) break;
+            const int qb = un & 1;
+            if (un >= 2) ok = wait(bar(kBarQEmpty, qb), ((un >> 1) - 1) & 1, true);
+            if (__any_sync(0xffffffffu, !ok)) break;
+            const int kvh = e0.y, rt = e0.z, q0 = e2.x, rows = e2.z;
+            constexpr int CH = 2 * D / 16;               // 16-byte chunks per row
+            constexpr int kBatch = 16;                   // loads in flight per lane
+            static_assert((kURows * CH / 32) % kBatch == 0, "Q load batches");
+            const int rows_here = min(kURows, rows - rt * kURows);
+            const uint32_t qdst = qbuf(qb);
+            for (int it0 = 0; it0 < kURows * CH / 32; it0 += kBatch) {
+                uint4 v[kBatch];
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) {
+                    const int idx = (it0 + k) * 32 + lane;
+                    const int r = idx / CH, c = idx % CH;
+                    v[k] = make_uint4(0u, 0u, 0u, 0u);
+                    if (r < rows_here) {
+                        const int row = rt * kURows + r;
+                        const int qi = row / p.g, hh = row - qi * p.g;
+                        const size_t off = ((size_t)(q0 + qi) * p.Hq + kvh * p.g + hh) * D + c * 8;
+                        v[k] = __ldg(reinterpret_cast<const uint4*>(q + off));
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) {
+                    const int idx = (it0 + k) * 32 + lane;
+                    const int r = idx / CH, c = idx % CH;
+                    st_shared_v4(qdst + (c >> 3) * (kURows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4), v[k]);
+                }
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) umma::mbar_arrive(bar(kBarQFull, qb));
+            ++un;
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------- MMA issue
@@ -282,17 +341,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             long long pv_pending = -1;
             bool pv_first = false, ok = true;
             auto issue_pv = [&](uint32_t gp, bool first) -> bool {
-                const int s = gp & 1;
-                if (!wait(bar(kBarPFull, s), (gp >> 1) & 1, true)) return false;
+                const int b = gp % kSBufs;
+                const uint32_t it = 2 * gp + 1;
+                if (!wait(bar(kBarItemFull, it % NI), item_full_parity(it), true) ||
+                    !wait(bar(kBarPFull, b), (gp / kSBufs) & 1, true))
+                    return false;
                 umma::fence_after_sync();
+                const uint32_t vb = item(it);
 #pragma unroll
                 for (int kk = 0; kk < kTok / 16; ++kk) {
-                    const uint64_t a = umma::desc_sw128(pbuf(s) + (kk >> 2) * (kURows * 128) + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = umma::desc_sw128(vpart(s) + kk * 2048, kTok * 128, 1024);
-                    umma::mma_bf16(tmem + kTmemO, a, b, idPV, !(first && kk == 0));
+                    const uint64_t bd = umma::desc_sw128(vb + kk * 2048, kTok * 128, 1024);
+                    mma_bf16_ts(tmem + kTmemO, tmem + b * kTok + kk * 8, bd, idPV, !(first && kk == 0));
                 }
-                umma::commit(bar(kBarODone, 0));
-                umma::commit(bar(kBarKvEmpty, s));
+                umma::commit(bar(kBarItemEmpty, it % NI));
+                umma::commit(bar(kBarSFree, b));      // also: O holds every product up to this one
                 return true;
             };
             for (;;) {
@@ -305,22 +367,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int qb = un & 1;
                 if (!wait(bar(kBarQFull, qb), (un >> 1) & 1, true)) break;
                 for (int j = 0; j < nst; ++j, ++g) {
-                    const int s = g & 1;
-                    if (!wait(bar(kBarKvFull, s), (g >> 1) & 1, true) ||
-                        (g >= 2 && !wait(bar(kBarSFree, s), ((g >> 1) - 1) & 1, true))) {
+                    const int b = g % kSBufs;
+                    const uint32_t it = 2 * g;
+                    if (!wait(bar(kBarItemFull, it % NI), item_full_parity(it), true) ||
+                        (g >= (uint32_t)kSBufs && !wait(bar(kBarSFree, b), ((g / kSBufs) - 1) & 1, true))) {
                         ok = false;
                         break;
                     }
                     umma::fence_after_sync();
+                    const uint32_t kb = item(it);
 #pragma unroll
                     for (int kk = 0; kk < C::KS; ++kk) {
                         const uint64_t a =
                             umma::desc_sw128(qbuf(qb) + (kk >> 2) * (kURows * 128) + (kk & 3) * 32, 16, 1024);
-                        const uint64_t b =
-                            umma::desc_sw128(kpart(s) + (kk >> 2) * (kTok * 128) + (kk & 3) * 32, 16, 1024);
-                        umma::mma_bf16(tmem + s * kTok, a, b, idS, kk > 0);
+                        const uint64_t bd = umma::desc_sw128(kb + (kk >> 2) * (kTok * 128) + (kk & 3) * 32, 16, 1024);
+                        umma::mma_bf16(tmem + b * kTok, a, bd, idS, kk > 0);
                     }
-                    umma::commit(bar(kBarSFull, s));
+                    umma::commit(bar(kBarSFull, b));
+                    umma::commit(bar(kBarItemEmpty, it % NI));
                     if (j == nst - 1) umma::commit(bar(kBarQEmpty, qb));
                     if (pv_pending >= 0 && !issue_pv((uint32_t)pv_pending, pv_first)) {
                         ok = false;
@@ -363,8 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_ref = -CUDART_INF_F, l = 0.f;
             const int nst = (k1 - k0 + kTok - 1) / kTok;
             for (int j = 0; j < nst; ++j, ++g) {
-                const int s = g & 1;
-                ok = wait(bar(kBarSFull, s), (g >> 1) & 1, true) && wait(bar(kBarKvFull, s), (g >> 1) & 1, true);
+                const int b = g % kSBufs;
+                // S_j done, and the producer's token masks of stage j published
+                ok = wait(bar(kBarSFull, b), (g / kSBufs) & 1, true) &&
+                     wait(bar(kBarMaskFull, g & 3), (g >> 2) & 1, true);
                 if (__any_sync(0xffffffffu, !ok)) {
                     bad = true;
                     break;
@@ -372,17 +438,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma::fence_after_sync();
                 uint32_t sr[4][32];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) umma::tmem_ld32(tmem + lane_base + s * kTok + 32 * q, sr[q]);
+                for (int q = 0; q < 4; ++q) umma::tmem_ld32(tmem + lane_base + b * kTok + 32 * q, sr[q]);
                 umma::tmem_wait_ld();
-                umma::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) umma::mbar_arrive(bar(kBarSFree, s));
 
                 const int lim = pos - (k0 + j * kTok);           // tokens t <= lim are visible to this row
                 uint32_t mw[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) mw[q] = masks[4 * s + q];
-                const bool whole = lim >= kTok - 1 && (mw[0] & mw[1] & mw[2] & mw[3]) == 0xffffffffu;
+                for (int q = 0; q < 4; ++q) mw[q] = masks[4 * (g & 3) + q];
+                __syncwarp();
+                if (lane == 0) umma::mbar_arrive(bar(kBarMaskEmpty, g & 3));
+                const bool all_present = (mw[0] & mw[1] & mw[2] & mw[3]) == 0xffffffffu;
+                const bool whole = lim >= kTok - 1 && all_present;
                 float mx8[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) mx8[k] = -CUDART_INF_F;
@@ -390,20 +456,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
 #pragma unroll
-                        for (int b = 0; b < 32; ++b) {
-                            const float xv = __uint_as_float(sr[q][b]) * scl;
-                            sr[q][b] = __float_as_uint(xv);
-                            mx8[b & 7] = fmaxf(mx8[b & 7], xv);
+                        for (int bb = 0; bb < 32; ++bb) {
+                            const float xv = __uint_as_float(sr[q][bb]) * scl;
+                            sr[q][bb] = __float_as_uint(xv);
+                            mx8[bb & 7] = fmaxf(mx8[bb & 7], xv);
                         }
                 } else {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
 #pragma unroll
-                        for (int b = 0; b < 32; ++b) {
-                            const bool live = ((mw[q] >> b) & 1u) && (32 * q + b) <= lim;
-                            const float xv = live ? __uint_as_float(sr[q][b]) * scl : -CUDART_INF_F;
-                            sr[q][b] = __float_as_uint(xv);
-                            mx8[b & 7] = fmaxf(mx8[b & 7], xv);
+                        for (int bb = 0; bb < 32; ++bb) {
+                            const bool live = ((mw[q] >> bb) & 1u) && (32 * q + bb) <= lim;
+                            const float xv = live ? __uint_as_float(sr[q][bb]) * scl : -CUDART_INF_F;
+                            sr[q][bb] = __float_as_uint(xv);
+                            mx8[bb & 7] = fmaxf(mx8[bb & 7], xv);
                         }
                 }
                 const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
@@ -421,8 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 l *= alpha;
                 if (__any_sync(0xffffffffu, resc)) {
-                    // O holds P_{j-1} . V_{j-1}: wait for that product, then scale in place
-                    ok = wait(bar(kBarODone, 0), (g - 1) & 1, true);
+                    // O holds the products up to stage j-1: wait for the last, then scale in place
+                    ok = wait(bar(kBarSFree, (g - 1) % kSBufs), ((g - 1) / kSBufs) & 1, true);
                     if (__any_sync(0xffffffffu, !ok)) {
                         bad = true;
                         break;
@@ -439,45 +505,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     umma::tmem_wait_st();
                 }
-                // V rows of tokens that were not loaded are zeroed (0 * garbage could be NaN)
-                if (!((mw[i >> 5] >> (i & 31)) & 1u)) {
+                // V rows of tokens that were not loaded are zeroed (0 * stale data could be NaN)
+                if (!__all_sync(0xffffffffu, all_present)) {
+                    ok = wait(bar(kBarItemFull, (2 * g + 1) % NI), item_full_parity(2 * g + 1), true);
+                    if (__any_sync(0xffffffffu, !ok)) {
+                        bad = true;
+                        break;
+                    }
+                    if (!((mw[i >> 5] >> (i & 31)) & 1u)) {
+                        const uint32_t vb = item(2 * g + 1);
 #pragma unroll
-                    for (int h = 0; h < C::kHalves; ++h)
+                        for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            st_shared_v4(vpart(s) + h * (kTok * 128) + i * 128 + c * 16, make_uint4(0u, 0u, 0u, 0u));
+                            for (int c = 0; c < 8; ++c)
+                                st_shared_v4(vb + h * (kTok * 128) + i * 128 + c * 16, make_uint4(0u, 0u, 0u, 0u));
+                    }
+                    fence_proxy_async();
                 }
-                // P row: 2^(x - m), bf16, 128-byte swizzled K-major rows of 64 tokens
+                // P row: 2^(x - m) as bf16 pairs over columns 0..63 of S_j's buffer
                 const float mb = m_ref == -CUDART_INF_F ? 0.f : m_ref;
                 float ls[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) ls[k] = 0.f;
-                const uint32_t prow = pbuf(s) + i * 128;
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    uint32_t w[4];
+                for (int hq = 0; hq < 2; ++hq) {
+                    uint32_t pw[32];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int t = 8 * c + 2 * k;
+                    for (int k = 0; k < 32; ++k) {
+                        const int t = 64 * hq + 2 * k;
                         const float a0 = fast_exp2(__uint_as_float(sr[t >> 5][t & 31]) - mb);
                         const float a1 = fast_exp2(__uint_as_float(sr[(t + 1) >> 5][(t + 1) & 31]) - mb);
-                        ls[2 * k] += a0;
-                        ls[2 * k + 1] += a1;
-                        w[k] = pack2<false>(a0, a1);
+                        ls[(2 * k) & 7] += a0;
+                        ls[(2 * k + 1) & 7] += a1;
+                        pw[k] = pack2<false>(a0, a1);
                     }
-                    st_shared_v4(prow + (c >> 3) * (kURows * 128) + (((c & 7) ^ (i & 7)) << 4),
-                                 make_uint4(w[0], w[1], w[2], w[3]));
+                    umma::tmem_st32(tmem + lane_base + b * kTok + 32 * hq, pw);
                 }
                 l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-                fence_proxy_async();
+                umma::tmem_wait_st();
                 umma::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) umma::mbar_arrive(bar(kBarPFull, s));
+                if (lane == 0) umma::mbar_arrive(bar(kBarPFull, b));
             }
             if (bad) break;
 
             // epilogue: O / l, or the partition's (m, l, O)
-            ok = wait(bar(kBarODone, 0), (g - 1) & 1, true);
+            ok = wait(bar(kBarSFree, (g - 1) % kSBufs), ((g - 1) / kSBufs) & 1, true);
             if (__any_sync(0xffffffffu, !ok)) break;
             umma::fence_after_sync();
             const size_t hrow = (size_t)(q0 + qi) * p.Hq + kvh * p.g + hh;

@@ -235,3 +235,20 @@ def test_full_size_query_chunks(name, nseq, nq, kernel):
     of = out.float()
     assert torch.isfinite(of).all()
     assert float(of.abs().max()) <= float(c.v_cache.float().abs().max()) * 1.01 + 1e-3
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_prefill_growing_logits_rescale(kernel):
+    """Keys whose scale grows along the sequence (token t scaled by
+    1 + t / 40): each 128-token stage's largest logit exceeds the previous
+    ones by far more than 2^8, so the kernels must rescale the running
+    output many times; the softmax itself is unchanged by that."""
+    w, hv, qs, q32 = _case("qwen2.5-1.5b", [1100, 700, 260], [300, 5, 260], 8, 2, 128, seed=9)
+    for s in range(w.S):
+        n = int(w.context_lens[s])
+        for t in range(n):
+            b = int(w.block_tables[s, t // w.bs])
+            hv.k_pool[b, t % w.bs] *= np.float32(1.0 + t / 40.0)
+    for partition in (-1, 256):
+        out = _run(w, hv, qs, q32, partition, kernel=kernel)
+        assert_close(out, _ref(w, hv, qs, q32), W.DT_BF16, f"growing logits {kernel} P={partition}")
