@@ -57,9 +57,11 @@ template <int D>
 struct UCfg {
     static constexpr int kHalves = D / 64;                 // 128-byte halves of a Q/K/V row
     static constexpr int kItemBytes = kTok * 2 * D;        // one K or V tile of a stage
-    static constexpr int kItems = D == 128 ? 5 : 8;        // ring of K/V tiles
+    static constexpr int kKItems = D == 128 ? 3 : 4;       // ring of K tiles
+    static constexpr int kVItems = D == 128 ? 2 : 4;       // ring of V tiles
     static constexpr int kQBytes = kURows * 2 * D;
-    static constexpr int kQOff = kItems * kItemBytes;
+    static constexpr int kVOff = kKItems * kItemBytes;
+    static constexpr int kQOff = (kKItems + kVItems) * kItemBytes;
     static constexpr int kCtlOff = kQOff + 2 * kQBytes;
     static constexpr int kCtlBytes = 1024;
     static constexpr int kSmemBytes = kCtlOff + kCtlBytes + 1024;
@@ -69,8 +71,10 @@ struct UCfg {
 
 // control block (byte offsets): mbarriers, then the TMEM slot, the abort
 // flag, the token masks of four stages and the ring of two unit records
-constexpr uint32_t kBarItemFull = 0;      // [8]
-constexpr uint32_t kBarItemEmpty = 64;    // [8]
+constexpr uint32_t kBarKFull = 0;         // [4]
+constexpr uint32_t kBarKEmpty = 32;       // [4]
+constexpr uint32_t kBarVFull = 64;        // [4]
+constexpr uint32_t kBarVEmpty = 96;       // [4]
 constexpr uint32_t kBarSFull = 128;       // [3]
 constexpr uint32_t kBarPFull = 152;       // [3]
 constexpr uint32_t kBarSFree = 176;       // [3]: P_j . V_j done (S buffer j % 3 free; O complete to stage j)
@@ -103,7 +107,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         int max_q, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, unsigned long long total_units, int rt_max) {
     using C = UCfg<D>;
-    constexpr int NI = C::kItems;
+    constexpr int NK = C::kKItems, NV = C::kVItems;
+    static_assert(NK <= 4 && NV <= 4, "barrier slots");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -114,14 +119,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(ctlp + kAbort);
     uint32_t* masks = reinterpret_cast<uint32_t*>(ctlp + kMasks);      // [4 stages][4 words]: tokens present
     int4* ring = reinterpret_cast<int4*>(ctlp + kRing);                // [2 units][4 int4]
-    auto item = [&](uint32_t it) { return base + (it % NI) * C::kItemBytes; };
+    auto ktile = [&](uint32_t j) { return base + (j % NK) * C::kItemBytes; };
+    auto vtile = [&](uint32_t j) { return base + C::kVOff + (j % NV) * C::kItemBytes; };
     auto qbuf = [&](int b) { return base + C::kQOff + b * C::kQBytes; };
     auto bar = [&](uint32_t off, int i) { return ctl + off + 8 * i; };
 
     if (tid == 0) {
-        for (int i = 0; i < NI; ++i) {
-            mbar_init(bar(kBarItemFull, i), 1);
-            mbar_init(bar(kBarItemEmpty, i), 1);
+        for (int i = 0; i < NK; ++i) {
+            mbar_init(bar(kBarKFull, i), 1);
+            mbar_init(bar(kBarKEmpty, i), 1);
+        }
+        for (int i = 0; i < NV; ++i) {
+            mbar_init(bar(kBarVFull, i), 1);
+            mbar_init(bar(kBarVEmpty, i), 1);
         }
         for (int i = 0; i < kSBufs; ++i) {
             mbar_init(bar(kBarSFull, i), 1);
@@ -166,8 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the awaited one, neither behind nor ahead; every wait below has that
     // bound by construction (e.g. "P_j . V_j done" is waited on its S
     // buffer's barrier, since S_j itself required P_{j-3} . V_{j-3} done).
-    // item `it` of the K/V ring: K_j is item 2j, V_j item 2j + 1 (j counted over the CTA's stages)
-    auto item_full_parity = [&](uint32_t it) { return (it / NI) & 1u; };
+    // K_j sits in slot j % NK of the K ring (phase j / NK), V_j in slot j % NV
+    // of the V ring (j counted over the CTA's stages)
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
@@ -217,7 +227,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return rb < unit_blocks ? __ldg(trow + rb) : 0;
             };
             int tab = load_chunk(0), tab_next = load_chunk(1), tab_chunk = 0;
-            for (int j = 0; j < nst; ++j, ++g) {
+            // one tile into its ring: K_j also publishes the token masks of stage j
+            auto issue = [&](bool isv, uint32_t gs, int pbv, uint32_t bmv, int nbv, int tnv) -> bool {
+                const uint32_t n_ring = isv ? NV : NK;
+                const uint32_t slot = gs % n_ring, ph = gs / n_ring;
+                if (ph >= 1) ok = wait(bar(isv ? kBarVEmpty : kBarKEmpty, slot), (ph - 1) & 1, true);
+                if (!isv && gs >= 4) ok = ok && wait(bar(kBarMaskEmpty, gs & 3), ((gs >> 2) - 1) & 1, true);
+                if (__any_sync(0xffffffffu, !ok)) return false;
+                if (!isv && lane < 4) {
+                    // tokens 32 lane .. 32 lane + 31: present where their block is valid and t < tn
+                    uint32_t w;
+                    if (p.bs == 16) {
+                        const uint32_t b2 = (bmv >> (2 * lane)) & 3u;
+                        w = ((b2 & 1u) ? 0x0000ffffu : 0u) | ((b2 & 2u) ? 0xffff0000u : 0u);
+                    } else {
+                        w = ((bmv >> lane) & 1u) ? 0xffffffffu : 0u;
+                    }
+                    const int lo = 32 * lane;
+                    const uint32_t tm = tnv >= lo + 32 ? 0xffffffffu : (tnv <= lo ? 0u : ((1u << (tnv - lo)) - 1u));
+                    masks[4 * (gs & 3) + lane] = w & tm;
+                }
+                __syncwarp();
+                if (!isv && lane == 0) umma::mbar_arrive(bar(kBarMaskFull, gs & 3));
+                const int bi = lane / C::kHalves, h = lane % C::kHalves;
+                const int pbb = __shfl_sync(0xffffffffu, pbv, bi & 31);
+                const bool live = bi < nbv && ((bmv >> bi) & 1u);
+                const uint32_t nlive = __popc(__ballot_sync(0xffffffffu, live));
+                const uint32_t full = bar(isv ? kBarVFull : kBarKFull, slot);
+                if (lane == 0) mbar_arrive_expect_tx(full, nlive * box_bytes);
+                __syncwarp();
+                if (live)
+                    tensor_load_2d((isv ? vtile(gs) : ktile(gs)) + h * (kTok * 128) + bi * p.bs * 128,
+                                   isv ? &vmap : &kmap, x.kvh * D + h * 64, pbb * p.bs, full);
+                return true;
+            };
+            // K runs one stage ahead of V: K_0, K_1, V_0, K_2, V_1, ..., V_last
+            int pv_pb = 0, pv_nb = 0, pv_tn = 0;
+            uint32_t pv_bm = 0;
+            for (int j = 0; j < nst; ++j) {
                 const int ts = x.k0 + j * kTok;
                 const int tn = min(kTok, x.k1 - ts);
                 const int nb = (tn + p.bs - 1) / p.bs;
@@ -231,50 +278,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool bok = lane < nb && pb >= 0 && pb < p.NB;
                 if (lane < nb && !bok) report(p.err, PKV_DEVERR_BLOCK_ID);
                 const uint32_t bm = __ballot_sync(0xffffffffu, bok);
-                const int bi = lane / C::kHalves, h = lane % C::kHalves;
-                const int pbb = __shfl_sync(0xffffffffu, pb, bi & 31);
-                const bool live = bi < nb && ((bm >> bi) & 1u);
-                const uint32_t nlive = __popc(__ballot_sync(0xffffffffu, live));
-                for (int kv = 0; kv < 2; ++kv) {
-                    const uint32_t it = 2 * g + kv;
-                    if (it >= (uint32_t)NI) ok = wait(bar(kBarItemEmpty, it % NI), ((it / NI) - 1) & 1, true);
-                    if (kv == 0 && g >= 4) ok = ok && wait(bar(kBarMaskEmpty, g & 3), ((g >> 2) - 1) & 1, true);
-                    if (__any_sync(0xffffffffu, !ok)) {
-                        bad = true;
-                        break;
-                    }
-                    if (kv == 0 && lane < 4) {
-                        // tokens 32 lane .. 32 lane + 31: present where their block is valid and t < tn
-                        uint32_t w;
-                        if (p.bs == 16) {
-                            const uint32_t b2 = (bm >> (2 * lane)) & 3u;
-                            w = ((b2 & 1u) ? 0x0000ffffu : 0u) | ((b2 & 2u) ? 0xffff0000u : 0u);
-                        } else {
-                            w = ((bm >> lane) & 1u) ? 0xffffffffu : 0u;
-                        }
-                        const int lo = 32 * lane;
-                        const uint32_t tm =
-                            tn >= lo + 32 ? 0xffffffffu : (tn <= lo ? 0u : ((1u << (tn - lo)) - 1u));
-                        masks[4 * (g & 3) + lane] = w & tm;
-                    }
-                    __syncwarp();
-                    if (kv == 0 && lane == 0) umma::mbar_arrive(bar(kBarMaskFull, g & 3));
-                    if (lane == 0) mbar_arrive_expect_tx(bar(kBarItemFull, it % NI), nlive * box_bytes);
-                    __syncwarp();
-                    if (live)
-                        tensor_load_2d(item(it) + h * (kTok * 128) + bi * p.bs * 128, kv ? &vmap : &kmap,
-                                       x.kvh * D + h * 64, pbb * p.bs, bar(kBarItemFull, it % NI));
+                if (!issue(false, g + j, pb, bm, nb, tn) ||
+                    (j > 0 && !issue(true, g + j - 1, pv_pb, pv_bm, pv_nb, pv_tn))) {
+                    bad = true;
+                    break;
                 }
-                if (bad) break;
+                pv_pb = pb;
+                pv_bm = bm;
+                pv_nb = nb;
+                pv_tn = tn;
             }
+            if (!bad && !issue(true, g + nst - 1, pv_pb, pv_bm, pv_nb, pv_tn)) bad = true;
+            g += nst;
             if (bad) break;
             ++un;
         }
         // copies still in flight land before the CTA leaves
-        for (uint32_t k = 1; k <= (uint32_t)NI && k <= 2 * g; ++k) {
-            const uint32_t it = 2 * g - k;
-            wait(bar(kBarItemFull, it % NI), item_full_parity(it), false);
-        }
+        for (uint32_t k = 1; k <= (uint32_t)NK && k <= g; ++k)
+            wait(bar(kBarKFull, (g - k) % NK), ((g - k) / NK) & 1, false);
+        for (uint32_t k = 1; k <= (uint32_t)NV && k <= g; ++k)
+            wait(bar(kBarVFull, (g - k) % NV), ((g - k) / NV) & 1, false);
         if (p.sched != nullptr && lane == 0) {
             unsigned long long* ctr = reinterpret_cast<unsigned long long*>(p.sched);
             __threadfence();
@@ -342,18 +365,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool pv_first = false, ok = true;
             auto issue_pv = [&](uint32_t gp, bool first) -> bool {
                 const int b = gp % kSBufs;
-                const uint32_t it = 2 * gp + 1;
-                if (!wait(bar(kBarItemFull, it % NI), item_full_parity(it), true) ||
+                if (!wait(bar(kBarVFull, gp % NV), (gp / NV) & 1, true) ||
                     !wait(bar(kBarPFull, b), (gp / kSBufs) & 1, true))
                     return false;
                 umma::fence_after_sync();
-                const uint32_t vb = item(it);
+                const uint32_t vb = vtile(gp);
 #pragma unroll
                 for (int kk = 0; kk < kTok / 16; ++kk) {
                     const uint64_t bd = umma::desc_sw128(vb + kk * 2048, kTok * 128, 1024);
                     mma_bf16_ts(tmem + kTmemO, tmem + b * kTok + kk * 8, bd, idPV, !(first && kk == 0));
                 }
-                umma::commit(bar(kBarItemEmpty, it % NI));
+                umma::commit(bar(kBarVEmpty, gp % NV));
                 umma::commit(bar(kBarSFree, b));      // also: O holds every product up to this one
                 return true;
             };
@@ -368,14 +390,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait(bar(kBarQFull, qb), (un >> 1) & 1, true)) break;
                 for (int j = 0; j < nst; ++j, ++g) {
                     const int b = g % kSBufs;
-                    const uint32_t it = 2 * g;
-                    if (!wait(bar(kBarItemFull, it % NI), item_full_parity(it), true) ||
+                    if (!wait(bar(kBarKFull, g % NK), (g / NK) & 1, true) ||
                         (g >= (uint32_t)kSBufs && !wait(bar(kBarSFree, b), ((g / kSBufs) - 1) & 1, true))) {
                         ok = false;
                         break;
                     }
                     umma::fence_after_sync();
-                    const uint32_t kb = item(it);
+                    const uint32_t kb = ktile(g);
 #pragma unroll
                     for (int kk = 0; kk < C::KS; ++kk) {
                         const uint64_t a =
@@ -384,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         umma::mma_bf16(tmem + b * kTok, a, bd, idS, kk > 0);
                     }
                     umma::commit(bar(kBarSFull, b));
-                    umma::commit(bar(kBarItemEmpty, it % NI));
+                    umma::commit(bar(kBarKEmpty, g % NK));
                     if (j == nst - 1) umma::commit(bar(kBarQEmpty, qb));
                     if (pv_pending >= 0 && !issue_pv((uint32_t)pv_pending, pv_first)) {
                         ok = false;
@@ -448,19 +469,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) umma::mbar_arrive(bar(kBarMaskEmpty, g & 3));
                 const bool all_present = (mw[0] & mw[1] & mw[2] & mw[3]) == 0xffffffffu;
-                const bool whole = lim >= kTok - 1 && all_present;
+                // rows past the tile's last take the same path: their output is never stored
+                const bool whole = ((lim >= kTok - 1 && all_present) || !rv) && scl > 0.f;
                 float mx8[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) mx8[k] = -CUDART_INF_F;
-                if (whole) {                                     // every token present and visible
+                if (whole) {                 // every token present and visible: max of the raw logits
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
 #pragma unroll
-                        for (int bb = 0; bb < 32; ++bb) {
-                            const float xv = __uint_as_float(sr[q][bb]) * scl;
-                            sr[q][bb] = __float_as_uint(xv);
-                            mx8[bb & 7] = fmaxf(mx8[bb & 7], xv);
-                        }
+                        for (int bb = 0; bb < 32; ++bb) mx8[bb & 7] = fmaxf(mx8[bb & 7], __uint_as_float(sr[q][bb]));
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mx8[k] *= scl;
                 } else {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
@@ -507,13 +527,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // V rows of tokens that were not loaded are zeroed (0 * stale data could be NaN)
                 if (!__all_sync(0xffffffffu, all_present)) {
-                    ok = wait(bar(kBarItemFull, (2 * g + 1) % NI), item_full_parity(2 * g + 1), true);
+                    ok = wait(bar(kBarVFull, g % NV), (g / NV) & 1, true);
                     if (__any_sync(0xffffffffu, !ok)) {
                         bad = true;
                         break;
                     }
                     if (!((mw[i >> 5] >> (i & 31)) & 1u)) {
-                        const uint32_t vb = item(2 * g + 1);
+                        const uint32_t vb = vtile(g);
 #pragma unroll
                         for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
@@ -522,8 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     fence_proxy_async();
                 }
-                // P row: 2^(x - m) as bf16 pairs over columns 0..63 of S_j's buffer
+                // P row: 2^(x - m) as bf16 pairs over columns 0..63 of S_j's buffer; on the
+                // fast path x = scl * s enters through one fused multiply-add
                 const float mb = m_ref == -CUDART_INF_F ? 0.f : m_ref;
+                const float xs = whole ? scl : 1.f;
                 float ls[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) ls[k] = 0.f;
@@ -533,8 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
                         const int t = 64 * hq + 2 * k;
-                        const float a0 = fast_exp2(__uint_as_float(sr[t >> 5][t & 31]) - mb);
-                        const float a1 = fast_exp2(__uint_as_float(sr[(t + 1) >> 5][(t + 1) & 31]) - mb);
+                        const float a0 = fast_exp2(fmaf(__uint_as_float(sr[t >> 5][t & 31]), xs, -mb));
+                        const float a1 = fast_exp2(fmaf(__uint_as_float(sr[(t + 1) >> 5][(t + 1) & 31]), xs, -mb));
                         ls[(2 * k) & 7] += a0;
                         ls[(2 * k + 1) & 7] += a1;
                         pw[k] = pack2<false>(a0, a1);
