@@ -10,10 +10,12 @@
 //
 // Work unit: (sequence, K/V head, tile of 128 (query, head) rows, partition
 // of P key tokens); one persistent CTA per SM claims units in order.  Roles:
-//   warp 4      producer: claims units and streams 128-token tiles, K_j then
-//               V_j, into one ring of shared-memory items by TMA tensor
-//               copies (one box per block and 64-value half row, 128-byte
-//               swizzle).  K_j's item is released as soon as S_j is done.
+//   warp 4      K producer: claims units and streams 128-token K tiles into
+//               a ring of shared-memory slots by TMA tensor copies (one box
+//               per block and 64-value half row, 128-byte swizzle), with the
+//               stage's token masks.  K_j's slot is released once S_j is done.
+//   warp 7      V producer: the V tiles of the same units into their own
+//               ring; V_j's slot is released once P_j . V_j is done.
 //   warp 6      Q loader: the tile's 128 rows of Q into one of two buffers.
 //   warp 5      one thread issues the MMAs:
 //                 S_j = Q . K_j^T        M 128, N 128, K d   (TMEM, 3 buffers)
@@ -46,8 +48,8 @@ using namespace tc;
 constexpr int kTok = 128;            // key tokens per stage
 constexpr int kURows = 128;          // (query, head) rows per tile: M of both products
 constexpr int kSBufs = 3;            // S (and P) buffers in TMEM
-constexpr int kThreads = 224;
-constexpr int kProducerWarp = 4, kMmaWarp = 5, kQWarp = 6;
+constexpr int kThreads = 256;
+constexpr int kProducerWarp = 4, kMmaWarp = 5, kQWarp = 6, kVWarp = 7;
 constexpr float kRescaleLog2 = 8.f;
 constexpr long long kUWaitLimit = 4000000000LL;   // ~2 s: a barrier that never completes
 constexpr uint32_t kTmemCols = 512;               // S buffers at 0, 128, 256; O at 384
@@ -142,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kBarQFull, i), 1);
             mbar_init(bar(kBarQEmpty, i), 1);
             mbar_init(bar(kBarUFull, i), 1);
-            mbar_init(bar(kBarUEmpty, i), 6);
+            mbar_init(bar(kBarUEmpty, i), 7);
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(bar(kBarMaskFull, i), 1);
@@ -261,9 +263,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    isv ? &vmap : &kmap, x.kvh * D + h * 64, pbb * p.bs, full);
                 return true;
             };
-            // K runs one stage ahead of V: K_0, K_1, V_0, K_2, V_1, ..., V_last
-            int pv_pb = 0, pv_nb = 0, pv_tn = 0;
-            uint32_t pv_bm = 0;
             for (int j = 0; j < nst; ++j) {
                 const int ts = x.k0 + j * kTok;
                 const int tn = min(kTok, x.k1 - ts);
@@ -278,17 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool bok = lane < nb && pb >= 0 && pb < p.NB;
                 if (lane < nb && !bok) report(p.err, PKV_DEVERR_BLOCK_ID);
                 const uint32_t bm = __ballot_sync(0xffffffffu, bok);
-                if (!issue(false, g + j, pb, bm, nb, tn) ||
-                    (j > 0 && !issue(true, g + j - 1, pv_pb, pv_bm, pv_nb, pv_tn))) {
+                if (!issue(false, g + j, pb, bm, nb, tn)) {
                     bad = true;
                     break;
                 }
-                pv_pb = pb;
-                pv_bm = bm;
-                pv_nb = nb;
-                pv_tn = tn;
             }
-            if (!bad && !issue(true, g + nst - 1, pv_pb, pv_bm, pv_nb, pv_tn)) bad = true;
             g += nst;
             if (bad) break;
             ++un;
@@ -296,8 +289,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // copies still in flight land before the CTA leaves
         for (uint32_t k = 1; k <= (uint32_t)NK && k <= g; ++k)
             wait(bar(kBarKFull, (g - k) % NK), ((g - k) / NK) & 1, false);
-        for (uint32_t k = 1; k <= (uint32_t)NV && k <= g; ++k)
-            wait(bar(kBarVFull, (g - k) % NV), ((g - k) / NV) & 1, false);
         if (p.sched != nullptr && lane == 0) {
             unsigned long long* ctr = reinterpret_cast<unsigned long long*>(p.sched);
             __threadfence();
@@ -307,6 +298,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atomicExch(ctr + 1, 0ull);
             }
         }
+    } else if (warp == kVWarp) {
+        // ---------------------------------------------------------- V producer
+        // follows the units the K producer publishes; V_j waits only for the
+        // product P_{j-NV} . V_{j-NV} to free its slot
+        uint32_t g = 0, un = 0;
+        const uint32_t box_bytes = (uint32_t)(p.bs < 32 ? p.bs : 32) * 128u;
+        bool ok = true, bad = false;          // bad: warp-uniform
+        for (;;) {
+            const int slot = un & 1;
+            ok = wait(bar(kBarUFull, slot), (un >> 1) & 1, true);
+            if (__any_sync(0xffffffffu, !ok)) break;
+            const int4 e0 = ring[4 * slot], e1 = ring[4 * slot + 1], e2 = ring[4 * slot + 2];
+            __syncwarp();
+            if (lane == 0) umma::mbar_arrive(bar(kBarUEmpty, slot));
+            if (e2.w == 0) break;
+            const int us = e0.x, kvh = e0.y, k0 = e1.x, k1 = e1.y;
+            const int nst = (k1 - k0 + kTok - 1) / kTok;
+            const int bps = kTok / p.bs;
+            const int unit_blocks = (k1 - k0 + p.bs - 1) / p.bs;
+            const int32_t* trow = p.block_tables + (size_t)us * p.MB + k0 / p.bs;
+            auto load_chunk = [&](int c) -> int {
+                const int rb = 32 * c + lane;
+                return rb < unit_blocks ? __ldg(trow + rb) : 0;
+            };
+            int tab = load_chunk(0), tab_next = load_chunk(1), tab_chunk = 0;
+            for (int j = 0; j < nst; ++j, ++g) {
+                const int tn = min(kTok, k1 - (k0 + j * kTok));
+                const int nb = (tn + p.bs - 1) / p.bs;
+                const int idx0 = j * bps;
+                if ((idx0 >> 5) != tab_chunk) {
+                    tab_chunk = idx0 >> 5;
+                    tab = tab_next;
+                    tab_next = load_chunk(tab_chunk + 1);
+                }
+                const int pb = __shfl_sync(0xffffffffu, tab, (idx0 + (lane & (bps - 1))) & 31);
+                const bool bok = lane < nb && pb >= 0 && pb < p.NB;     // reported by the K producer
+                const uint32_t bm = __ballot_sync(0xffffffffu, bok);
+                if (g >= (uint32_t)NV) ok = wait(bar(kBarVEmpty, g % NV), ((g / NV) - 1) & 1, true);
+                if (__any_sync(0xffffffffu, !ok)) {
+                    bad = true;
+                    break;
+                }
+                const int bi = lane / C::kHalves, h = lane % C::kHalves;
+                const int pbb = __shfl_sync(0xffffffffu, pb, bi & 31);
+                const bool live = bi < nb && ((bm >> bi) & 1u);
+                const uint32_t nlive = __popc(__ballot_sync(0xffffffffu, live));
+                const uint32_t full = bar(kBarVFull, g % NV);
+                if (lane == 0) mbar_arrive_expect_tx(full, nlive * box_bytes);
+                __syncwarp();
+                if (live)
+                    tensor_load_2d(vtile(g) + h * (kTok * 128) + bi * p.bs * 128, &vmap, kvh * D + h * 64, pbb * p.bs,
+                                   full);
+            }
+            if (bad) break;
+            ++un;
+        }
+        for (uint32_t k = 1; k <= (uint32_t)NV && k <= g; ++k)
+            wait(bar(kBarVFull, (g - k) % NV), ((g - k) / NV) & 1, false);
     } else if (warp == kQWarp) {
         // ------------------------------------------------------------ Q loader
         uint32_t un = 0;
