@@ -249,26 +249,38 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+KERNEL_SOURCES = {
+    "pkv_decode": ["pkv_decode_tc.cu", "pkv_decode_simt.cu", "pkv_common.cuh", "pkv_tc_common.cuh"],
+    "pkv_prefill": ["pkv_prefill_umma.cu", "pkv_prefill_tc.cu", "pkv_qtile.cuh", "pkv_umma.cuh", "pkv_common.cuh",
+                    "pkv_tc_common.cuh"],
+}
+
+
+def kernel_source_hash(prefix: str = "pkv_decode") -> str:
+    """Hash of the sources a traffic record was taken on: the kernels' files,
+    the headers they include, and the parameter struct they read."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_44_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.startswith("pkv_decode") or f.endswith(".cuh") or f.endswith(".h"):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    for f in KERNEL_SOURCES[prefix]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    with open(os.path.join(csrc, "pkv_internal.h")) as fh:
+        txt = fh.read()
+    i0 = txt.index("struct DecodeParams {")
+    h.update(txt[i0: txt.index("};", i0)].encode())
     return h.hexdigest()[:16]
 
 
-def measured_traffic(workload: str, kernel: str):
-    """DRAM bytes per decode launch from a committed ncu summary, if it was
-    taken on the current kernel sources; else None."""
-    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+def measured_traffic(workload: str, kernel: str, table: str = "decode_traffic.json", prefix: str = "pkv_decode"):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", table)
     try:
         with open(p) as f:
             rec = json.load(f).get(f"{workload}/{kernel}")
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("source_hash") != kernel_source_hash():
+    if not rec or rec.get("source_hash") != kernel_source_hash(prefix):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -647,7 +659,8 @@ def run_prefill(args, w: W.Workload):
                 "frac": round(per_launch_gbs / hbm, 4), "peak_kind": hbm_kind}
         e2e_v = whole_job_gbs(ws, nbytes, e2e_s * 1e3)
     kname = "tcgen05" if args.prefill_kernel == "auto" else args.prefill_kernel
-    roof.update({"traffic": None, "kernel": "paged_attention_prefill (%s)" % kname,
+    roof.update({"traffic": measured_traffic(w.name, kname, "prefill_traffic.json", "pkv_prefill"),
+                 "kernel": "paged_attention_prefill (%s)" % kname,
                  "algorithmic_flops_per_launch": flops,
                  "algorithmic_bytes_per_launch": nbytes, "launch_ms": round(ms_step, 5)})
     line = {
