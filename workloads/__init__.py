@@ -149,9 +149,11 @@ SHAPES: Dict[str, dict] = {
     "fp8-bs32": dict(S=128, Hq=28, Hkv=4, d=128, bs=32, q_dtype=DT_BF16,
                      cache_dtype=DT_E4M3, partition_size=0, seed=5),
     # Several queries per sequence.  Chunked prefill next to decodes
-    # ("LLM推論の基礎とvLLMの内部", section 6): 16 prompts each computing a
-    # 512-token chunk that ends at a multiple of 512 up to 8,192, beside 48
-    # decoding sequences (one query each) -- 8,240 query tokens in one step.
+    # ("LLM推論の基礎とvLLMの内部", section 6: running requests first, then
+    # prompts cut to the rest of the step's token budget, which section 7's
+    # table puts at 16384 tokens on cards with >= 160 GiB): 16 prompts each
+    # computing a 512-token chunk that ends at a multiple of 512 up to 8,192,
+    # beside 48 decoding sequences (one query each) -- 8,240 query tokens.
     "qwen2.5-7b-chunked": dict(S=64, Hq=28, Hkv=4, d=128, bs=16, q_dtype=DT_BF16,
                                cache_dtype=DT_BF16, partition_size=0, seed=6),
     # Speculative verification at long context (same page, section 3: a
