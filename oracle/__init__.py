@@ -22,6 +22,12 @@ What each function computes, and the pages it follows:
   section 4: shared blocks carry a reference count and are copied on write).
 * ``kv_bytes_per_token`` / ``blocks_for_tokens`` -- the size formula of the
   first page, section 2, and ceil(n / block_size).
+* ``paged_attention_prefill`` -- several queries per sequence, causal (first
+  page, sections 3 and 6).
+* ``token_attention_decode`` / ``repack_tokens`` -- decode through a token
+  table and the repacking that moves live tokens ("LLM推論の「見えないメモリ
+  問題」を解く … vToken", token-level virtualisation and asynchronous
+  repacking).
 """
 from __future__ import annotations
 
@@ -82,6 +88,12 @@ def _load():
         lib.oracle_copy_blocks.argtypes = [ctypes.POINTER(c_p), ctypes.POINTER(c_p), c_i, c_p,
                                            c_i, c_i, ctypes.c_size_t]
         lib.oracle_copy_blocks.restype = c_i
+        lib.oracle_token_attention_decode.argtypes = [c_p, c_p, c_i, c_p, c_p, c_i, c_p, c_i, c_p, c_i, c_i, c_i,
+                                                      c_i, c_i, c_i, c_f, c_f, c_f, c_i]
+        lib.oracle_token_attention_decode.restype = c_i
+        lib.oracle_repack_tokens.argtypes = [ctypes.POINTER(c_p), ctypes.POINTER(c_p), c_i, c_p, c_i, c_i, c_p, c_i,
+                                             c_i, c_i, ctypes.c_size_t]
+        lib.oracle_repack_tokens.restype = c_i
         lib.oracle_kv_bytes_per_token.argtypes = [c_i, c_i, c_i, c_i]
         lib.oracle_kv_bytes_per_token.restype = ctypes.c_longlong
         lib.oracle_blocks_for_tokens.argtypes = [ctypes.c_longlong, c_i]
@@ -218,6 +230,51 @@ def copy_blocks(key_caches, value_caches, block_mapping) -> int:
     kp = (ctypes.c_void_p * L)(*[_ptr(a) for a in key_caches])
     vp = (ctypes.c_void_p * L)(*[_ptr(a) for a in value_caches])
     return lib.oracle_copy_blocks(kp, vp, L, _ptr(bm), bm.shape[0], NB, block_bytes)
+
+
+# ------------------------------------------------------------- token table
+
+def token_attention_decode(query, q_dt, key_cache, value_cache, cache_dt, token_slots, num_tokens, scale,
+                           k_scale=1.0, v_scale=1.0, threads=None) -> np.ndarray:
+    """Decode through a token table: token_slots [S, MT] int32 lists each
+    sequence's live tokens in logical order as slots (block * bs + offset);
+    num_tokens [S].  Returns the fp64 output [S, Hq, d]."""
+    lib = _load()
+    query = _check(np.ascontiguousarray(query), q_dt, "query")
+    _check(key_cache, cache_dt, "key_cache")
+    _check(value_cache, cache_dt, "value_cache")
+    ts = np.ascontiguousarray(token_slots, dtype=np.int32)
+    nt = np.ascontiguousarray(num_tokens, dtype=np.int32)
+    S, Hq, d = query.shape
+    NB, bs, Hkv, d2 = key_cache.shape
+    assert d2 == d and ts.shape[0] == S and nt.shape == (S,)
+    out = np.zeros((S, Hq, d), dtype=np.float64)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    rc = lib.oracle_token_attention_decode(_ptr(out), _ptr(query), q_dt, _ptr(key_cache), _ptr(value_cache),
+                                           cache_dt, _ptr(ts), ts.shape[1], _ptr(nt), S, Hq, Hkv, d, bs, NB,
+                                           float(scale), float(k_scale), float(v_scale), int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle token decode failed with code {rc}")
+    return out
+
+
+def repack_tokens(key_caches, value_caches, token_slots, moves) -> int:
+    """Apply moves [M, 4] = (sequence, logical index, src slot, dst slot) in
+    place: every layer's K/V row of the token is copied and the table entry
+    rewritten.  Returns 0, or -1 if a move was skipped."""
+    lib = _load()
+    assert token_slots.dtype == np.int32 and token_slots.flags.c_contiguous
+    L = len(key_caches)
+    mv = np.ascontiguousarray(moves, dtype=np.int64).reshape(-1, 4)
+    NB, bs = key_caches[0].shape[0], key_caches[0].shape[1]
+    token_bytes = key_caches[0][0, 0].nbytes
+    for a in list(key_caches) + list(value_caches):
+        assert a.flags.c_contiguous and a.shape[:2] == (NB, bs)
+    kp = (ctypes.c_void_p * L)(*[_ptr(a) for a in key_caches])
+    vp = (ctypes.c_void_p * L)(*[_ptr(a) for a in value_caches])
+    return lib.oracle_repack_tokens(kp, vp, L, _ptr(token_slots), token_slots.shape[1], token_slots.shape[0],
+                                    _ptr(mv), mv.shape[0], NB, bs, token_bytes)
 
 
 # --------------------------------------------------------- byte accounting

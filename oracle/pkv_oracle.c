@@ -210,6 +210,7 @@ typedef struct {
     const void* q; int q_dt;
     const void* kc; const void* vc; int c_dt;
     const int32_t* block_tables; int MB;
+    const int32_t* token_slots; int MT;     /* if set: gather through the token table instead */
     const int32_t* context_lens; int S;
     int Hq, Hkv, d, bs, NB;
     double scale, k_scale, v_scale;
@@ -229,12 +230,23 @@ static int decode_one(decode_job* J, int s, double* Kc, double* Vc, double* x, d
     int g = J->Hq / J->Hkv;
     int t, h, e, kvh;
     double* out = J->out + (size_t)s * J->Hq * J->d;
-    if (n < 0 || n > J->MB * J->bs)
+    if (n < 0 || (J->token_slots ? n > J->MT : n > J->MB * J->bs))
         return -1;
-    /* gather K/V of every cached token, in logical order */
+    /* gather K/V of every cached token, in logical order: through the block
+     * table (logical block t / bs, offset t % bs), or through the token table
+     * (token t sits in slot token_slots[s][t] = block * bs + offset) */
     for (t = 0; t < n; ++t) {
-        int pb = J->block_tables[(size_t)s * J->MB + t / J->bs];
-        int off = t % J->bs;
+        int pb, off;
+        if (J->token_slots) {
+            int64_t slot = J->token_slots[(size_t)s * J->MT + t];
+            if (slot < 0 || slot >= (int64_t)J->NB * J->bs)
+                return -1;
+            pb = (int)(slot / J->bs);
+            off = (int)(slot % J->bs);
+        } else {
+            pb = J->block_tables[(size_t)s * J->MB + t / J->bs];
+            off = t % J->bs;
+        }
         if (pb < 0 || pb >= J->NB)
             return -1;
         for (kvh = 0; kvh < J->Hkv; ++kvh)
@@ -320,7 +332,7 @@ static int decode_one(decode_job* J, int s, double* Kc, double* Vc, double* x, d
 static void* decode_worker(void* arg)
 {
     decode_job* J = (decode_job*)arg;
-    size_t maxtok = (size_t)J->MB * J->bs;
+    size_t maxtok = J->token_slots ? (size_t)J->MT : (size_t)J->MB * J->bs;
     double* Kc = malloc(sizeof(double) * (maxtok ? maxtok : 1) * J->Hkv * J->d);
     double* Vc = malloc(sizeof(double) * (maxtok ? maxtok : 1) * J->Hkv * J->d);
     double* x = malloc(sizeof(double) * (maxtok ? maxtok : 1));
@@ -357,12 +369,10 @@ static void* decode_worker(void* arg)
  * per-partition (max, sum, weighted sum) triples and their merge.  Runs
  * `threads` POSIX threads over sequences.  Returns 0, -1 on an
  * out-of-range block id or length, -2 on allocation failure. */
-int oracle_paged_attention_decode(double* out, const void* q, int q_dt,
-                                  const void* key_cache, const void* value_cache,
-                                  int cache_dt, const int32_t* block_tables, int MB,
-                                  const int32_t* context_lens, int S, int Hq, int Hkv,
-                                  int d, int bs, int NB, float scale, float k_scale,
-                                  float v_scale, int partition, int threads)
+static int run_decode(double* out, const void* q, int q_dt, const void* key_cache, const void* value_cache,
+                      int cache_dt, const int32_t* block_tables, int MB, const int32_t* token_slots, int MT,
+                      const int32_t* context_lens, int S, int Hq, int Hkv, int d, int bs, int NB, float scale,
+                      float k_scale, float v_scale, int partition, int threads)
 {
     decode_job J;
     pthread_t* tid;
@@ -371,7 +381,8 @@ int oracle_paged_attention_decode(double* out, const void* q, int q_dt,
         return -1;
     memset(&J, 0, sizeof J);
     J.q = q; J.q_dt = q_dt; J.kc = key_cache; J.vc = value_cache; J.c_dt = cache_dt;
-    J.block_tables = block_tables; J.MB = MB; J.context_lens = context_lens; J.S = S;
+    J.block_tables = block_tables; J.MB = MB; J.token_slots = token_slots; J.MT = MT;
+    J.context_lens = context_lens; J.S = S;
     J.Hq = Hq; J.Hkv = Hkv; J.d = d; J.bs = bs; J.NB = NB;
     J.scale = (double)scale;
     J.k_scale = cache_dt == OR_E4M3 ? (double)k_scale : 1.0;
@@ -390,6 +401,17 @@ int oracle_paged_attention_decode(double* out, const void* q, int q_dt,
     free(tid);
     pthread_mutex_destroy(&J.mu);
     return J.status;
+}
+
+int oracle_paged_attention_decode(double* out, const void* q, int q_dt,
+                                  const void* key_cache, const void* value_cache,
+                                  int cache_dt, const int32_t* block_tables, int MB,
+                                  const int32_t* context_lens, int S, int Hq, int Hkv,
+                                  int d, int bs, int NB, float scale, float k_scale,
+                                  float v_scale, int partition, int threads)
+{
+    return run_decode(out, q, q_dt, key_cache, value_cache, cache_dt, block_tables, MB, NULL, 0, context_lens, S,
+                      Hq, Hkv, d, bs, NB, scale, k_scale, v_scale, partition, threads);
 }
 
 /* ---------------------------------------------------------------- prefill */
@@ -548,6 +570,57 @@ int oracle_copy_blocks(void* const* key_caches, void* const* value_caches, int n
             memcpy((char*)value_caches[l] + dst * block_bytes,
                    (const char*)value_caches[l] + src * block_bytes, block_bytes);
         }
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------ token table */
+
+/*
+ * Decode attention through a token table ("LLM推論の「見えないメモリ問題」を
+ * 解く … vToken", section on token-level virtualisation): the table maps each
+ * live token, in the sequence's logical order, to its physical slot
+ * block * bs + offset; deleted tokens are simply absent.  The result is the
+ * textbook softmax attention over the live tokens, as in the decode above.
+ * token_slots [S, MT]; num_tokens [S] live tokens per sequence.
+ */
+int oracle_token_attention_decode(double* out, const void* q, int q_dt, const void* key_cache,
+                                  const void* value_cache, int cache_dt, const int32_t* token_slots, int MT,
+                                  const int32_t* num_tokens, int S, int Hq, int Hkv, int d, int bs, int NB,
+                                  float scale, float k_scale, float v_scale, int threads)
+{
+    return run_decode(out, q, q_dt, key_cache, value_cache, cache_dt, NULL, 0, token_slots, MT, num_tokens, S,
+                      Hq, Hkv, d, bs, NB, scale, k_scale, v_scale, 0, threads);
+}
+
+/*
+ * Repacking (same page, "非同期リパッキング"): live tokens move to free slots
+ * of other blocks so that emptied blocks can be released; the token table
+ * entry of each moved token is rewritten, and the logical order is kept.
+ * moves [M, 4] = (sequence, logical index, source slot, destination slot);
+ * a move applies only if its indices are in range and the table holds the
+ * source slot at that position.  Every layer's K and V row of the token
+ * (token_bytes bytes each) is copied.  Returns -1 if any move was skipped.
+ */
+int oracle_repack_tokens(void* const* key_caches, void* const* value_caches, int num_layers, int32_t* token_slots,
+                         int MT, int S, const int64_t* moves, int M, int NB, int bs, size_t token_bytes)
+{
+    int i, l, bad = 0;
+    const int64_t slots = (int64_t)NB * bs;
+    for (i = 0; i < M; ++i) {
+        int64_t seq = moves[4 * i], idx = moves[4 * i + 1], src = moves[4 * i + 2], dst = moves[4 * i + 3];
+        if (seq < 0 || seq >= S || idx < 0 || idx >= MT || src < 0 || src >= slots || dst < 0 || dst >= slots ||
+            token_slots[seq * MT + idx] != src) {
+            bad = 1;
+            continue;
+        }
+        for (l = 0; l < num_layers; ++l) {
+            memcpy((char*)key_caches[l] + dst * token_bytes, (const char*)key_caches[l] + src * token_bytes,
+                   token_bytes);
+            memcpy((char*)value_caches[l] + dst * token_bytes, (const char*)value_caches[l] + src * token_bytes,
+                   token_bytes);
+        }
+        token_slots[seq * MT + idx] = (int32_t)dst;
+    }
     return bad ? -1 : 0;
 }
 

@@ -31,6 +31,13 @@ MUTANTS = {
     "prefill-causal-excludes-self": ("for (t = 0; t <= pos; ++t) {\n                double acc = 0.0;",
                                      "for (t = 0; t < pos; ++t) {\n                double acc = 0.0;"),
     "prefill-positions-from-start": ("int pos = n - ql + i;", "int pos = i;"),
+    "token-slot-split-swapped": ("pb = (int)(slot / J->bs);\n            off = (int)(slot % J->bs);",
+                                 "pb = (int)(slot % J->bs);\n            off = (int)(slot / J->bs);"),
+    "repack-table-not-rewritten": ("        token_slots[seq * MT + idx] = (int32_t)dst;\n", ""),
+    "repack-values-not-moved": ("            memcpy((char*)value_caches[l] + dst * token_bytes, "
+                                "(const char*)value_caches[l] + src * token_bytes,\n                   token_bytes);\n",
+                                ""),
+    "repack-no-stale-check": (" ||\n            token_slots[seq * MT + idx] != src) {", ") {"),
     "softmax-sum-skips-last": ("for (t = 0; t < n; ++t) {\n                double p = exp(x[t] - m);",
                                "for (t = 0; t < n; ++t) {\n                double p = t + 1 < n ? exp(x[t] - m) : 0.0;"),
 }
@@ -99,3 +106,29 @@ def test_pool_pins_catch_mutant(tmp_path, name):
         m.add_sequence(0, a)
         caught = m.add_sequence(1, b) != 16 or m.ref[m.block_table(0)[0]] != 2 or len(m.block_table(0)) != 3
     assert caught, f"pool mutant {name} survived the pins"
+
+
+# ---- the repacking planner model (oracle/vtoken_plan.py)
+
+PLAN_MUTANTS = {
+    "keep-sparsest": ("key=lambda b: (-count[b], b)", "key=lambda b: (count[b], b)"),
+    "holes-from-the-top": ("for b in sorted(keep) for o in range(bs)", "for b in sorted(keep, reverse=True) for o in range(bs)"),
+    "shared-blocks-movable": ("if len(users[sl // bs]) == 1", "if len(users[sl // bs]) >= 1"),
+    "one-block-too-few": ("k = -(-sum(count.values()) // bs)", "k = max(1, sum(count.values()) // bs)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PLAN_MUTANTS))
+def test_plan_pins_catch_mutant(tmp_path, name):
+    import importlib.util
+    from tests.test_vtoken_plan import model_pins
+    old, new = PLAN_MUTANTS[name]
+    src = open(os.path.join(ROOT, "oracle", "vtoken_plan.py"), encoding="utf-8").read()
+    assert src.count(old) == 1, name
+    path = tmp_path / "vtoken_plan_mutant.py"
+    path.write_text(src.replace(old, new), encoding="utf-8")
+    spec = importlib.util.spec_from_file_location("vtoken_plan_mutant", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    with pytest.raises(Exception):
+        model_pins(mod)

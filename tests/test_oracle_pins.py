@@ -438,3 +438,145 @@ def test_prefill_one_query_is_decode(oracle):
     dec = oracle.paged_attention_decode(q, oracle.F32, kp, vp, oracle.F32, tabs, cl, 0.125)
     pre = oracle.paged_attention_prefill(q, oracle.F32, kp, vp, oracle.F32, tabs, cl, np.arange(4), 0.125)
     np.testing.assert_array_equal(dec, pre)
+
+
+# ------------------------------------------------------------ token table
+
+def _token_case(rng, lens, keep_frac, Hq, Hkv, d, bs):
+    """A block-table case whose tokens a deletion policy then thins out at
+    random: the token table lists the survivors' slots in logical order."""
+    q, kp, vp, tabs, cl, kctx, vctx = _scatter_case(rng, lens, Hq, Hkv, d, bs)
+    MT = max(max(lens), 1)
+    slots = np.zeros((len(lens), MT), np.int32)
+    nt = np.zeros(len(lens), np.int32)
+    lk, lv = [], []
+    for s, n in enumerate(lens):
+        keep = rng.random(n) < keep_frac
+        if n and not keep.any():
+            keep[rng.integers(0, n)] = True
+        idx = np.nonzero(keep)[0]
+        slots[s, : idx.size] = [tabs[s, t // bs] * bs + t % bs for t in idx]
+        nt[s] = idx.size
+        lk.append(kctx[s][idx])
+        lv.append(vctx[s][idx])
+    return q, kp, vp, tabs, cl, slots, nt, lk, lv
+
+
+@pytest.mark.parametrize("cache", ["f32", "bf16", "e4m3"])
+def test_token_table_of_all_tokens_is_the_block_table(oracle, cache):
+    """A token table that lists every token's slot in order gathers exactly
+    what the block table gathers: identical outputs."""
+    rng = np.random.default_rng(301)
+    bs = 16
+    q, kp, vp, tabs, cl, _, _ = _scatter_case(rng, [1, 16, 17, 45, 64], 8, 2, 64, bs)
+    MT = int(cl.max())
+    slots = np.zeros((len(cl), MT), np.int32)
+    for s, n in enumerate(cl):
+        slots[s, :n] = [tabs[s, t // bs] * bs + t % bs for t in range(n)]
+    if cache == "f32":
+        kc, vc, dt, ks = kp, vp, oracle.F32, 1.0
+    elif cache == "bf16":
+        kc, vc, dt, ks = W.bf16_bits(kp), W.bf16_bits(vp), oracle.BF16, 1.0
+    else:
+        ks = W.e4m3_scale(kp)
+        kc, vc, dt = oracle.e4m3_from_float32(kp / np.float32(ks)), oracle.e4m3_from_float32(vp / np.float32(ks)), oracle.E4M3
+    a = oracle.paged_attention_decode(q, oracle.F32, kc, vc, dt, tabs, cl, 0.125, ks, ks)
+    b = oracle.token_attention_decode(q, oracle.F32, kc, vc, dt, slots, cl, 0.125, ks, ks)
+    np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (8, 1), (6, 6)])
+def test_token_decode_after_deletion_brute_force(oracle, Hq, Hkv):
+    """Deleted tokens are absent from the table: the result is attention over
+    the survivors (torch fp64 SDPA on their gathered K/V)."""
+    rng = np.random.default_rng(302 + Hq)
+    d, bs = 64, 16
+    q, kp, vp, _, _, slots, nt, lk, lv = _token_case(rng, [1, 16, 40, 70, 33], 0.4, Hq, Hkv, d, bs)
+    out = oracle.token_attention_decode(q, oracle.F32, kp, vp, oracle.F32, slots, nt, 0.125)
+    g = Hq // Hkv
+    for s in range(len(nt)):
+        qt = torch.from_numpy(q[s].astype(np.float64))[:, None, :]                 # [Hq, 1, d]
+        kt = torch.from_numpy(lk[s].astype(np.float64)).permute(1, 0, 2).repeat_interleave(g, dim=0)
+        vt = torch.from_numpy(lv[s].astype(np.float64)).permute(1, 0, 2).repeat_interleave(g, dim=0)
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=0.125)[:, 0].numpy()
+        np.testing.assert_allclose(out[s], ref, atol=1e-12, rtol=0)
+
+
+def test_token_decode_logical_order_does_not_change_attention(oracle):
+    rng = np.random.default_rng(303)
+    q, kp, vp, _, _, slots, nt, _, _ = _token_case(rng, [50, 90], 0.7, 8, 2, 64, 16)
+    out = oracle.token_attention_decode(q, oracle.F32, kp, vp, oracle.F32, slots, nt, 0.125)
+    sh = slots.copy()
+    for s in range(len(nt)):
+        sh[s, : nt[s]] = rng.permutation(slots[s, : nt[s]])
+    out2 = oracle.token_attention_decode(q, oracle.F32, kp, vp, oracle.F32, sh, nt, 0.125)
+    np.testing.assert_allclose(out, out2, atol=1e-12, rtol=0)
+
+
+def _scrub_blocks(pools, blocks, bs):
+    """A released block's slots are reused: overwrite them."""
+    for a in pools:
+        for b in blocks:
+            a[b] = np.float32(1e30)
+
+
+def test_repack_keeps_attention_and_releases_blocks(oracle):
+    """Plan (oracle/vtoken_plan.py), move the rows, rewrite the table, then
+    overwrite every released block: attention is bit-identical to before, each
+    sequence's live tokens fill ceil(n / bs) blocks, and no live token is in a
+    released block."""
+    from oracle.vtoken_plan import plan, apply
+    rng = np.random.default_rng(304)
+    bs = 16
+    q, kp, vp, _, _, slots, nt, _, _ = _token_case(rng, [100, 40, 260, 16, 77], 0.3, 8, 2, 64, bs)
+    NB = kp.shape[0]
+    before = oracle.token_attention_decode(q, oracle.F32, kp, vp, oracle.F32, slots, nt, 0.125)
+    moves, freed = plan(slots, nt, bs, NB)
+    assert moves and freed
+    kc2, vc2, sl2 = kp.copy(), vp.copy(), slots.copy()
+    assert oracle.repack_tokens([kc2], [vc2], sl2, np.array(moves)) == 0
+    np.testing.assert_array_equal(sl2, apply(slots, moves))
+    for s, t, src, dst in moves:
+        np.testing.assert_array_equal(kc2[dst // bs, dst % bs], kp[src // bs, src % bs])
+        np.testing.assert_array_equal(vc2[dst // bs, dst % bs], vp[src // bs, src % bs])
+    _scrub_blocks([kc2, vc2], freed, bs)
+    after = oracle.token_attention_decode(q, oracle.F32, kc2, vc2, oracle.F32, sl2, nt, 0.125)
+    np.testing.assert_array_equal(before, after)
+    for s in range(len(nt)):
+        blocks = {int(x) // bs for x in sl2[s, : nt[s]]}
+        assert len(blocks) == -(-int(nt[s]) // bs)
+        assert not blocks & set(freed)
+    live = [int(x) for s in range(len(nt)) for x in sl2[s, : nt[s]]]
+    assert len(live) == len(set(live))
+
+
+def test_repack_pages_example(oracle):
+    from oracle.vtoken_plan import plan
+    rows = [ln.split() for ln in open(os.path.join(GOLDEN, "vtoken_repack_example.txt"), encoding="utf-8")
+            if ln.strip() and not ln.startswith("#")]
+    kv = {r[0]: r[1:] for r in rows if r[0] in ("bs", "NB", "slots", "freed")}
+    bs, NB = int(kv["bs"][0]), int(kv["NB"][0])
+    slots = np.array([[int(x) for x in kv["slots"]]], np.int32)
+    want_moves = [tuple(int(x) for x in r[1:]) for r in rows if r[0] == "move"]
+    moves, freed = plan(slots, np.array([slots.shape[1]]), bs, NB)
+    assert moves == want_moves and freed == [int(x) for x in kv["freed"]]
+    # the oracle's repack applies them
+    kp = np.random.default_rng(5).standard_normal((NB, bs, 1, 8)).astype(np.float32)
+    vp = kp + 1
+    k2, v2, s2 = kp.copy(), vp.copy(), slots.copy()
+    assert oracle.repack_tokens([k2], [v2], s2, np.array(moves)) == 0
+    assert list(s2[0, 12:]) == [28, 29, 30, 31]
+    np.testing.assert_array_equal(k2[1, 12:], kp[2, [0, 5, 10, 15]])
+    np.testing.assert_array_equal(v2[1, 12:], vp[2, [0, 5, 10, 15]])
+
+
+def test_repack_rejects_a_stale_move(oracle):
+    """A move whose source is no longer in the table is skipped and reported."""
+    rng = np.random.default_rng(305)
+    kp = rng.standard_normal((4, 16, 1, 8)).astype(np.float32)
+    vp = kp.copy()
+    slots = np.array([[0, 1, 2]], np.int32)
+    k2 = kp.copy()
+    assert oracle.repack_tokens([k2], [vp.copy()], slots, np.array([[0, 1, 5, 40]])) == -1
+    assert list(slots[0]) == [0, 1, 2]
+    np.testing.assert_array_equal(k2, kp)
