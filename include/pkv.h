@@ -68,11 +68,13 @@ enum {
     PKV_DEVERR_NONE = 0,
     PKV_DEVERR_BLOCK_ID = 1,      /* a block table entry outside [0, NB) */
     PKV_DEVERR_CONTEXT_LEN = 2,   /* context_lens[s] < 0 or > max_context_len (clamped) */
-    PKV_DEVERR_SLOT = 3,          /* slot_mapping[i] >= NB * bs */
+    PKV_DEVERR_SLOT = 3,          /* slot_mapping[i] >= NB * bs, or a token-table slot outside [0, NB * bs) */
     PKV_DEVERR_COPY_PAIR = 4,     /* a copy pair with an id outside [0, NB) */
     PKV_DEVERR_TIMEOUT = 5,       /* a staged copy did not land within ~2 s; the kernel gave up */
-    PKV_DEVERR_QUERY_LEN = 6      /* prefill: a sequence's queries are < 0, more than its length or
+    PKV_DEVERR_QUERY_LEN = 6,     /* prefill: a sequence's queries are < 0, more than its length or
                                      than max_query_len, or outside [0, T) (the sequence is skipped) */
+    PKV_DEVERR_MOVE = 7           /* repack: a move out of range, or whose source is not the slot the
+                                     token table holds (the move is skipped) */
 };
 
 /*
@@ -325,6 +327,79 @@ PKV_API pkv_status pkv_paged_attention_prefill_ex(void* out, const void* query, 
                                                   float scale, int partition_size,
                                                   void* workspace, size_t workspace_bytes,
                                                   int32_t* err_word, pkv_stream_t stream, int kernel);
+
+/* ------------------------------------------------------------------------
+ * Token tables and repacking.
+ *
+ * Source: "LLM推論の「見えないメモリ問題」を解く：トークンレベル仮想化でKV
+ * キャッシュを再利用可能にする「vToken」", sections on token-level
+ * virtualisation and asynchronous repacking: a token table maps each live
+ * token of a sequence, in logical order, to its physical slot; a deletion
+ * policy removes tokens from the table; repacking moves the survivors of
+ * sparse blocks to free slots of other blocks, rewrites their table entries
+ * and releases the emptied blocks.  Attention reads through the table, so
+ * the cache pools and captured CUDA graphs are untouched by repacking.
+ *
+ * A slot is block * bs + offset, i.e. the row of the cache seen as
+ * [NB * bs, Hkv, d].
+ * ------------------------------------------------------------------------ */
+
+/*
+ * token_attention_decode -- the decode of pkv_paged_attention_decode, with
+ * each sequence's K/V reached through its token table instead of a block
+ * table: token_slots [S, MT] int32 (device) lists the slots of the
+ * sequence's live tokens in logical order; num_tokens [S] (device) how many;
+ * max_tokens >= every num_tokens (host value; <= MT).  Output, scales,
+ * partitioning and workspace are those of the decode
+ * (pkv_decode_workspace_size(S, Hq, d, max_tokens, partition_size)).
+ * Supported: the tensor-core decode's dtypes (bf16 query and cache, or an
+ * E4M3 cache with a bf16 or fp32 query), d in {64, 128}, bs in {16, 32};
+ * anything else returns PKV_ERR_UNSUPPORTED.  A slot outside the pool is
+ * treated as an absent token and reported (PKV_DEVERR_SLOT).
+ */
+PKV_API pkv_status pkv_token_attention_decode(void* out, const void* query, pkv_dtype q_dtype,
+                                              const void* key_cache, const void* value_cache,
+                                              pkv_dtype cache_dtype,
+                                              const int32_t* token_slots, int MT,
+                                              const int32_t* num_tokens, int S, int max_tokens,
+                                              int Hq, int Hkv, int d, int bs, int NB,
+                                              float scale, float k_scale, float v_scale,
+                                              int partition_size,
+                                              void* workspace, size_t workspace_bytes,
+                                              int32_t* err_word, pkv_stream_t stream);
+
+/*
+ * repack_tokens -- apply moves [M, 4] int64 (device) = (sequence, logical
+ * index, source slot, destination slot): for every layer, the token's K and
+ * V rows (token_bytes = Hkv * d * element size bytes each) are copied from
+ * the source slot to the destination, then token_slots[sequence][index]
+ * becomes the destination.  key_caches / value_caches are host arrays of
+ * num_layers (<= 256) device pointers.  Preconditions: destinations are free
+ * slots, distinct, and no move's destination is another move's source; each
+ * (sequence, index) appears once.  A move out of range or whose source is
+ * not what the table holds is skipped and reported (PKV_DEVERR_MOVE).
+ */
+PKV_API pkv_status pkv_repack_tokens(void* const* key_caches, void* const* value_caches, int num_layers,
+                                     int32_t* token_slots, int MT, int S, const int64_t* moves, int M,
+                                     int NB, int bs, size_t token_bytes, int32_t* err_word,
+                                     pkv_stream_t stream);
+
+/*
+ * vtoken_plan -- host planner for repacking (host arrays).  Per sequence,
+ * over the blocks only that sequence uses (a block several sequences
+ * reference is left alone): the sequence needs k = ceil(live tokens in
+ * those blocks / bs) blocks; the k with the most live tokens stay (lower id
+ * first on ties); its tokens in the others move, in logical order, to the
+ * free slots of the kept blocks, lowest slot first; the others are then
+ * empty and are listed in `freed` (ascending per sequence).  Writes up to
+ * max_moves moves [.., 4] and max_freed block ids, and the counts needed in
+ * *num_moves / *num_freed.  Returns PKV_ERR_INVALID_ARG for a slot outside
+ * the pool or a sequence holding one slot twice, PKV_ERR_WORKSPACE when an
+ * output array is too small (counts still set, arrays untouched).
+ */
+PKV_API pkv_status pkv_vtoken_plan(const int32_t* token_slots, int MT, const int32_t* num_tokens, int S, int bs,
+                                   int NB, int64_t* moves, int64_t max_moves, int64_t* num_moves,
+                                   int32_t* freed, int64_t max_freed, int64_t* num_freed);
 
 /* ------------------------------------------------------------------------
  * Host block manager: the bookkeeping that produces the block tables, slot

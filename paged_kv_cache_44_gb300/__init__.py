@@ -21,6 +21,7 @@ import math
 import os
 from typing import Optional, Sequence
 
+import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -39,7 +40,8 @@ EXPORTED = ("pkv_paged_kv_write", "pkv_decode_workspace_size", "pkv_decode_parti
             "pkv_pool_num_cached_blocks", "pkv_pool_block_ref_count", "pkv_pool_add_sequence",
             "pkv_pool_append_token", "pkv_pool_fork", "pkv_pool_free_sequence", "pkv_pool_block_table",
             "pkv_pool_append_tokens", "pkv_pool_block_tables", "pkv_prefill_workspace_size",
-            "pkv_paged_attention_prefill", "pkv_paged_attention_prefill_ex")
+            "pkv_paged_attention_prefill", "pkv_paged_attention_prefill_ex", "pkv_token_attention_decode",
+            "pkv_repack_tokens", "pkv_vtoken_plan")
 STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -107,6 +109,13 @@ def _load() -> ctypes.CDLL:
     lib.pkv_paged_attention_prefill.restype = i32
     lib.pkv_paged_attention_prefill_ex.argtypes = lib.pkv_paged_attention_prefill.argtypes + [i32]
     lib.pkv_paged_attention_prefill_ex.restype = i32
+    lib.pkv_token_attention_decode.argtypes = dec
+    lib.pkv_token_attention_decode.restype = i32
+    lib.pkv_repack_tokens.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32, vp, i32, i32, vp, i32, i32, i32,
+                                      sz, vp, vp]
+    lib.pkv_repack_tokens.restype = i32
+    lib.pkv_vtoken_plan.argtypes = [pi32, i32, pi32, i32, i32, i32, pi64, i64, pi64, pi32, i64, pi64]
+    lib.pkv_vtoken_plan.restype = i32
     lib.pkv_status_string.argtypes = [i32]
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_version.argtypes = []
@@ -299,6 +308,71 @@ def copy_blocks(key_caches: Sequence[torch.Tensor], value_caches: Sequence[torch
     vp = (ctypes.c_void_p * L)(*[_ptr(t) for t in value_caches])
     _check("copy_blocks", lib.pkv_copy_blocks(kp, vp, L, _ptr(block_mapping), P, NB, block_bytes,
                                               _ptr(err_word), _stream(stream)))
+
+
+def token_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                           value_cache: torch.Tensor, token_slots: torch.Tensor, num_tokens: torch.Tensor,
+                           max_tokens: int, scale: Optional[float] = None, k_scale: float = 1.0, v_scale: float = 1.0,
+                           partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
+                           err_word: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode through a token table: token_slots int32 [S, MT] lists each
+    sequence's live tokens as slots (block * bs + offset) in logical order;
+    num_tokens int32 [S]; max_tokens (host) >= every count."""
+    S, Hq, d = query.shape
+    NB, bs, Hkv, d2 = key_cache.shape
+    if d2 != d or out.shape != query.shape or out.dtype != query.dtype or value_cache.shape != key_cache.shape:
+        raise ValueError("shape or dtype mismatch")
+    if token_slots.dtype != torch.int32 or num_tokens.dtype != torch.int32 or token_slots.dim() != 2:
+        raise ValueError("token_slots and num_tokens must be int32")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
+    _check("token_attention_decode", lib.pkv_token_attention_decode(
+        _ptr(out), _ptr(query), dtype_code(query.dtype), _ptr(key_cache), _ptr(value_cache),
+        dtype_code(key_cache.dtype), _ptr(token_slots), token_slots.shape[1], _ptr(num_tokens), S,
+        int(max_tokens), Hq, Hkv, d, bs, NB, float(scale), float(k_scale), float(v_scale), int(partition_size),
+        ws_ptr, ws_bytes, _ptr(err_word), _stream(stream)))
+    return out
+
+
+def repack_tokens(key_caches: Sequence[torch.Tensor], value_caches: Sequence[torch.Tensor],
+                  token_slots: torch.Tensor, moves: torch.Tensor, err_word: Optional[torch.Tensor] = None,
+                  stream=None) -> None:
+    """Move live tokens: moves int64 [M, 4] = (sequence, logical index, src
+    slot, dst slot); every layer's K/V row is copied and token_slots (int32
+    [S, MT], device) rewritten."""
+    L = len(key_caches)
+    if len(value_caches) != L or L == 0:
+        raise ValueError("need the same, non-zero number of key and value caches")
+    NB, bs = key_caches[0].shape[0], key_caches[0].shape[1]
+    token_bytes = key_caches[0][0, 0].numel() * key_caches[0].element_size()
+    for t in list(key_caches) + list(value_caches):
+        if t.shape != key_caches[0].shape or t.dtype != key_caches[0].dtype:
+            raise ValueError("all caches must share shape and dtype")
+    if moves.dtype != torch.int64 or token_slots.dtype != torch.int32 or token_slots.dim() != 2:
+        raise ValueError("moves must be int64 [M, 4], token_slots int32 [S, MT]")
+    kp = (ctypes.c_void_p * L)(*[_ptr(t) for t in key_caches])
+    vp = (ctypes.c_void_p * L)(*[_ptr(t) for t in value_caches])
+    _check("repack_tokens", lib.pkv_repack_tokens(kp, vp, L, _ptr(token_slots), token_slots.shape[1],
+                                                  token_slots.shape[0], _ptr(moves), moves.numel() // 4, NB, bs,
+                                                  token_bytes, _ptr(err_word), _stream(stream)))
+
+
+def vtoken_plan(token_slots: np.ndarray, num_tokens: np.ndarray, block_size: int, num_blocks: int):
+    """Host repacking plan (pkv_vtoken_plan): returns (moves int64 [M, 4],
+    freed int32 [F]) for host token tables."""
+    ts = np.ascontiguousarray(token_slots, dtype=np.int32)
+    nt = np.ascontiguousarray(num_tokens, dtype=np.int32)
+    S, MT = ts.shape
+    nm, nf = ctypes.c_int64(0), ctypes.c_int64(0)
+    cap_m, cap_f = max(int(nt.sum()), 1), max(num_blocks, 1)
+    moves = np.zeros((cap_m, 4), np.int64)
+    freed = np.zeros(cap_f, np.int32)
+    as32 = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))  # noqa: E731
+    as64 = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))  # noqa: E731
+    _check("vtoken_plan", lib.pkv_vtoken_plan(as32(ts), MT, as32(nt), S, block_size, num_blocks, as64(moves), cap_m,
+                                              ctypes.byref(nm), as32(freed), cap_f, ctypes.byref(nf)))
+    return moves[: nm.value].copy(), freed[: nf.value].copy()
 
 
 class BlockPool:

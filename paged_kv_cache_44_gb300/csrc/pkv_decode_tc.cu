@@ -32,6 +32,17 @@
 //
 // A unit that covers its whole sequence writes `out`; otherwise it writes
 // (m, l, unnormalised O) to the workspace for the merge kernel.
+//
+// Through a token table (TT): "LLM推論の「見えないメモリ問題」を解く … vToken",
+// token-level virtualisation: each live token of a sequence, in logical
+// order, names its own slot (block * bs + offset), so a stage's 32 tokens
+// may come from anywhere in the pool.  The issue side then copies each
+// token's row with 16-byte cp.async requests (eight lanes per 128-byte line)
+// straight into the same swizzled stage layout, and the stage's mbarrier
+// counts one arrival per lane when its copies land; the math is unchanged.
+// (A tensor copy that gathers rows could write only whole 1024-byte swizzle
+// atoms, which four 128-byte rows do not fill.)
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math_constants.h>
@@ -165,7 +176,7 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, size_t idx, flo
 
 // ------------------------------------------------------------------ kernel
 
-template <int D, bool FP8, typename QF>
+template <int D, bool FP8, typename QF, bool TT>
 __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
     decode_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, unsigned long long total_units,
@@ -192,7 +203,8 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
     auto lds64 = [&](uint32_t a) { return *reinterpret_cast<const uint2*>(ws + (a - ws_addr)); };
 
     if (lane == 0) {
-        for (int i = 0; i < C::kStages; ++i) mbar_init(bar(i), 1);
+        // through a token table every lane's copies arrive on the stage barrier, and lane 0 once more
+        for (int i = 0; i < C::kStages; ++i) mbar_init(bar(i), TT ? 33 : 1);
         fence_barrier_init();
     }
     __syncwarp();
@@ -264,10 +276,12 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
             i_have = true;
             i_stage = 0;
             i_nst = (iu.t1 - iu.t0 + kTok - 1) / kTok;
-            tab_blocks = (iu.t1 - iu.t0 + p.bs - 1) / p.bs;
-            tab_chunk = 0;
-            tab = load_chunk(0);
-            tab_next = load_chunk(1);
+            if constexpr (!TT) {
+                tab_blocks = (iu.t1 - iu.t0 + p.bs - 1) / p.bs;
+                tab_chunk = 0;
+                tab = load_chunk(0);
+                tab_next = load_chunk(1);
+            }
         }
         // the unit's query rows ride on its first stage
         const uint32_t q_bytes = i_stage == 0 ? (uint32_t)(iu.nh * D * QF::bytes) : 0u;
@@ -275,6 +289,46 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
         const int ts = iu.t0 + i_stage * kTok;
         const int tn = min(kTok, iu.t1 - ts);
         const int rs = i_stage * kTok;                         // token offset of the stage in the unit
+        if constexpr (TT) {
+            // lane i: the slot of token ts + i; -1 when past the unit or out of the pool
+            int tslot = -1;
+            if (lane < tn) {
+                tslot = __ldg(p.token_slots + (size_t)iu.s * p.MT + ts + lane);
+                if (tslot < 0 || (long long)tslot >= (long long)p.NB * p.bs) {
+                    report(p.err, PKV_DEVERR_SLOT);
+                    tslot = -1;
+                }
+            }
+            const uint32_t m = __ballot_sync(0xffffffffu, tslot >= 0);
+            // lanes cover token rows 16 bytes each: CPR lanes per row, 32 / CPR rows per request
+            constexpr int CPR = C::kRowBytes / 16;
+            constexpr int TPI = 32 / CPR;
+            const int j = lane % CPR;
+            const unsigned char* kcb = static_cast<const unsigned char*>(p.kc);
+            const unsigned char* vcb = static_cast<const unsigned char*>(p.vc);
+#pragma unroll 4
+            for (int t0 = 0; t0 < kTok; t0 += TPI) {
+                const int t = t0 + lane / CPR;
+                const int sl = __shfl_sync(0xffffffffu, tslot, t);
+                if (sl >= 0) {
+                    const size_t row = ((size_t)sl * p.Hkv + iu.kvh) * C::kRowBytes + 16 * j;
+                    cp_async16(swz<C::kRowBytes, kTok>(stage_k(slot), t, 16 * j), kcb + row);
+                    cp_async16(swz<C::kRowBytes, kTok>(stage_v(slot), t, 16 * j), vcb + row);
+                }
+            }
+            cp_async_mbar_arrive_noinc(bar(slot));
+            if (lane == 0) {
+                masks[slot] = m;
+                mbar_arrive_expect_tx(bar(slot), q_bytes);
+                if (q_bytes)
+                    bulk_load(ws_addr + C::kQOff + i_qslot * C::kQSlotBytes,
+                              static_cast<const unsigned char*>(p.q) + ((size_t)iu.s * p.Hq + iu.h0) * D * QF::bytes,
+                              q_bytes, bar(slot));
+            }
+            ++g_issue;
+            ++i_stage;
+            return true;
+        }
         if (rs / p.bs / 32 != tab_chunk) {                     // the stage's blocks start a new chunk
             ++tab_chunk;
             tab = tab_next;
@@ -590,6 +644,9 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
         }
     }
 
+    // copies of this lane still in flight land before the warp leaves
+    if constexpr (TT) asm volatile("cp.async.wait_all;" ::: "memory");
+
     // ---- leave the scheduling counters at zero for the next launch
     if (p.sched != nullptr && lane == 0) {
         unsigned long long* ctr = reinterpret_cast<unsigned long long*>(p.sched);
@@ -638,10 +695,10 @@ bool encode_cache_map(CUtensorMap* map, const void* base, const DecodeParams& p)
     return rc == CUDA_SUCCESS;
 }
 
-template <int D, bool FP8, typename QF>
+template <int D, bool FP8, typename QF, bool TT>
 cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t st) {
     using C = Cfg<D, FP8, QF::bytes>;
-    auto kern = decode_tc_kernel<D, FP8, QF>;
+    auto kern = decode_tc_kernel<D, FP8, QF, TT>;
     // the shared-memory opt-in is per device: remember it per device ordinal
     static bool configured[64] = {false};
     int dev = 0;
@@ -675,14 +732,20 @@ bool decode_tc_supports(pkv_dtype q_dt, pkv_dtype c_dt, int d, int bs, int NB) {
     return c_dt == PKV_FP8_E4M3 && (q_dt == PKV_BF16 || q_dt == PKV_F32);
 }
 
-cudaError_t launch_decode_tc(const DecodeParams& p, pkv_dtype q_dt, pkv_dtype c_dt, int num_sms, cudaStream_t st) {
-    if (p.S == 0) return cudaSuccess;
-    if (c_dt == PKV_BF16) {
-        return p.d == 64 ? launch_one<64, false, BF16>(p, num_sms, st) : launch_one<128, false, BF16>(p, num_sms, st);
-    }
+template <bool TT>
+cudaError_t launch_tc(const DecodeParams& p, pkv_dtype q_dt, pkv_dtype c_dt, int num_sms, cudaStream_t st) {
+    if (c_dt == PKV_BF16)
+        return p.d == 64 ? launch_one<64, false, BF16, TT>(p, num_sms, st)
+                         : launch_one<128, false, BF16, TT>(p, num_sms, st);
     if (q_dt == PKV_BF16)
-        return p.d == 64 ? launch_one<64, true, BF16>(p, num_sms, st) : launch_one<128, true, BF16>(p, num_sms, st);
-    return p.d == 64 ? launch_one<64, true, F32>(p, num_sms, st) : launch_one<128, true, F32>(p, num_sms, st);
+        return p.d == 64 ? launch_one<64, true, BF16, TT>(p, num_sms, st) : launch_one<128, true, BF16, TT>(p, num_sms, st);
+    return p.d == 64 ? launch_one<64, true, F32, TT>(p, num_sms, st) : launch_one<128, true, F32, TT>(p, num_sms, st);
+}
+
+cudaError_t launch_decode_tc(const DecodeParams& p, pkv_dtype q_dt, pkv_dtype c_dt, int num_sms, cudaStream_t st,
+                             bool token_table) {
+    if (p.S == 0) return cudaSuccess;
+    return token_table ? launch_tc<true>(p, q_dt, c_dt, num_sms, st) : launch_tc<false>(p, q_dt, c_dt, num_sms, st);
 }
 
 }  // namespace pkv

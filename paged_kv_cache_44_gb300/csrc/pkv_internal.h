@@ -35,18 +35,31 @@ struct CopyParams {
 };
 cudaError_t launch_copy(const CopyParams& p, cudaStream_t st);
 
+struct RepackParams {
+    const int64_t* moves;     // [M][4]: sequence, logical index, source slot, destination slot
+    int32_t* token_slots;     // [S][MT]
+    int32_t* err;
+    int M, L, S, MT, NB, bs;
+    unsigned long long token_bytes;
+    void* k[kMaxCopyLayers];
+    void* v[kMaxCopyLayers];
+};
+cudaError_t launch_repack(const RepackParams& p, cudaStream_t st);
+
 struct DecodeParams {
     void* out;
     const void* q;
     const void* kc;
     const void* vc;
     const int32_t* block_tables;
-    const int32_t* context_lens;
+    const int32_t* token_slots;   // [S][MT]: decoding through a token table (then block_tables is unused)
+    const int32_t* context_lens;  // tokens per sequence (live tokens, with a token table)
     float* part_ml;       // [S][Hq][Pmax][2]: running max (log2 units) and sum
     float* part_acc;      // [S][Hq][Pmax][d]: un-normalised weighted sums of V
     unsigned* sched;      // scheduling counters in the workspace header (or null)
     int32_t* err;
     int S, MB, Hq, Hkv, g, d, bs, NB;
+    int MT;               // row length of token_slots
     int P;                // tokens per partition (> 0)
     int Pmax;             // partitions of the longest sequence
     int max_ctx;
@@ -66,7 +79,7 @@ enum class DecodeKernel { Simt = 0, TensorCore = 1 };
 
 cudaError_t launch_decode_simt(const DecodeParams& p, pkv_dtype q_dt, pkv_dtype c_dt, cudaStream_t st);
 cudaError_t launch_decode_tc(const DecodeParams& p, pkv_dtype q_dt, pkv_dtype c_dt, int num_sms,
-                             cudaStream_t st);
+                             cudaStream_t st, bool token_table = false);
 cudaError_t launch_decode_reduce(const DecodeParams& p, pkv_dtype q_dt, cudaStream_t st);
 bool decode_tc_supports(pkv_dtype q_dt, pkv_dtype c_dt, int d, int bs, int NB);
 cudaError_t launch_prefill_tc(const DecodeParams& p, const int32_t* query_start, int T, int max_q_len, int num_sms,

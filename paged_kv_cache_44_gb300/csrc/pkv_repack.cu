@@ -1,0 +1,68 @@
+// Repacking of live tokens ("LLM推論の「見えないメモリ問題」を解く … vToken",
+// asynchronous repacking): each move names a sequence, the logical index of
+// one of its live tokens, the token's current slot and a free destination
+// slot.  The first kernel copies the token's K and V rows of every layer
+// from the source slot to the destination; the second, ordered after it on
+// the stream, rewrites the token-table entry.  Keeping them apart means no
+// copy ever reads an entry that another block has already rewritten.  A move
+// whose indices are out of range, or whose source is not what the table
+// holds, is skipped by both and reported (PKV_DEVERR_MOVE).
+#include "pkv_common.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+__device__ __forceinline__ bool move_ok(const RepackParams& p, int m, int64_t& seq, int64_t& idx, int64_t& src,
+                                        int64_t& dst) {
+    const int64_t* mv = p.moves + 4 * (size_t)m;
+    seq = mv[0];
+    idx = mv[1];
+    src = mv[2];
+    dst = mv[3];
+    const int64_t slots = (int64_t)p.NB * p.bs;
+    return seq >= 0 && seq < p.S && idx >= 0 && idx < p.MT && src >= 0 && src < slots && dst >= 0 && dst < slots &&
+           p.token_slots[seq * p.MT + idx] == src;
+}
+
+// grid (moves, layers); a block copies one token's K and V rows of one layer
+__global__ void __launch_bounds__(128) repack_copy_kernel(const __grid_constant__ RepackParams p) {
+    int64_t seq, idx, src, dst;
+    if (!move_ok(p, blockIdx.x, seq, idx, src, dst)) return;
+    const int l = blockIdx.y;
+    const size_t n16 = p.token_bytes / 16;
+    const uint4* ks = reinterpret_cast<const uint4*>(static_cast<const char*>(p.k[l]) + src * p.token_bytes);
+    const uint4* vs = reinterpret_cast<const uint4*>(static_cast<const char*>(p.v[l]) + src * p.token_bytes);
+    uint4* kd = reinterpret_cast<uint4*>(static_cast<char*>(p.k[l]) + dst * p.token_bytes);
+    uint4* vd = reinterpret_cast<uint4*>(static_cast<char*>(p.v[l]) + dst * p.token_bytes);
+    for (size_t i = threadIdx.x; i < n16; i += blockDim.x) {
+        const uint4 a = ks[i], b = vs[i];
+        kd[i] = a;
+        vd[i] = b;
+    }
+}
+
+// one thread per move: the table entry now names the destination slot
+__global__ void __launch_bounds__(256) repack_table_kernel(const __grid_constant__ RepackParams p) {
+    const long long m = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (m >= p.M) return;
+    int64_t seq, idx, src, dst;
+    if (!move_ok(p, (int)m, seq, idx, src, dst)) {
+        report(p.err, PKV_DEVERR_MOVE);
+        return;
+    }
+    p.token_slots[seq * p.MT + idx] = (int32_t)dst;
+}
+
+}  // namespace
+
+cudaError_t launch_repack(const RepackParams& p, cudaStream_t st) {
+    if (p.M == 0 || p.L == 0) return cudaSuccess;
+    repack_copy_kernel<<<dim3((unsigned)p.M, (unsigned)p.L), 128, 0, st>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    repack_table_kernel<<<(unsigned)((p.M + 255) / 256), 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -106,3 +106,45 @@ def test_model_rejects_bad_tables():
         model.plan(np.array([[3, 3]], np.int32), np.array([2]), 16, 4)
     with pytest.raises(ValueError):
         model.plan(np.array([[99]], np.int32), np.array([1]), 16, 4)
+
+
+# ---- the library's planner (C++, pkv_vtoken_plan) against the model
+
+@pytest.fixture(scope="module")
+def pkv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_44_gb300 as P
+    return P
+
+
+def _lib_plan(pkv):
+    def plan_fn(slots, nt, bs, NB):
+        m, f = pkv.vtoken_plan(slots, nt, bs, NB)
+        return [tuple(int(x) for x in r) for r in m], [int(x) for x in f]
+    return plan_fn
+
+
+def test_library_planner_pins(pkv):
+    fn = _lib_plan(pkv)
+    pages_example(fn)
+    hole_order_case(fn)
+    sparse_shared_case(fn, model.apply)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_library_planner_matches_model(pkv, seed):
+    rng = np.random.default_rng(100 + seed)
+    bs = int(rng.choice([4, 16, 32]))
+    slots, nt, sh = random_tables(rng, int(rng.integers(1, 9)), bs, 400, float(rng.uniform(0.05, 1.0)),
+                                  int(rng.integers(0, 3)))
+    want = model.plan(slots, nt, bs, 400)
+    got = _lib_plan(pkv)(slots, nt, bs, 400)
+    assert got[0] == [tuple(m) for m in want[0]] and got[1] == want[1]
+
+
+def test_library_planner_rejects(pkv):
+    with pytest.raises(pkv.PkvError):
+        pkv.vtoken_plan(np.array([[3, 3]], np.int32), np.array([2], np.int32), 16, 4)
+    with pytest.raises(pkv.PkvError):
+        pkv.vtoken_plan(np.array([[99]], np.int32), np.array([1], np.int32), 16, 4)

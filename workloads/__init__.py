@@ -350,3 +350,26 @@ def device_pool_chunks(seed: int, which: int, numel: int, device="cuda", chunk: 
     for i, c0 in enumerate(range(0, numel, chunk)):
         n = min(chunk, numel - c0)
         yield c0, device_normal(seed, which * 100000 + i, n, device)
+
+
+# ------------------------------------------------------------- token tables
+
+def token_tables(w: Workload, keep_frac: float, seed_tag: str = "deletion"):
+    """Token tables after a deletion policy thinned each sequence of `w`: every
+    token survives with probability keep_frac (at least one per non-empty
+    sequence).  Returns (token_slots int32 [S, MT], num_tokens int32 [S]): the
+    survivors' slots (block * bs + offset, from the block table) in logical
+    order, and their counts."""
+    rng = _rng(w.seed, seed_tag)
+    MT = max(int(w.context_lens.max()) if w.S else 1, 1)
+    slots = np.zeros((w.S, MT), np.int32)
+    nt = np.zeros(w.S, np.int32)
+    for s in range(w.S):
+        n = int(w.context_lens[s])
+        keep = rng.random(n) < keep_frac
+        if n and not keep.any():
+            keep[int(rng.integers(0, n))] = True
+        t = np.nonzero(keep)[0]
+        slots[s, : t.size] = w.block_tables[s, t // w.bs].astype(np.int64) * w.bs + t % w.bs
+        nt[s] = t.size
+    return slots, nt
