@@ -253,6 +253,7 @@ KERNEL_SOURCES = {
     "pkv_decode": ["pkv_decode_tc.cu", "pkv_decode_simt.cu", "pkv_common.cuh", "pkv_tc_common.cuh"],
     "pkv_prefill": ["pkv_prefill_umma.cu", "pkv_prefill_tc.cu", "pkv_qtile.cuh", "pkv_umma.cuh", "pkv_common.cuh",
                     "pkv_tc_common.cuh"],
+    "pkv_vtoken": ["pkv_decode_tc.cu", "pkv_decode_simt.cu", "pkv_repack.cu", "pkv_common.cuh", "pkv_tc_common.cuh"],
 }
 
 
@@ -730,6 +731,146 @@ def prefill_cpu_baseline(w: W.Workload, qlens: np.ndarray, budget: float, tensor
                       "tokens), %.1f s" % (seqs, calls, queries, keys, spent)}
 
 
+def token_decode_bytes(w: W.Workload, nt: np.ndarray) -> int:
+    """Algorithmic bytes of a decode through token tables: query and output,
+    the K/V rows of every live token once, and the table entries read."""
+    bq, bkv = ELEM[w.q_dtype], ELEM[w.cache_dtype]
+    live = int(nt.astype(np.int64).sum())
+    return 2 * w.S * w.Hq * w.d * bq + live * w.Hkv * w.d * 2 * bkv + live * 4 + w.S * 4
+
+
+def run_vtoken(args, w: W.Workload):
+    """Token tables after a deletion policy kept half of each sequence's
+    tokens at random: decode through the sparse tables, plan and run the
+    repacking (every layer's K and V row of each moved token, one layer
+    here), then decode through the compacted tables."""
+    import torch
+    import paged_kv_cache_44_gb300 as pkv
+
+    ws, rank, local = dist_setup()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    seed = w.seed + 7919 * rank
+    keep = 0.5
+    slots_h, nt_h = W.token_tables(w, keep)
+    kc, vc, k_scale, v_scale = device_caches(w, seed, dev, stream)
+    with torch.cuda.stream(stream):
+        q = W.device_bf16_from_draws(W.device_normal(seed, 31, w.S * w.Hq * w.d, dev)).view(w.S, w.Hq, w.d)
+    ts0 = torch.from_numpy(slots_h).to(dev)
+    nt = torch.from_numpy(nt_h).to(dev)
+    mx = int(nt_h.max())
+    P = args.partition if args.partition is not None else w.partition_size
+    wsp = pkv.make_workspace(w.S, w.Hq, w.Hkv, w.d, w.bs, mx, P, device=dev)
+    out = torch.empty_like(q)
+    torch.cuda.synchronize(dev)
+    nbytes = token_decode_bytes(w, nt_h)
+
+    def decode(ts, qq=q, ntt=nt):
+        pkv.token_attention_decode(out, qq, kc, vc, ts, ntt, mx, scale=w.scale, k_scale=k_scale, v_scale=v_scale,
+                                   partition_size=P, workspace=wsp, stream=stream)
+
+    def timed_decode(ts):
+        for _ in range(args.warmup):
+            decode(ts)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            decode(ts)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / args.steps
+
+    uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    with ClockSampler(uuid) as clk:
+        ms_sparse = timed_decode(ts0)
+    clocks = clk.summary()
+
+    # repacking: plan on the host, move on the device
+    t0 = time.perf_counter()
+    moves_h, freed_h = pkv.vtoken_plan(slots_h, nt_h, w.bs, w.NB)
+    plan_s = time.perf_counter() - t0
+    moves = torch.from_numpy(moves_h).to(dev)
+    moved_bytes = 2 * 2 * len(moves_h) * w.Hkv * w.d * ELEM[w.cache_dtype]      # K and V, read and write
+    ts = ts0.clone()
+    rep_ms = []
+    for i in range(args.warmup + 5):
+        ts.copy_(ts0)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        pkv.repack_tokens([kc], [vc], ts, moves, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= args.warmup:
+            rep_ms.append(e0.elapsed_time(e1))
+    ms_repack = statistics.median(rep_ms)
+    ms_dense = timed_decode(ts)
+    (ms_sparse, ms_dense, ms_repack) = max_over_ranks([ms_sparse, ms_dense, ms_repack], dev)
+
+    # end to end: host query and tables in, output out, through the public API
+    h_in = {k: v.cpu().pin_memory() for k, v in dict(q=q, ts=ts, nt=nt).items()}
+    d_in = {k: torch.empty_like(v, device=dev) for k, v in h_in.items()}
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 100))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for k in h_in:
+                d_in[k].copy_(h_in[k], non_blocking=True)
+        decode(d_in["ts"], qq=d_in["q"], ntt=d_in["nt"])
+        with torch.cuda.stream(stream):
+            h_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    w0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    (e2e_s,) = max_over_ranks([(time.perf_counter() - w0) / e2e_steps], dev)
+
+    gbs_sparse = whole_job_gbs(ws, nbytes, ms_sparse)
+    gbs_dense = whole_job_gbs(ws, nbytes, ms_dense)
+    peak, peak_kind = peak_hbm()
+    line = {
+        "component": "vtoken", "metric": "token-table decode KV GB/s (live tokens), after repacking",
+        "value": round(gbs_dense, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_dense, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.cache_dtype == W.DT_BF16 else w.cache_dtype, "data": "synthetic",
+        "config": {"workload": w.name + "-vtoken", "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "bs": w.bs,
+                   "tokens_before_deletion": int(w.context_lens.astype(np.int64).sum()),
+                   "live_tokens": int(nt_h.sum()), "deletion": "each token kept with probability %.2f" % keep,
+                   "partition_size": P, "l2": "inputs larger than L2",
+                   "step": "token_attention_decode over every sequence's live tokens"},
+        "decode_before_repack_gbs": round(gbs_sparse, 2), "decode_before_repack_ms": round(ms_sparse, 5),
+        "repack": {"moves": int(len(moves_h)), "blocks_released": int(len(freed_h)),
+                   "blocks_in_use_before": int(len({int(x) // w.bs for s in range(w.S) for x in slots_h[s, : nt_h[s]]})),
+                   "ms": round(ms_repack, 5), "gbs": round(moved_bytes / (ms_repack * 1e-3) / 1e9, 2),
+                   "plan_ms_host": round(plan_s * 1e3, 2), "layers": 1},
+        "roofline": {"bound": "hbm", "achieved": round(gbs_dense / ws, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs_dense / ws / peak, 4), "peak_kind": peak_kind,
+                     "traffic": measured_traffic(w.name, "vtoken", "vtoken_traffic.json", "pkv_vtoken"),
+                     "kernel": "token_attention_decode (tensor cores, cp.async row gather)",
+                     "algorithmic_bytes_per_launch": nbytes, "launch_ms": round(ms_dense, 5)},
+        "e2e": {"value": round(whole_job_gbs(ws, nbytes, e2e_s * 1e3), 2), "unit": "GB/s",
+                "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in h_in.values()),
+                "d2h_bytes_per_step": h_out.numel() * h_out.element_size(), "ms_per_step": round(e2e_s * 1e3, 4)},
+        "gpu_launches": (2 if wsp.numel() > 256 else 1) * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def run_block_manager(args):
     """Host block manager throughput, serving-like: S sequences whose
     prompts share a system prefix are admitted (prefix-cache lookups and
@@ -786,7 +927,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--S", type=int, default=None, help="fewer sequences (small profiling cases)")
-    ap.add_argument("--component", default="decode-step", choices=["decode-step", "prefill", "block-manager"],
+    ap.add_argument("--component", default="decode-step", choices=["decode-step", "prefill", "vtoken",
+                                                                   "block-manager"],
                     help="prefill: paged attention over query chunks; block-manager: the host block "
                          "manager (each prints its own line)")
     args = ap.parse_args()
@@ -798,6 +940,11 @@ def main():
     if args.workload is None:
         args.workload = "qwen2.5-7b-chunked" if args.component == "prefill" else "qwen2.5-72b-long"
     w = W.make(args.workload, S=args.S) if args.S else W.make(args.workload)
+    if args.component == "vtoken":
+        if args.impl == "reference":
+            ap.error("--impl reference times the decode step")
+        run_vtoken(args, w)
+        return
     if args.component == "prefill":
         if args.impl == "reference":
             ap.error("--impl reference times the decode step")
