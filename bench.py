@@ -422,13 +422,25 @@ def run_ours(args, w: W.Workload):
     launches_per_step = 1 + (2 if split else 1) + (1 if len(w.cow_pairs) else 0)
     torch.cuda.synchronize(dev)
 
+    fused = args.fused and decode_kernel_name(args.kernel, w) == "tensor_cores"
+    if fused:
+        launches_per_step -= 1
+
     def step(ev0=None, ev1=None, qq=q, nk=new_k, nv=new_v, btab=bt, clen=cl, slots=sm, pairs=cow, o=out):
-        pkv.paged_kv_write(nk, nv, kc, vc, slots, k_scale, v_scale, stream=stream)
-        if ev0 is not None:
-            ev0.record(stream)
-        pkv.paged_attention_decode(o, qq, kc, vc, btab, clen, mc, scale=w.scale, k_scale=k_scale,
-                                   v_scale=v_scale, partition_size=P, workspace=wsp, stream=stream,
-                                   kernel=args.kernel)
+        if fused:
+            # one launch writes the new tokens and decodes (the timed "decode" includes the write)
+            if ev0 is not None:
+                ev0.record(stream)
+            pkv.paged_kv_write_decode(o, qq, nk, nv, kc, vc, slots, btab, clen, mc, scale=w.scale,
+                                      k_scale=k_scale, v_scale=v_scale, partition_size=P, workspace=wsp,
+                                      stream=stream)
+        else:
+            pkv.paged_kv_write(nk, nv, kc, vc, slots, k_scale, v_scale, stream=stream)
+            if ev0 is not None:
+                ev0.record(stream)
+            pkv.paged_attention_decode(o, qq, kc, vc, btab, clen, mc, scale=w.scale, k_scale=k_scale,
+                                       v_scale=v_scale, partition_size=P, workspace=wsp, stream=stream,
+                                       kernel=args.kernel)
         if ev1 is not None:
             ev1.record(stream)
         if len(w.cow_pairs):
@@ -493,17 +505,14 @@ def run_ours(args, w: W.Workload):
     (e2e_s,) = max_over_ranks([e2e_s], dev)
 
     # ---- numbers
-    dbytes = decode_bytes(w)
-    sbytes = dbytes + write_bytes(w) + copy_bytes(w)
+    dbytes = decode_bytes(w) + (write_bytes(w) if fused else 0)
+    sbytes = decode_bytes(w) + write_bytes(w) + copy_bytes(w)
     value = whole_job_gbs(ws, sbytes, ms_step)
     achieved = dbytes / (dec_ms * 1e-3) / 1e9
     peak, peak_kind = peak_hbm()
     traffic = measured_traffic(w.name, args.kernel)
     clocks = clk.summary()
-    kname = args.kernel
-    if kname == "auto":
-        kname = "tensor_cores" if (w.cache_dtype == W.DT_E4M3 or
-                                   (w.cache_dtype == W.DT_BF16 and w.q_dtype == W.DT_BF16)) else "cuda_cores"
+    kname = decode_kernel_name(args.kernel, w)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
@@ -511,18 +520,20 @@ def run_ours(args, w: W.Workload):
         "data": "synthetic",
         "config": {"workload": w.name, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "bs": w.bs,
                    "cache_dtype": w.cache_dtype, "q_dtype": w.q_dtype, "max_context_len": mc,
-                   "partition_size": Pres, "decode_kernel": kname,
+                   "partition_size": Pres, "decode_kernel": kname, "fused_write_decode": bool(fused),
                    "kv_bytes": int(w.context_lens.astype(np.int64).sum()) * w.Hkv * w.d * 2 * ELEM[w.cache_dtype],
                    "l2": "inputs larger than L2" if dbytes > 2 * 129e6 else "not flushed: inputs near L2 size",
-                   "step": "paged_kv_write(1 token/seq) + paged_attention_decode + copy_blocks(%d pairs)"
-                           % len(w.cow_pairs)},
+                   "step": ("paged_kv_write_decode(1 token/seq, one launch)" if fused else
+                            "paged_kv_write(1 token/seq) + paged_attention_decode") +
+                           " + copy_blocks(%d pairs)" % len(w.cow_pairs)},
         "seq_steps_per_s": round(ws * w.S / (ms_step * 1e-3), 1),
         "decode_gbs": round(achieved, 2),
         "hbm_frac_of_measured": round(achieved / peak, 4),
         "hbm_frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "traffic": traffic, "kernel": "paged_attention_decode (" + kname + ")",
+                     "traffic": None if fused else traffic,
+                     "kernel": ("paged_kv_write_decode (" if fused else "paged_attention_decode (") + kname + ")",
                      "algorithmic_bytes_per_launch": dbytes, "launch_ms": round(dec_ms, 5)},
         "e2e": {"value": round(whole_job_gbs(ws, sbytes, e2e_s * 1e3), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)},
@@ -541,6 +552,13 @@ def run_ours(args, w: W.Workload):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def decode_kernel_name(kernel: str, w: W.Workload) -> str:
+    if kernel != "auto":
+        return kernel
+    return "tensor_cores" if (w.cache_dtype == W.DT_E4M3 or
+                              (w.cache_dtype == W.DT_BF16 and w.q_dtype == W.DT_BF16)) else "cuda_cores"
 
 
 def peak_bf16(sustained: bool):
@@ -923,6 +941,8 @@ def main():
     ap.add_argument("--kernel", default="auto", choices=["auto", "cuda_cores", "tensor_cores"])
     ap.add_argument("--partition", type=int, default=None)
     ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "tcgen05", "mma_sync"])
+    ap.add_argument("--fused", action="store_true",
+                    help="decode-step: write the new tokens and decode in one launch")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

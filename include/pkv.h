@@ -171,6 +171,32 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* query, pkv_
                                       void* workspace, size_t workspace_bytes,
                                       int32_t* err_word, pkv_stream_t stream);
 
+/*
+ * paged_kv_write_decode -- pkv_paged_kv_write of one new token per sequence
+ * followed by pkv_paged_attention_decode, in one launch (plus the merge
+ * when split).  key/value [S, Hkv, d] (in_dtype f32 or bf16) are the new
+ * tokens, slot_mapping [S] int64 their slots, which must be the slots of
+ * the sequences' last positions (context_lens[s] - 1, through
+ * block_tables); a negative slot skips that sequence's write, as in
+ * paged_kv_write.  The caches end up as after the two calls and the output
+ * equals theirs bit for bit.  The decode unit that holds a sequence's last
+ * token puts the converted new K/V into its staged rows and stores them to
+ * the slot.  Supported: the tensor-core decode's dtypes (see
+ * pkv_paged_attention_decode_ex); anything else returns PKV_ERR_UNSUPPORTED.
+ * Source: the two calls' passages; one launch per step instead of two.
+ */
+PKV_API pkv_status pkv_paged_kv_write_decode(void* out, const void* query, pkv_dtype q_dtype,
+                                             const void* key, const void* value, pkv_dtype in_dtype,
+                                             void* key_cache, void* value_cache, pkv_dtype cache_dtype,
+                                             const int64_t* slot_mapping,
+                                             const int32_t* block_tables, int MB,
+                                             const int32_t* context_lens, int S, int max_context_len,
+                                             int Hq, int Hkv, int d, int bs, int NB,
+                                             float scale, float k_scale, float v_scale,
+                                             int partition_size,
+                                             void* workspace, size_t workspace_bytes,
+                                             int32_t* err_word, pkv_stream_t stream);
+
 /* Kernel choice for pkv_paged_attention_decode_ex. */
 typedef enum {
     PKV_DECODE_AUTO = 0,          /* tensor cores where supported, else CUDA cores */

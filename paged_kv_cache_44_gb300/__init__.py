@@ -41,7 +41,7 @@ EXPORTED = ("pkv_paged_kv_write", "pkv_decode_workspace_size", "pkv_decode_parti
             "pkv_pool_append_token", "pkv_pool_fork", "pkv_pool_free_sequence", "pkv_pool_block_table",
             "pkv_pool_append_tokens", "pkv_pool_block_tables", "pkv_prefill_workspace_size",
             "pkv_paged_attention_prefill", "pkv_paged_attention_prefill_ex", "pkv_token_attention_decode",
-            "pkv_repack_tokens", "pkv_vtoken_plan")
+            "pkv_repack_tokens", "pkv_vtoken_plan", "pkv_paged_kv_write_decode")
 STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -109,6 +109,9 @@ def _load() -> ctypes.CDLL:
     lib.pkv_paged_attention_prefill.restype = i32
     lib.pkv_paged_attention_prefill_ex.argtypes = lib.pkv_paged_attention_prefill.argtypes + [i32]
     lib.pkv_paged_attention_prefill_ex.restype = i32
+    lib.pkv_paged_kv_write_decode.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, i32, vp, vp, i32, vp, i32, i32, i32,
+                                              i32, i32, i32, i32, f32, f32, f32, i32, vp, sz, vp, vp]
+    lib.pkv_paged_kv_write_decode.restype = i32
     lib.pkv_token_attention_decode.argtypes = dec
     lib.pkv_token_attention_decode.restype = i32
     lib.pkv_repack_tokens.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32, vp, i32, i32, vp, i32, i32, i32,
@@ -308,6 +311,36 @@ def copy_blocks(key_caches: Sequence[torch.Tensor], value_caches: Sequence[torch
     vp = (ctypes.c_void_p * L)(*[_ptr(t) for t in value_caches])
     _check("copy_blocks", lib.pkv_copy_blocks(kp, vp, L, _ptr(block_mapping), P, NB, block_bytes,
                                               _ptr(err_word), _stream(stream)))
+
+
+def paged_kv_write_decode(out: torch.Tensor, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
+                          key_cache: torch.Tensor, value_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                          block_tables: torch.Tensor, context_lens: torch.Tensor, max_context_len: int,
+                          scale: Optional[float] = None, k_scale: float = 1.0, v_scale: float = 1.0,
+                          partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
+                          err_word: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """paged_kv_write of each sequence's new token (key/value [S, Hkv, d],
+    slot_mapping int64 [S]: the slot of its last position) and the decode, in
+    one launch.  Same results as the two calls."""
+    S, Hq, d = query.shape
+    NB, bs, Hkv, d2 = key_cache.shape
+    if d2 != d or out.shape != query.shape or out.dtype != query.dtype or value_cache.shape != key_cache.shape:
+        raise ValueError("shape or dtype mismatch")
+    if key.shape != (S, Hkv, d) or value.shape != key.shape or key.dtype != value.dtype:
+        raise ValueError("key/value must be [S, Hkv, d] of one dtype")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != S:
+        raise ValueError("slot_mapping must be int64 [S]")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 or block_tables.dim() != 2:
+        raise ValueError("block_tables and context_lens must be int32")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
+    _check("paged_kv_write_decode", lib.pkv_paged_kv_write_decode(
+        _ptr(out), _ptr(query), dtype_code(query.dtype), _ptr(key), _ptr(value), dtype_code(key.dtype),
+        _ptr(key_cache), _ptr(value_cache), dtype_code(key_cache.dtype), _ptr(slot_mapping), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), S, int(max_context_len), Hq, Hkv, d, bs, NB, float(scale),
+        float(k_scale), float(v_scale), int(partition_size), ws_ptr, ws_bytes, _ptr(err_word), _stream(stream)))
+    return out
 
 
 def token_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,

@@ -192,6 +192,67 @@ pkv_status pkv_paged_attention_decode_ex(void* out, const void* query, pkv_dtype
     return from_cuda(e);
 }
 
+pkv_status pkv_paged_kv_write_decode(void* out, const void* query, pkv_dtype q_dtype, const void* key,
+                                     const void* value, pkv_dtype in_dtype, void* key_cache, void* value_cache,
+                                     pkv_dtype cache_dtype, const int64_t* slot_mapping, const int32_t* block_tables,
+                                     int MB, const int32_t* context_lens, int S, int max_context_len, int Hq, int Hkv,
+                                     int d, int bs, int NB, float scale, float k_scale, float v_scale,
+                                     int partition_size, void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                     pkv_stream_t stream) {
+    if (S < 0 || MB < 1 || NB < 1 || Hkv < 1 || Hq < 1 || max_context_len < 0) return PKV_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return PKV_ERR_INVALID_ARG;
+    if (q_dtype != PKV_F32 && q_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (in_dtype != PKV_F32 && in_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (cache_dtype != PKV_F32 && cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3)
+        return PKV_ERR_UNSUPPORTED;
+    if (!decode_tc_supports(q_dtype, cache_dtype, d, bs, NB)) return PKV_ERR_UNSUPPORTED;
+    if (S > 65535) return PKV_ERR_UNSUPPORTED;
+    if ((long long)max_context_len > (long long)MB * bs) return PKV_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    if (cache_dtype == PKV_FP8_E4M3 && (!finite_pos(k_scale) || !finite_pos(v_scale))) return PKV_ERR_INVALID_ARG;
+    if (partition_size < -1 || (partition_size > 0 && partition_size % bs != 0)) return PKV_ERR_INVALID_ARG;
+    if (S == 0) return PKV_OK;
+    if (!out || !query || !key || !value || !key_cache || !value_cache || !slot_mapping || !block_tables ||
+        !context_lens)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(key) || !aligned16(value) || !aligned16(key_cache) ||
+        !aligned16(value_cache) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+        return PKV_ERR_INVALID_ARG;
+    const int P = resolve_partition(S, Hq, Hkv, d, bs, max_context_len, partition_size);
+    if (P < 0) return PKV_ERR_INVALID_ARG;
+    const DecodePlan pl = make_plan(S, Hq, d, max_context_len, P);
+    if (pl.split) {
+        if (!workspace || workspace_bytes < pl.bytes) return PKV_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return PKV_ERR_INVALID_ARG;
+    }
+    DecodeParams p{};
+    p.out = out; p.q = query; p.kc = key_cache; p.vc = value_cache;
+    p.block_tables = block_tables; p.context_lens = context_lens; p.err = err_word;
+    p.S = S; p.MB = MB; p.Hq = Hq; p.Hkv = Hkv; p.g = Hq / Hkv; p.d = d; p.bs = bs; p.NB = NB;
+    p.P = pl.P > 0 ? pl.P : MB * bs;
+    p.Pmax = pl.Pmax;
+    p.max_ctx = max_context_len;
+    const float ks = cache_dtype == PKV_FP8_E4M3 ? k_scale : 1.f;
+    p.logit_scale_log2 = scale * ks * kLog2e;
+    p.out_scale = cache_dtype == PKV_FP8_E4M3 ? v_scale : 1.f;
+    p.new_k = key; p.new_v = value; p.slot_mapping = slot_mapping; p.new_dt = in_dtype;
+    p.k_scale = k_scale; p.v_scale = v_scale;
+    if (pl.split) {
+        char* ws = static_cast<char*>(workspace);
+        p.sched = reinterpret_cast<unsigned*>(ws);
+        p.part_ml = reinterpret_cast<float*>(ws + pl.ml_offset);
+        p.part_acc = reinterpret_cast<float*>(ws + pl.acc_offset);
+    } else if (workspace && workspace_bytes >= kWorkspaceHeaderBytes && aligned16(workspace)) {
+        p.sched = reinterpret_cast<unsigned*>(workspace);
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_decode_tc(p, q_dtype, cache_dtype, num_sms_current(), st);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    if (pl.split) e = launch_decode_reduce(p, q_dtype, st);
+    return from_cuda(e);
+}
+
 pkv_status pkv_token_attention_decode(void* out, const void* query, pkv_dtype q_dtype, const void* key_cache,
                                       const void* value_cache, pkv_dtype cache_dtype, const int32_t* token_slots,
                                       int MT, const int32_t* num_tokens, int S, int max_tokens, int Hq, int Hkv,

@@ -65,4 +65,67 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float a, float b) {
     return r;
 }
 
+// ---- the conversions of a new token's K/V into the cache format, shared by
+// paged_kv_write and the fused write + decode
+
+// 8 consecutive input elements as fp32
+template <typename In>
+__device__ __forceinline__ void load8(const void* base, size_t i, float v[8]);
+template <>
+__device__ __forceinline__ void load8<F32>(const void* base, size_t i, float v[8]) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
+    float4 a = __ldg(p), b = __ldg(p + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void load8<BF16>(const void* base, size_t i, float v[8]) {
+    uint4 r = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + i));
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        v[2 * k] = __uint_as_float(w[k] << 16);
+        v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+}
+// 8 elements in bf16: round to nearest even
+__device__ __forceinline__ uint4 pack8_bf16(const float v[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+        w[k] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+// 8 elements in E4M3: one IEEE fp32 divide by the scale per element, then
+// round to nearest even with saturation
+__device__ __forceinline__ uint2 pack8_e4m3(const float v[8], float scale) {
+    uint32_t w[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(v[4 * k + 0], scale), __fdiv_rn(v[4 * k + 1], scale));
+        uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(v[4 * k + 2], scale), __fdiv_rn(v[4 * k + 3], scale));
+        w[k] = lo | (hi << 16);
+    }
+    return make_uint2(w[0], w[1]);
+}
+
+template <typename Out>
+__device__ __forceinline__ void store8(void* base, size_t i, const float v[8], float scale);
+template <>
+__device__ __forceinline__ void store8<F32>(void* base, size_t i, const float v[8], float) {
+    float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + i);
+    p[0] = make_float4(v[0], v[1], v[2], v[3]);
+    p[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+template <>
+__device__ __forceinline__ void store8<BF16>(void* base, size_t i, const float v[8], float) {
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + i) = pack8_bf16(v);
+}
+template <>
+__device__ __forceinline__ void store8<E4M3>(void* base, size_t i, const float v[8], float scale) {
+    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(base) + i) = pack8_e4m3(v, scale);
+}
+
 }  // namespace pkv

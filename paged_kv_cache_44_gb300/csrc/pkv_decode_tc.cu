@@ -381,6 +381,48 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
     const float scl = p.logit_scale_log2;
     bool bail = false;
 
+    // Fused write + decode: when this stage holds the sequence's last token,
+    // its rows in the stage are replaced by the step's new K and V (converted
+    // exactly as paged_kv_write converts them), and the unit of the first
+    // head set stores them to the cache slot.  Lanes 0..CPR-1 take 16-byte
+    // chunks of the K row, CPR..2 CPR-1 those of the V row.
+    auto patch_new_token = [&](uint32_t kb, uint32_t vb) {
+        const int n = min(max(__ldg(p.context_lens + cu.s), 0), p.max_ctx);
+        const int ts = cu.t0 + c_stage * kTok;
+        const int tl = n - 1 - ts;
+        if (n < 1 || n > cu.t1 || tl < 0 || tl >= kTok) return;
+        const long long sn = __ldg(p.slot_mapping + cu.s);
+        if (sn < 0 || sn >= (long long)p.NB * p.bs) return;
+        constexpr int CPR = C::kRowBytes / 16;
+        static_assert(2 * CPR <= 32, "one chunk per lane");
+        if (lane < 2 * CPR) {
+            const bool isv = lane >= CPR;
+            const int j = lane % CPR;
+            const void* src = isv ? p.new_v : p.new_k;
+            uint4 chunk;
+            float v[8];
+            if constexpr (FP8) {
+                const size_t e = ((size_t)cu.s * p.Hkv + cu.kvh) * D + 16 * (size_t)j;
+                const float sc = isv ? p.v_scale : p.k_scale;
+                if (p.new_dt == PKV_F32) load8<F32>(src, e, v); else load8<BF16>(src, e, v);
+                const uint2 lo = pack8_e4m3(v, sc);
+                if (p.new_dt == PKV_F32) load8<F32>(src, e + 8, v); else load8<BF16>(src, e + 8, v);
+                const uint2 hi = pack8_e4m3(v, sc);
+                chunk = make_uint4(lo.x, lo.y, hi.x, hi.y);
+            } else {
+                const size_t e = ((size_t)cu.s * p.Hkv + cu.kvh) * D + 8 * (size_t)j;
+                if (p.new_dt == PKV_F32) load8<F32>(src, e, v); else load8<BF16>(src, e, v);
+                chunk = pack8_bf16(v);
+            }
+            *reinterpret_cast<uint4*>(ws + (swz<C::kRowBytes, C::kTok>(isv ? vb : kb, tl, 16 * j) - ws_addr)) = chunk;
+            if (cu.h0 == cu.kvh * p.g) {
+                unsigned char* cache = static_cast<unsigned char*>(const_cast<void*>(isv ? p.vc : p.kc));
+                *reinterpret_cast<uint4*>(cache + ((size_t)sn * p.Hkv + cu.kvh) * C::kRowBytes + 16 * j) = chunk;
+            }
+        }
+        __syncwarp();
+    };
+
     for (int i = 0; i < C::kStages; ++i)
         if (!issue_one()) break;
 
@@ -447,6 +489,9 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
         }
         const uint32_t vmask = masks[slot];
         const uint32_t kb = stage_k(slot), vb = stage_v(slot);
+        if constexpr (!TT) {
+            if (p.new_k != nullptr) patch_new_token(kb, vb);
+        }
 
         // ---- S^T = K . Q^T for the 16-token m-tiles of the stage
         float sacc[C::kMT][4];

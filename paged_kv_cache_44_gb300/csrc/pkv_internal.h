@@ -65,6 +65,14 @@ struct DecodeParams {
     int max_ctx;
     float logit_scale_log2;   // scale * k_scale * log2(e)
     float out_scale;          // v_scale for E4M3 caches, else 1
+    // fused write + decode (new_k != null): each sequence's new token, K and
+    // V [S][Hkv][d] of type new_dt, goes to slot_mapping[s], the slot of its
+    // last position, before the decode reads it
+    const void* new_k;
+    const void* new_v;
+    const int64_t* slot_mapping;
+    pkv_dtype new_dt;
+    float k_scale, v_scale;   // E4M3 write scales
 };
 
 // Resolved layout of the decode workspace.

@@ -12,57 +12,6 @@
 namespace pkv {
 namespace {
 
-template <typename In>
-__device__ __forceinline__ void load8(const void* base, size_t i, float v[8]);
-template <>
-__device__ __forceinline__ void load8<F32>(const void* base, size_t i, float v[8]) {
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
-    float4 a = __ldg(p), b = __ldg(p + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-template <>
-__device__ __forceinline__ void load8<BF16>(const void* base, size_t i, float v[8]) {
-    uint4 r = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + i));
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        v[2 * k] = __uint_as_float(w[k] << 16);
-        v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-    }
-}
-
-template <typename Out>
-__device__ __forceinline__ void store8(void* base, size_t i, const float v[8], float scale);
-template <>
-__device__ __forceinline__ void store8<F32>(void* base, size_t i, const float v[8], float) {
-    float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + i);
-    p[0] = make_float4(v[0], v[1], v[2], v[3]);
-    p[1] = make_float4(v[4], v[5], v[6], v[7]);
-}
-template <>
-__device__ __forceinline__ void store8<BF16>(void* base, size_t i, const float v[8], float) {
-    uint32_t w[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
-        w[k] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + i) = make_uint4(w[0], w[1], w[2], w[3]);
-}
-template <>
-__device__ __forceinline__ void store8<E4M3>(void* base, size_t i, const float v[8], float scale) {
-    uint32_t w[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        // one IEEE fp32 divide per element, then RNE + saturation to e4m3
-        uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(v[4 * k + 0], scale), __fdiv_rn(v[4 * k + 1], scale));
-        uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(v[4 * k + 2], scale), __fdiv_rn(v[4 * k + 3], scale));
-        w[k] = lo | (hi << 16);
-    }
-    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(base) + i) = make_uint2(w[0], w[1]);
-}
-
 template <typename In, typename Out>
 __global__ void __launch_bounds__(256) write_kernel(WriteParams p) {
     const int chunks = p.d / 8;
