@@ -218,7 +218,9 @@ def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
     MB = block_tables.shape[1]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
+    if workspace is None:          # convenience: a fresh one per call (pass one in to avoid the allocation)
+        workspace = make_workspace(S, Hq, Hkv, d, bs, max_context_len, partition_size, device=query.device)
+    ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     _check("paged_attention_decode", lib.pkv_paged_attention_decode_ex(
         _ptr(out), _ptr(query), dtype_code(query.dtype), _ptr(key_cache), _ptr(value_cache),
         dtype_code(key_cache.dtype), _ptr(block_tables), MB, _ptr(context_lens), S, int(max_context_len),
@@ -334,7 +336,9 @@ def paged_kv_write_decode(out: torch.Tensor, query: torch.Tensor, key: torch.Ten
         raise ValueError("block_tables and context_lens must be int32")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
+    if workspace is None:
+        workspace = make_workspace(S, Hq, Hkv, d, bs, max_context_len, partition_size, device=query.device)
+    ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     _check("paged_kv_write_decode", lib.pkv_paged_kv_write_decode(
         _ptr(out), _ptr(query), dtype_code(query.dtype), _ptr(key), _ptr(value), dtype_code(key.dtype),
         _ptr(key_cache), _ptr(value_cache), dtype_code(key_cache.dtype), _ptr(slot_mapping), _ptr(block_tables),
@@ -359,7 +363,9 @@ def token_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
         raise ValueError("token_slots and num_tokens must be int32")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
+    if workspace is None:
+        workspace = make_workspace(S, Hq, Hkv, d, bs, max_tokens, partition_size, device=query.device)
+    ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     _check("token_attention_decode", lib.pkv_token_attention_decode(
         _ptr(out), _ptr(query), dtype_code(query.dtype), _ptr(key_cache), _ptr(value_cache),
         dtype_code(key_cache.dtype), _ptr(token_slots), token_slots.shape[1], _ptr(num_tokens), S,
