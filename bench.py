@@ -250,10 +250,11 @@ def peak_hbm():
 
 
 KERNEL_SOURCES = {
-    "pkv_decode": ["pkv_decode_tc.cu", "pkv_decode_simt.cu", "pkv_common.cuh", "pkv_tc_common.cuh"],
+    "pkv_decode": ["pkv_decode_tc.cu", "pkv_decode_simt.cu", "pkv_common.cuh", "pkv_tc_common.cuh", "pkv_merge.cuh"],
     "pkv_prefill": ["pkv_prefill_umma.cu", "pkv_prefill_tc.cu", "pkv_qtile.cuh", "pkv_umma.cuh", "pkv_common.cuh",
-                    "pkv_tc_common.cuh"],
-    "pkv_vtoken": ["pkv_decode_tc.cu", "pkv_decode_simt.cu", "pkv_repack.cu", "pkv_common.cuh", "pkv_tc_common.cuh"],
+                    "pkv_tc_common.cuh", "pkv_merge.cuh"],
+    "pkv_vtoken": ["pkv_decode_tc.cu", "pkv_decode_simt.cu", "pkv_repack.cu", "pkv_common.cuh", "pkv_tc_common.cuh",
+                   "pkv_merge.cuh"],
 }
 
 

@@ -18,6 +18,7 @@
 
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
+#include "pkv_merge.cuh"
 
 namespace pkv {
 namespace {
@@ -35,6 +36,8 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
     const int h0 = kvh * p.g + set * kHeads;
     const int nh = min(kHeads, p.g - set * kHeads);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    // the partition merge that may follow can be scheduled now; it waits for this grid's results
+    asm volatile("griddepcontrol.launch_dependents;");
 
     int n = p.context_lens[s];
     if (n < 0 || n > p.max_ctx) {   // max_ctx <= MB * bs was checked on the host
@@ -160,18 +163,15 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
 }
 
 // Merge of a sequence's partitions: M = max m_p, L = sum 2^(m_p - M) l_p,
-// O = sum 2^(m_p - M) acc_p / L.  One warp per (sequence, query head), eight
-// warps per CTA: lane i weighs partitions i, i+32, ...; the weights are
-// broadcast by shuffle and every lane sums D/32 consecutive elements of each
-// partition's row (one coalesced row load per partition).  Sequences that
-// fit one partition were finished by the decode kernel.  Launched as a
-// programmatic dependent of the decode kernel: it waits for the decode's
-// results before reading them.
+// O = sum 2^(m_p - M) acc_p / L, one warp per (sequence, query head), eight
+// warps per CTA (merge_partitions).  Sequences that fit one partition were
+// finished by the decode kernel.  Launched as a programmatic dependent of
+// the decode kernel, which lets it start at once: the lengths are an input
+// of the decode, so they are read before waiting for the decode's results.
 constexpr int kMergeWarps = 8;
 
 template <int D, typename QF>
 __global__ void __launch_bounds__(kMergeWarps * 32) decode_reduce_kernel(DecodeParams p) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr int E = D / 32;
     const int lane = threadIdx.x & 31;
     const long long gw = (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
@@ -181,111 +181,15 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_reduce_kernel(DecodeP
     n = n < 0 ? 0 : min(n, p.max_ctx);     // same clamp as the decode kernel: np <= Pmax
     const int np = n > 0 ? (n + p.P - 1) / p.P : 1;
     if (np <= 1) return;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t u0 = ((size_t)s * p.Hq + h) * p.Pmax;
-    float mx = -CUDART_INF_F;
-    for (int i = lane; i < np; i += 32) mx = fmaxf(mx, p.part_ml[2 * (u0 + i)]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    float lsum = 0.f, o[E];
-#pragma unroll
-    for (int k = 0; k < E; ++k) o[k] = 0.f;
-    for (int c0 = 0; c0 < np; c0 += 32) {
-        const int i = c0 + lane;
-        float w = 0.f;
-        if (i < np) {
-            const float m = p.part_ml[2 * (u0 + i)];
-            w = m == -CUDART_INF_F ? 0.f : exp2f(m - mx);
-            lsum = fmaf(w, p.part_ml[2 * (u0 + i) + 1], lsum);
-        }
-        const int cn = min(32, np - c0);
-        const float* acc = p.part_acc + (u0 + c0) * D + lane * E;
-#pragma unroll 4
-        for (int j = 0; j < cn; ++j) {
-            const float wj = __shfl_sync(0xffffffffu, w, j);
-            if constexpr (E == 4) {
-                const float4 a = *reinterpret_cast<const float4*>(acc + (size_t)j * D);
-                o[0] = fmaf(wj, a.x, o[0]); o[1] = fmaf(wj, a.y, o[1]);
-                o[2] = fmaf(wj, a.z, o[2]); o[3] = fmaf(wj, a.w, o[3]);
-            } else {
-                const float2 a = *reinterpret_cast<const float2*>(acc + (size_t)j * D);
-                o[0] = fmaf(wj, a.x, o[0]); o[1] = fmaf(wj, a.y, o[1]);
-            }
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-    const float f = lsum > 0.f ? p.out_scale / lsum : 0.f;
+    float o[E];
+    const float L = merge_partitions<D>(p.part_ml + 2 * u0, p.part_acc + u0 * D, np, lane, o);
+    const float f = L > 0.f ? p.out_scale / L : 0.f;
     const size_t ob = ((size_t)s * p.Hq + h) * D + lane * E;
 #pragma unroll
     for (int k = 0; k < E; ++k) store_elem<QF>(p.out, ob + k, o[k] * f);
 }
-
-// The same merge for sequences with many partitions: one CTA of D threads
-// per (query head, sequence); thread e owns output element e.  The weights 2^(m_p - M) of a
-// chunk of D partitions are computed once into shared memory, then every
-// thread sums its column of acc over the chunk with independent loads.
-// Sequences that fit one partition were finished by the decode kernel.
-// Launched as a programmatic dependent of the decode kernel: it waits for
-// the decode's results before reading them.
-template <int D, typename QF>
-__global__ void __launch_bounds__(D) decode_reduce_long_kernel(DecodeParams p) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int h = blockIdx.x, s = blockIdx.y, e = threadIdx.x;
-    int n = p.context_lens[s];
-    n = n < 0 ? 0 : min(n, p.max_ctx);     // same clamp as the decode kernel: np <= Pmax
-    const int np = n > 0 ? (n + p.P - 1) / p.P : 1;
-    if (np <= 1) return;
-    const size_t u0 = ((size_t)s * p.Hq + h) * p.Pmax;
-    __shared__ float w_s[D];
-    __shared__ float red[D / 32];
-    // M = max over partitions
-    float mx = -CUDART_INF_F;
-    for (int i = e; i < np; i += D) mx = fmaxf(mx, p.part_ml[2 * (u0 + i)]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if ((e & 31) == 0) red[e >> 5] = mx;
-    __syncthreads();
-    float M = red[0];
-#pragma unroll
-    for (int i = 1; i < D / 32; ++i) M = fmaxf(M, red[i]);
-    __syncthreads();
-    float lsum = 0.f, o = 0.f;
-    for (int c0 = 0; c0 < np; c0 += D) {
-        const int cn = min(D, np - c0);
-        if (e < cn) {
-            const float m = p.part_ml[2 * (u0 + c0 + e)];
-            const float w = m == -CUDART_INF_F ? 0.f : exp2f(m - M);
-            w_s[e] = w;
-            lsum = fmaf(w, p.part_ml[2 * (u0 + c0 + e) + 1], lsum);
-        }
-        __syncthreads();
-        const float* acc = p.part_acc + (u0 + c0) * D + e;
-        int j = 0;
-        for (; j + 4 <= cn; j += 4) {
-            const float a0 = acc[(size_t)j * D], a1 = acc[(size_t)(j + 1) * D];
-            const float a2 = acc[(size_t)(j + 2) * D], a3 = acc[(size_t)(j + 3) * D];
-            o = fmaf(w_s[j], a0, o);
-            o = fmaf(w_s[j + 1], a1, o);
-            o = fmaf(w_s[j + 2], a2, o);
-            o = fmaf(w_s[j + 3], a3, o);
-        }
-        for (; j < cn; ++j) o = fmaf(w_s[j], acc[(size_t)j * D], o);
-        __syncthreads();
-    }
-    // L = sum of every thread's share
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-    if ((e & 31) == 0) red[e >> 5] = lsum;
-    __syncthreads();
-    float L = 0.f;
-#pragma unroll
-    for (int i = 0; i < D / 32; ++i) L += red[i];
-    store_elem<QF>(p.out, ((size_t)s * p.Hq + h) * D + e, L > 0.f ? o / L * p.out_scale : 0.f);
-}
-
-// Sequences that may span this many partitions or more are merged by a
-// whole CTA per query head; fewer, by one warp per query head.
-constexpr int kLongMerge = 32;
 
 template <int D, typename QF>
 cudaError_t launch_reduce(const DecodeParams& p, cudaStream_t st) {
@@ -296,11 +200,6 @@ cudaError_t launch_reduce(const DecodeParams& p, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (p.Pmax >= kLongMerge) {
-        cfg.gridDim = dim3(p.Hq, p.S);
-        cfg.blockDim = dim3(D);
-        return cudaLaunchKernelEx(&cfg, decode_reduce_long_kernel<D, QF>, p);
-    }
     const long long warps = (long long)p.S * p.Hq;
     cfg.gridDim = dim3((unsigned)((warps + kMergeWarps - 1) / kMergeWarps));
     cfg.blockDim = dim3(kMergeWarps * 32);

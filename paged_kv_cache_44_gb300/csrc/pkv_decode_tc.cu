@@ -202,6 +202,8 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
     auto lds128 = [&](uint32_t a) { return *reinterpret_cast<const uint4*>(ws + (a - ws_addr)); };
     auto lds64 = [&](uint32_t a) { return *reinterpret_cast<const uint2*>(ws + (a - ws_addr)); };
 
+    // the partition merge that may follow can be scheduled now; it waits for this grid's results
+    asm volatile("griddepcontrol.launch_dependents;");
     if (lane == 0) {
         // through a token table every lane's copies arrive on the stage barrier, and lane 0 once more
         for (int i = 0; i < C::kStages; ++i) mbar_init(bar(i), TT ? 33 : 1);

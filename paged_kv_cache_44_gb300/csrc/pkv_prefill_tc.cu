@@ -30,6 +30,7 @@
 
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
+#include "pkv_merge.cuh"
 #include "pkv_qtile.cuh"
 #include "pkv_tc_common.cuh"
 
@@ -83,6 +84,8 @@ __global__ void __launch_bounds__(kPWarps * 32, 1)
     auto bar = [&](int i) { return ctl_addr + 8 * i; };
     auto stage_k = [&](int i) { return ws_addr + i * C::kStageBytes; };
     auto stage_v = [&](int i) { return ws_addr + i * C::kStageBytes + C::kPartBytes; };
+    // the partition merge that may follow can be scheduled now; it waits for this grid's results
+    asm volatile("griddepcontrol.launch_dependents;");
 
     if (lane == 0) {
         for (int i = 0; i < kPStages; ++i) mbar_init(bar(i), 1);
@@ -402,14 +405,15 @@ __global__ void __launch_bounds__(kPWarps * 32, 1)
     }
 }
 
-// Merge of a query's partitions, one warp per (query token, head): the
-// token's sequence by binary search over query_start, its tile's partition
-// count from the same formula the decode units use.  Launched as a
-// programmatic dependent of the prefill kernel.
+// Merge of a query's partitions, one warp per (query token, head)
+// (merge_partitions): the token's sequence by binary search over
+// query_start, its tile's partition count from the same formula the decode
+// units use.  Launched as a programmatic dependent of the prefill kernel;
+// the lengths and query offsets are inputs of that kernel, so they are read
+// before waiting for its results.
 template <int D>
 __global__ void __launch_bounds__(256) prefill_merge_kernel(DecodeParams p, const int32_t* __restrict__ query_start,
                                                             int T, int tile_rows, int max_q) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr int E = D / 32;
     const int lane = threadIdx.x & 31;
     const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -430,33 +434,11 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(DecodeParams p, cons
     const int key_end = n - ql + last_row / p.g + 1;
     const int np = (key_end + p.P - 1) / p.P;
     if (np <= 1) return;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t u0 = ((size_t)tq * p.Hq + h) * p.Pmax;
-    float mx = -CUDART_INF_F;
-    for (int i = lane; i < np; i += 32) mx = fmaxf(mx, p.part_ml[2 * (u0 + i)]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    float lsum = 0.f, acc[E];
-#pragma unroll
-    for (int k = 0; k < E; ++k) acc[k] = 0.f;
-    for (int c0 = 0; c0 < np; c0 += 32) {
-        const int i = c0 + lane;
-        float w = 0.f;
-        if (i < np) {
-            const float m = p.part_ml[2 * (u0 + i)];
-            w = m == -CUDART_INF_F ? 0.f : exp2f(m - mx);
-            lsum = fmaf(w, p.part_ml[2 * (u0 + i) + 1], lsum);
-        }
-        const int cn = min(32, np - c0);
-        const float* a = p.part_acc + (u0 + c0) * D + lane * E;
-        for (int j = 0; j < cn; ++j) {
-            const float wj = __shfl_sync(0xffffffffu, w, j);
-#pragma unroll
-            for (int k = 0; k < E; ++k) acc[k] = fmaf(wj, a[(size_t)j * D + k], acc[k]);
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-    const float f = lsum > 0.f ? 1.f / lsum : 0.f;
+    float acc[E];
+    const float L = merge_partitions<D>(p.part_ml + 2 * u0, p.part_acc + u0 * D, np, lane, acc);
+    const float f = L > 0.f ? 1.f / L : 0.f;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + ((size_t)tq * p.Hq + h) * D + lane * E;
 #pragma unroll
     for (int k = 0; k < E; ++k) out[k] = __float2bfloat16_rn(acc[k] * f);

@@ -125,6 +125,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto vtile = [&](uint32_t j) { return base + C::kVOff + (j % NV) * C::kItemBytes; };
     auto qbuf = [&](int b) { return base + C::kQOff + b * C::kQBytes; };
     auto bar = [&](uint32_t off, int i) { return ctl + off + 8 * i; };
+    // the partition merge that may follow can be scheduled now; it waits for this grid's results
+    asm volatile("griddepcontrol.launch_dependents;");
 
     if (tid == 0) {
         for (int i = 0; i < NK; ++i) {

@@ -84,6 +84,8 @@ SWEEP = [
     ("bf16", "bf16", 128, 16, 12, 2), ("bf16", "bf16", 64, 32, 16, 2), ("bf16", "bf16", 128, 16, 8, 8),
     ("bf16", "bf16", 128, 32, 28, 4), ("bf16", "f32", 128, 16, 8, 1),
     ("e4m3", "bf16", 128, 16, 28, 4), ("e4m3", "bf16", 128, 32, 7, 1), ("e4m3", "f32", 64, 16, 4, 4),
+    # more than 8 query heads per K/V head: several head sets, the last one short
+    ("bf16", "bf16", 128, 16, 32, 2), ("e4m3", "bf16", 64, 16, 12, 1),
 ]
 
 
@@ -112,6 +114,31 @@ def test_decode_sweep(cfg):
             out = gpu_decode(c, partition_size=P, kernel=kernel)
             assert_close(out, ref, w.cache_dtype, f"{kernel} P={P}")
             assert (out[0] == 0).all()
+
+
+@pytest.mark.parametrize("cfg", [("bf16", "bf16", 128, 16, 28, 4), ("e4m3", "bf16", 64, 32, 12, 1)],
+                         ids=["bf16-g7", "e4m3-g12"])
+def test_split_decode_reuses_workspace(cfg):
+    """A split decode leaves the workspace's scheduling header zero, so one
+    workspace serves call after call, with bit-identical results."""
+    w = _sweep_workload(*cfg, seed=77)
+    c = build_case(w)
+    ref = oracle_decode(c)
+    for P in (w.bs, 64, 512):
+        ws = pkv.make_workspace(w.S, w.Hq, w.Hkv, w.d, w.bs, w.max_context_len, P)
+        zero = 256
+        outs = []
+        for _ in range(3):
+            out = torch.empty_like(c.q)
+            pkv.paged_attention_decode(out, c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens,
+                                       w.max_context_len, scale=w.scale, k_scale=c.k_scale, v_scale=c.v_scale,
+                                       partition_size=P, workspace=ws, kernel="tensor_cores")
+            torch.cuda.synchronize()
+            assert int(ws[:zero].count_nonzero()) == 0, f"P={P}: scheduling state left behind"
+            outs.append(out)
+        assert_close(outs[0], ref, w.cache_dtype, f"P={P}")
+        for o in outs[1:]:
+            assert torch.equal(o, outs[0])
 
 
 # ---------------------------------------------------------------- invariance
