@@ -109,7 +109,7 @@ PKV_API pkv_status pkv_paged_kv_write(const void* key, const void* value, pkv_dt
  * this partition request (see below); 0 for invalid arguments.  The
  * workspace holds a 256-byte scheduling header and, when a sequence may span
  * several partitions, one (max, sum, weighted sum) triple per (sequence,
- * query head, partition).  The header must be zero before a workspace is
+ * query head, partition or chunk; see below).  The header must be zero before a workspace is
  * first used (every decode leaves it zero when it completes, so zero-filling
  * once at allocation is enough).  One workspace must not be used by two
  * decodes that may run at the same time.
@@ -147,7 +147,11 @@ PKV_API int pkv_decode_partition_size(int S, int Hq, int Hkv, int d, int bs,
  * Long contexts are split into partitions of `partition_size` tokens
  * (a multiple of bs): each partition keeps its own running max and sum, and
  * a second pass merges them (M = max m_p, L = sum e^(m_p - M) l_p,
- * O = sum e^(m_p - M) acc_p / L).  partition_size: 0 = library choice,
+ * O = sum e^(m_p - M) acc_p / L).  When a decode is split, each sequence's
+ * last, partial partition is processed in chunks of a quarter partition
+ * (rounded down to a multiple of 32 tokens; partitions under 128 tokens are
+ * not cut), which are merged like partitions: the launch then ends on small
+ * pieces of work.  partition_size: 0 = library choice,
  * -1 = never split, > 0 = that size.  When any sequence may span more than
  * one partition, `workspace` must hold pkv_decode_workspace_size(...) bytes,
  * else PKV_ERR_WORKSPACE is returned.

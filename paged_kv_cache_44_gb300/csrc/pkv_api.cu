@@ -44,13 +44,32 @@ int resolve_partition(int S, int Hq, int Hkv, int d, int bs, int max_ctx, int re
     return P;
 }
 
+// The last, partial partition of a sequence is cut into chunks of Q tokens
+// (a quarter partition, a multiple of 32 tokens and so of the block size):
+// those chunks are the last units a launch hands out, so the launch ends on
+// small units instead of on whichever partial partitions happened to be large.
+int tail_chunk(int P) { return P >= 128 ? (P / 4) / 32 * 32 : P; }
+
+// Partial results per row for lengths up to max_ctx: a sequence of n tokens
+// has n / P full partitions and ceil((n % P) / Q) chunks; the count is
+// largest at max_ctx or just below its last multiple of P.
+int max_partitions(int max_ctx, int P, int Q) {
+    const int F = max_ctx / P, R = max_ctx - F * P;
+    int m = F + (R + Q - 1) / Q;
+    if (F >= 1) m = m > F - 1 + (P - 1 + Q - 1) / Q ? m : F - 1 + (P - 1 + Q - 1) / Q;
+    return m > 1 ? m : 1;
+}
+
 DecodePlan make_plan(int S, int Hq, int d, int max_ctx, int P) {
     DecodePlan pl{};
     pl.P = P;
+    pl.Q = P;
     pl.Pmax = P > 0 ? (max_ctx > 0 ? (max_ctx + P - 1) / P : 1) : 1;
     pl.split = P > 0 && pl.Pmax > 1;
     pl.bytes = kWorkspaceHeaderBytes;
     if (!pl.split) return pl;
+    pl.Q = tail_chunk(P);
+    pl.Pmax = max_partitions(max_ctx, P, pl.Q);
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     const size_t units = (size_t)S * Hq * pl.Pmax;
     pl.ml_offset = kWorkspaceHeaderBytes;
@@ -171,6 +190,7 @@ pkv_status pkv_paged_attention_decode_ex(void* out, const void* query, pkv_dtype
     p.block_tables = block_tables; p.context_lens = context_lens; p.err = err_word;
     p.S = S; p.MB = MB; p.Hq = Hq; p.Hkv = Hkv; p.g = Hq / Hkv; p.d = d; p.bs = bs; p.NB = NB;
     p.P = pl.P > 0 ? pl.P : MB * bs;      // no split: one partition covers the whole table
+    p.Q = pl.P > 0 ? pl.Q : p.P;
     p.Pmax = pl.Pmax;
     p.max_ctx = max_context_len;
     const float ks = cache_dtype == PKV_FP8_E4M3 ? k_scale : 1.f;
@@ -231,6 +251,7 @@ pkv_status pkv_paged_kv_write_decode(void* out, const void* query, pkv_dtype q_d
     p.block_tables = block_tables; p.context_lens = context_lens; p.err = err_word;
     p.S = S; p.MB = MB; p.Hq = Hq; p.Hkv = Hkv; p.g = Hq / Hkv; p.d = d; p.bs = bs; p.NB = NB;
     p.P = pl.P > 0 ? pl.P : MB * bs;
+    p.Q = pl.P > 0 ? pl.Q : p.P;
     p.Pmax = pl.Pmax;
     p.max_ctx = max_context_len;
     const float ks = cache_dtype == PKV_FP8_E4M3 ? k_scale : 1.f;
@@ -287,6 +308,7 @@ pkv_status pkv_token_attention_decode(void* out, const void* query, pkv_dtype q_
     p.token_slots = token_slots; p.MT = MT; p.context_lens = num_tokens; p.err = err_word;
     p.S = S; p.MB = 1; p.Hq = Hq; p.Hkv = Hkv; p.g = Hq / Hkv; p.d = d; p.bs = bs; p.NB = NB;
     p.P = pl.P > 0 ? pl.P : (max_tokens > 0 ? max_tokens : 1);
+    p.Q = pl.P > 0 ? pl.Q : p.P;
     p.Pmax = pl.Pmax;
     p.max_ctx = max_tokens;
     const float ks = cache_dtype == PKV_FP8_E4M3 ? k_scale : 1.f;
@@ -445,6 +467,7 @@ pkv_status pkv_paged_attention_prefill_ex(void* out, const void* query, pkv_dtyp
     p.block_tables = block_tables; p.context_lens = context_lens; p.err = err_word;
     p.S = S; p.MB = MB; p.Hq = Hq; p.Hkv = Hkv; p.g = Hq / Hkv; p.d = d; p.bs = bs; p.NB = NB;
     p.P = pl.P > 0 ? pl.P : MB * bs;
+    p.Q = p.P;                            // query chunks: whole partitions only
     p.Pmax = pl.Pmax;
     p.max_ctx = max_context_len;
     p.logit_scale_log2 = scale * kLog2e;

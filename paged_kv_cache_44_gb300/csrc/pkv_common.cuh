@@ -20,6 +20,27 @@ __device__ __forceinline__ void report(int32_t* err, int code) {
     if (err != nullptr) atomicCAS(err, 0, code);
 }
 
+// Split-K layout of a sequence of n tokens: n / P full partitions of P
+// tokens, then the remainder cut into chunks of Q tokens (Q = P: one partial
+// partition); a sequence with no tokens has one, empty, partition.
+__device__ __forceinline__ int num_partitions(int n, int P, int Q) {
+    if (n <= 0) return 1;
+    const int full = n / P;
+    return full + (n - full * P + Q - 1) / Q;
+}
+
+// Tokens [t0, t1) of partition `part` of a sequence of n tokens.
+__device__ __forceinline__ void partition_range(int n, int P, int Q, int part, int& t0, int& t1) {
+    const int full = n / P;
+    if (part < full) {
+        t0 = part * P;
+        t1 = t0 + P;
+    } else {
+        t0 = full * P + (part - full) * Q;
+        t1 = min(t0 + Q, n);
+    }
+}
+
 // ---- scalar element -> float (fp8: the code's value, scale applied by caller)
 
 __device__ __forceinline__ float to_float(float x) { return x; }

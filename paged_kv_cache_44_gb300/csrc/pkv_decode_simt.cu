@@ -44,9 +44,10 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
         if (part == 0 && blockIdx.y == 0 && threadIdx.x == 0) report(p.err, PKV_DEVERR_CONTEXT_LEN);
         n = n < 0 ? 0 : p.max_ctx;
     }
-    const int np = n > 0 ? (n + p.P - 1) / p.P : 1;
+    const int np = num_partitions(n, p.P, p.Q);
     if (part >= np) return;
-    const int t0 = part * p.P, t1 = min(n, t0 + p.P);
+    int t0, t1;
+    partition_range(n, p.P, p.Q, part, t0, t1);
 
     __shared__ float q_s[kHeads][D];
     __shared__ float x_s[kHeads][kChunk];
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_reduce_kernel(DecodeP
     const int s = (int)(gw / p.Hq), h = (int)(gw % p.Hq);
     int n = p.context_lens[s];
     n = n < 0 ? 0 : min(n, p.max_ctx);     // same clamp as the decode kernel: np <= Pmax
-    const int np = n > 0 ? (n + p.P - 1) / p.P : 1;
+    const int np = num_partitions(n, p.P, p.Q);
     if (np <= 1) return;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t u0 = ((size_t)s * p.Hq + h) * p.Pmax;

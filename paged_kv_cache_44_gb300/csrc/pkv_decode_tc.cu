@@ -130,18 +130,19 @@ struct __align__(16) Unit {
 //   A: every full partition (P tokens), partition-major -- the same
 //      partition of every sequence is claimed close together in time, so
 //      shared prefix blocks are read while still in L2;
-//   B: each sequence's last, partial partition (fewer than P tokens, or the
-//      empty one of a sequence with no tokens).
+//   B: the chunks (Q tokens) of each sequence's last, partial partition,
+//      chunk-major (and the empty unit of a sequence with no tokens).
 // Claimed in id order, the long units go first and the short ones last, so
 // the tail of the launch is short.  Returns false for ids that name no
-// work (a partition past the sequence's full ones, or no partial part).
+// work (a partition past the sequence's full ones, or a chunk past its
+// remainder).
 __device__ __forceinline__ bool unit_of(const DecodeParams& p, unsigned long long u, int nsets,
                                         unsigned long long region_a, Unit& x) {
     const unsigned long long per_part = (unsigned long long)p.S * p.Hkv * nsets;
     const bool in_a = u < region_a;
     const unsigned long long v = in_a ? u : u - region_a;
-    const int part_a = (int)(v / per_part);
-    const unsigned long long rem = v - (unsigned long long)part_a * per_part;
+    const int idx = (int)(v / per_part);                  // partition (A) or chunk (B) index
+    const unsigned long long rem = v - (unsigned long long)idx * per_part;
     x.s = (int)(rem / (unsigned)(p.Hkv * nsets));
     const int r2 = (int)(rem - (unsigned long long)x.s * (p.Hkv * nsets));
     x.kvh = r2 / nsets;
@@ -150,22 +151,19 @@ __device__ __forceinline__ bool unit_of(const DecodeParams& p, unsigned long lon
     x.nh = min(kHeadsPerUnit, p.g - set * kHeadsPerUnit);
     int n = __ldg(p.context_lens + x.s);
     if (n < 0 || n > p.max_ctx) {
-        if (!in_a && r2 == 0) report(p.err, PKV_DEVERR_CONTEXT_LEN);
+        if (!in_a && idx == 0 && r2 == 0) report(p.err, PKV_DEVERR_CONTEXT_LEN);
         n = n < 0 ? 0 : p.max_ctx;
     }
-    x.np = n > 0 ? (n + p.P - 1) / p.P : 1;
+    x.np = num_partitions(n, p.P, p.Q);
     const int full = n / p.P;
     if (in_a) {
-        if (part_a >= full) return false;
-        x.part = part_a;
-        x.t0 = part_a * p.P;
-        x.t1 = x.t0 + p.P;
+        if (idx >= full) return false;
+        x.part = idx;
     } else {
-        if (n > 0 && n == full * p.P) return false;      // no partial partition
-        x.part = full;
-        x.t0 = full * p.P;
-        x.t1 = n;
+        if (n == 0 ? idx > 0 : full * p.P + idx * p.Q >= n) return false;   // past the remainder
+        x.part = full + idx;
     }
+    partition_range(n, p.P, p.Q, x.part, x.t0, x.t1);
     return true;
 }
 
@@ -762,7 +760,8 @@ cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t st) {
     const int nsets = (p.g + kHeadsPerUnit - 1) / kHeadsPerUnit;
     const unsigned long long per_part = (unsigned long long)p.S * p.Hkv * nsets;
     const unsigned long long region_a = (unsigned long long)(p.max_ctx / p.P) * per_part;   // full partitions
-    const unsigned long long units = region_a + per_part;                               // + partial ones
+    const int chunks = (p.P - 1 + p.Q - 1) / p.Q;                  // chunks of the longest remainder
+    const unsigned long long units = region_a + (unsigned long long)(chunks > 0 ? chunks : 1) * per_part;
     unsigned long long want = (units + C::kWarps - 1) / C::kWarps;
     int grid = (int)(want < (unsigned long long)num_sms ? want : (unsigned long long)num_sms);
     if (grid < 1) grid = 1;

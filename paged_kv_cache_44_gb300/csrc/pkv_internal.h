@@ -61,7 +61,8 @@ struct DecodeParams {
     int S, MB, Hq, Hkv, g, d, bs, NB;
     int MT;               // row length of token_slots
     int P;                // tokens per partition (> 0)
-    int Pmax;             // partitions of the longest sequence
+    int Q;                // a sequence's last, partial partition is cut into chunks of Q tokens (Q <= P)
+    int Pmax;             // partitions (and chunks) of the longest sequence: partial results per row
     int max_ctx;
     float logit_scale_log2;   // scale * k_scale * log2(e)
     float out_scale;          // v_scale for E4M3 caches, else 1
@@ -78,6 +79,7 @@ struct DecodeParams {
 // Resolved layout of the decode workspace.
 struct DecodePlan {
     int P;            // tokens per partition; 0 = one partition per sequence
+    int Q;            // chunk of the last, partial partition (= P when not split)
     int Pmax;
     bool split;       // a reduce pass is needed
     size_t ml_offset, acc_offset, bytes;
