@@ -20,6 +20,24 @@ __device__ __forceinline__ void report(int32_t* err, int code) {
     if (err != nullptr) atomicCAS(err, 0, code);
 }
 
+// L2 eviction priorities for the split-K partial results: the decode writes
+// them with "evict last", so that the K/V streaming through L2 does not push
+// them out before the merge, which reads each of them once with "evict
+// first".  (PTX createpolicy / .L2::cache_hint, sm_80 and later.)
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void st_l2_hint(float* p, float v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
+}
+
 // Split-K layout of a sequence of n tokens: n / P full partitions of P
 // tokens, then the remainder cut into chunks of Q tokens (Q = P: one partial
 // partition); a sequence with no tokens has one, empty, partition.

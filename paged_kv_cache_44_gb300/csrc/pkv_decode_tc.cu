@@ -130,12 +130,13 @@ struct __align__(16) Unit {
 //   A: every full partition (P tokens), partition-major -- the same
 //      partition of every sequence is claimed close together in time, so
 //      shared prefix blocks are read while still in L2;
-//   B: the chunks (Q tokens) of each sequence's last, partial partition,
-//      chunk-major (and the empty unit of a sequence with no tokens).
+//   B: the chunks of each sequence's last, partial partition: first every
+//      full-size chunk (Q tokens), chunk-major, then each sequence's
+//      shorter last chunk (and the empty unit of a sequence with no tokens).
 // Claimed in id order, the long units go first and the short ones last, so
 // the tail of the launch is short.  Returns false for ids that name no
-// work (a partition past the sequence's full ones, or a chunk past its
-// remainder).
+// work (a partition past the sequence's full ones, a chunk past its
+// remainder, or a last chunk that does not exist).
 __device__ __forceinline__ bool unit_of(const DecodeParams& p, unsigned long long u, int nsets,
                                         unsigned long long region_a, Unit& x) {
     const unsigned long long per_part = (unsigned long long)p.S * p.Hkv * nsets;
@@ -156,12 +157,18 @@ __device__ __forceinline__ bool unit_of(const DecodeParams& p, unsigned long lon
     }
     x.np = num_partitions(n, p.P, p.Q);
     const int full = n / p.P;
+    const int tail = n - full * p.P;
+    const int cfull = (p.P - 1) / p.Q;                     // full-size chunks of the longest remainder
     if (in_a) {
         if (idx >= full) return false;
         x.part = idx;
-    } else {
-        if (n == 0 ? idx > 0 : full * p.P + idx * p.Q >= n) return false;   // past the remainder
+    } else if (idx < cfull) {
+        if ((idx + 1) * p.Q > tail) return false;          // full-size chunks first
         x.part = full + idx;
+    } else {
+        if (idx > cfull) return false;
+        if (n > 0 && tail % p.Q == 0) return false;        // then the remainder's partial chunk
+        x.part = full + tail / p.Q;
     }
     partition_range(n, p.P, p.Q, x.part, x.t0, x.t1);
     return true;
@@ -670,6 +677,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
                     if (wB) { store_out<QF>(p, oB + d0, o[t][1] * fB); store_out<QF>(p, oB + d1, o[t][3] * fB); }
                 }
             } else {
+                const uint64_t keep = l2_policy_evict_last();   // held in L2 until the merge reads it
                 const size_t uA = ((size_t)cu.s * p.Hq + cu.h0 + hA) * p.Pmax + cu.part;
                 const size_t uB = uA + p.Pmax;
 #pragma unroll
@@ -677,12 +685,12 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
                     int d0, d1;
                     if constexpr (FP8) { d0 = (D / 8) * r + 2 * t; d1 = d0 + 1; }
                     else { d0 = 16 * t + r; d1 = d0 + 8; }
-                    if (wA) { p.part_acc[uA * D + d0] = o[t][0]; p.part_acc[uA * D + d1] = o[t][2]; }
-                    if (wB) { p.part_acc[uB * D + d0] = o[t][1]; p.part_acc[uB * D + d1] = o[t][3]; }
+                    if (wA) { st_l2_hint(p.part_acc + uA * D + d0, o[t][0], keep); st_l2_hint(p.part_acc + uA * D + d1, o[t][2], keep); }
+                    if (wB) { st_l2_hint(p.part_acc + uB * D + d0, o[t][1], keep); st_l2_hint(p.part_acc + uB * D + d1, o[t][3], keep); }
                 }
                 if (r == 0) {
-                    if (wA) { p.part_ml[2 * uA] = m_run[0]; p.part_ml[2 * uA + 1] = l0; }
-                    if (wB) { p.part_ml[2 * uB] = m_run[1]; p.part_ml[2 * uB + 1] = l1; }
+                    if (wA) { st_l2_hint(p.part_ml + 2 * uA, m_run[0], keep); st_l2_hint(p.part_ml + 2 * uA + 1, l0, keep); }
+                    if (wB) { st_l2_hint(p.part_ml + 2 * uB, m_run[1], keep); st_l2_hint(p.part_ml + 2 * uB + 1, l1, keep); }
                 }
             }
             have_unit = false;
@@ -760,8 +768,8 @@ cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t st) {
     const int nsets = (p.g + kHeadsPerUnit - 1) / kHeadsPerUnit;
     const unsigned long long per_part = (unsigned long long)p.S * p.Hkv * nsets;
     const unsigned long long region_a = (unsigned long long)(p.max_ctx / p.P) * per_part;   // full partitions
-    const int chunks = (p.P - 1 + p.Q - 1) / p.Q;                  // chunks of the longest remainder
-    const unsigned long long units = region_a + (unsigned long long)(chunks > 0 ? chunks : 1) * per_part;
+    const int cfull = (p.P - 1) / p.Q;                               // full-size chunks, then one partial
+    const unsigned long long units = region_a + (unsigned long long)(cfull + 1) * per_part;
     unsigned long long want = (units + C::kWarps - 1) / C::kWarps;
     int grid = (int)(want < (unsigned long long)num_sms ? want : (unsigned long long)num_sms);
     if (grid < 1) grid = 1;

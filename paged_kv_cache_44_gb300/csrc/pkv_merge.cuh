@@ -13,20 +13,27 @@
 #include <math_constants.h>
 
 #include <cstddef>
+#include <cstdint>
+
+#include "pkv_common.cuh"
 
 namespace pkv {
 
 constexpr int kMergeChunk = 16;
 
+// One row's E elements of this lane, read through L2 (ld.global.cg) with an
+// "evict first" hint: each partial result is read exactly once.
 template <int E>
-__device__ __forceinline__ void merge_load_row(const float* src, float (&a)[E]) {
+__device__ __forceinline__ void merge_load_row(const float* src, float (&a)[E], uint64_t pol) {
     if constexpr (E == 4) {
-        const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
-        a[0] = x.x; a[1] = x.y; a[2] = x.z; a[3] = x.w;
+        asm volatile("ld.global.cg.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+                     : "=f"(a[0]), "=f"(a[1]), "=f"(a[2]), "=f"(a[3])
+                     : "l"(src), "l"(pol));
     } else {
         static_assert(E == 2, "rows of 64 or 128 elements");
-        const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
-        a[0] = x.x; a[1] = x.y;
+        asm volatile("ld.global.cg.L2::cache_hint.v2.f32 {%0, %1}, [%2], %3;"
+                     : "=f"(a[0]), "=f"(a[1])
+                     : "l"(src), "l"(pol));
     }
 }
 
@@ -38,6 +45,7 @@ template <int D>
 __device__ __forceinline__ float merge_partitions(const float* __restrict__ ml, const float* __restrict__ acc,
                                                   int np, int lane, float (&o)[D / 32]) {
     constexpr int E = D / 32, B = kMergeChunk;
+    const uint64_t once = l2_policy_evict_first();
     float M = -CUDART_INF_F, lpart = 0.f;
 #pragma unroll
     for (int k = 0; k < E; ++k) o[k] = 0.f;
@@ -45,15 +53,15 @@ __device__ __forceinline__ float merge_partitions(const float* __restrict__ ml, 
         const int cn = min(B, np - c0);
         float m = -CUDART_INF_F, l = 0.f;
         if (lane < cn) {
-            const float2 x = __ldcg(reinterpret_cast<const float2*>(ml) + c0 + lane);
-            m = x.x;
-            l = x.y;
+            asm volatile("ld.global.cg.L2::cache_hint.v2.f32 {%0, %1}, [%2], %3;"
+                         : "=f"(m), "=f"(l)
+                         : "l"(reinterpret_cast<const float2*>(ml) + c0 + lane), "l"(once));
         }
         float a[B][E];
 #pragma unroll
         for (int j = 0; j < B; ++j) {
             if (j < cn) {
-                merge_load_row<E>(acc + (size_t)(c0 + j) * D + lane * E, a[j]);
+                merge_load_row<E>(acc + (size_t)(c0 + j) * D + lane * E, a[j], once);
             } else {
 #pragma unroll
                 for (int k = 0; k < E; ++k) a[j][k] = 0.f;
