@@ -427,7 +427,8 @@ def run_ours(args, w: W.Workload):
     if fused:
         launches_per_step -= 1
 
-    def step(ev0=None, ev1=None, qq=q, nk=new_k, nv=new_v, btab=bt, clen=cl, slots=sm, pairs=cow, o=out):
+    def step(ev0=None, ev1=None, qq=q, nk=new_k, nv=new_v, btab=bt, clen=cl, slots=sm, pairs=cow, o=out,
+             evw=None, evc=None):
         if fused:
             # one launch writes the new tokens and decodes (the timed "decode" includes the write)
             if ev0 is not None:
@@ -436,7 +437,11 @@ def run_ours(args, w: W.Workload):
                                       k_scale=k_scale, v_scale=v_scale, partition_size=P, workspace=wsp,
                                       stream=stream)
         else:
+            if evw is not None:
+                evw[0].record(stream)
             pkv.paged_kv_write(nk, nv, kc, vc, slots, k_scale, v_scale, stream=stream)
+            if evw is not None:
+                evw[1].record(stream)
             if ev0 is not None:
                 ev0.record(stream)
             pkv.paged_attention_decode(o, qq, kc, vc, btab, clen, mc, scale=w.scale, k_scale=k_scale,
@@ -445,7 +450,11 @@ def run_ours(args, w: W.Workload):
         if ev1 is not None:
             ev1.record(stream)
         if len(w.cow_pairs):
+            if evc is not None:
+                evc[0].record(stream)
             pkv.copy_blocks([kc], [vc], pairs, stream=stream)
+            if evc is not None:
+                evc[1].record(stream)
 
     def barrier():
         if ws > 1:
@@ -476,6 +485,16 @@ def run_ours(args, w: W.Workload):
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(dec0, dec1))
     ms_total, dec_ms = max_over_ranks([ms_total, dec_ms], dev)
     ms_step = ms_total / args.steps
+
+    # ---- the step's other calls, timed on their own (outside the timed region)
+    n_parts = max(3, min(args.steps, 200))
+    evw = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_parts)]
+    evc = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_parts)]
+    for i in range(n_parts):
+        step(evw=None if fused else evw[i], evc=evc[i] if len(w.cow_pairs) else None)
+    torch.cuda.synchronize(dev)
+    write_ms = None if fused else statistics.mean(a.elapsed_time(b) for a, b in evw)
+    copy_ms = statistics.mean(a.elapsed_time(b) for a, b in evc) if len(w.cow_pairs) else None
 
     # ---- end to end: host buffers in, host result out, through the public API
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
@@ -529,6 +548,9 @@ def run_ours(args, w: W.Workload):
                            " + copy_blocks(%d pairs)" % len(w.cow_pairs)},
         "seq_steps_per_s": round(ws * w.S / (ms_step * 1e-3), 1),
         "decode_gbs": round(achieved, 2),
+        "decode_ms": round(dec_ms, 5),
+        "write_ms": None if write_ms is None else round(write_ms, 5),
+        "copy_blocks_ms": None if copy_ms is None else round(copy_ms, 5),
         "hbm_frac_of_measured": round(achieved / peak, 4),
         "hbm_frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
@@ -548,6 +570,11 @@ def run_ours(args, w: W.Workload):
         line["cpu_baseline"] = {"value": round(b / spent / 1e9, 4), "unit": "GB/s", "cores": threads,
                                 "kind": "oracle", "sample": sampler.describe(n, spent),
                                 "seq_steps_per_s": round(sampler.seq_steps_per_s(b / spent / 1e9), 4)}
+        if threads > 1:
+            one = OracleSampler(w, 1)
+            b1, spent1, n1 = one.run(max(1.0, args.cpu_seconds / 4))
+            line["cpu_baseline"]["one_thread"] = {"value": round(b1 / spent1 / 1e9, 4), "unit": "GB/s",
+                                                  "sample": one.describe(n1, spent1)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
