@@ -151,7 +151,9 @@ PKV_API int pkv_decode_partition_size(int S, int Hq, int Hkv, int d, int bs,
  * last, partial partition is processed in chunks of a quarter partition
  * (rounded down to a multiple of 32 tokens; partitions under 128 tokens are
  * not cut), which are merged like partitions: the launch then ends on small
- * pieces of work.  partition_size: 0 = library choice,
+ * pieces of work.  With an E4M3 cache on the tensor-core kernel, a sequence
+ * of four or more full partitions has its last full partition cut into
+ * chunks too.  partition_size: 0 = library choice,
  * -1 = never split, > 0 = that size.  When any sequence may span more than
  * one partition, `workspace` must hold pkv_decode_workspace_size(...) bytes,
  * else PKV_ERR_WORKSPACE is returned.

@@ -5,6 +5,7 @@
 
 #include <mutex>
 
+#include "pkv_common.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -50,13 +51,26 @@ int resolve_partition(int S, int Hq, int Hkv, int d, int bs, int max_ctx, int re
 // small units instead of on whichever partial partitions happened to be large.
 int tail_chunk(int P) { return P >= 128 ? (P / 4) / 32 * 32 : P; }
 
-// Partial results per row for lengths up to max_ctx: a sequence of n tokens
-// has n / P full partitions and ceil((n % P) / Q) chunks; the count is
-// largest at max_ctx or just below its last multiple of P.
-int max_partitions(int max_ctx, int P, int Q) {
-    const int F = max_ctx / P, R = max_ctx - F * P;
-    int m = F + (R + Q - 1) / Q;
-    if (F >= 1) m = m > F - 1 + (P - 1 + Q - 1) / Q ? m : F - 1 + (P - 1 + Q - 1) / Q;
+// Full partitions held back into chunks at a long sequence's end
+// (num_partitions), for E4M3 caches on the tensor-core kernel: a worker
+// streams E4M3 at the pace of its own arithmetic (about 17 tokens/us, a
+// full 1024-token unit lasts ~60 us), so the units claimed last decide when
+// the launch ends, and small ones end it sooner.  On bf16 caches the same
+// layout was slower (more units and partial results for the same tail).
+constexpr int kTailHold = 1;
+int tail_hold(pkv_dtype cache_dtype, bool tensor_cores) {
+    return cache_dtype == PKV_FP8_E4M3 && tensor_cores ? kTailHold : 0;
+}
+
+// Partial results per row for lengths up to max_ctx with `hold` held-back
+// partitions: the count (num_partitions) grows with n between multiples of
+// P, so its largest value is at max_ctx, just below the last multiple of P,
+// or just below the length from which partitions are held back.
+int max_partitions(int max_ctx, int P, int Q, int hold) {
+    int m = num_partitions(max_ctx, P, Q, hold);
+    const int F = max_ctx / P;
+    if (F >= 1) m = max(m, num_partitions(F * P - 1, P, Q, hold));
+    m = max(m, num_partitions(min(max_ctx, kTailHoldMin * P - 1), P, Q, hold));
     return m > 1 ? m : 1;
 }
 
@@ -65,11 +79,14 @@ DecodePlan make_plan(int S, int Hq, int d, int max_ctx, int P) {
     pl.P = P;
     pl.Q = P;
     pl.Pmax = P > 0 ? (max_ctx > 0 ? (max_ctx + P - 1) / P : 1) : 1;
+    pl.Pmax_plain = pl.Pmax;
     pl.split = P > 0 && pl.Pmax > 1;
     pl.bytes = kWorkspaceHeaderBytes;
     if (!pl.split) return pl;
     pl.Q = tail_chunk(P);
-    pl.Pmax = max_partitions(max_ctx, P, pl.Q);
+    // the workspace fits both layouts; each launch uses its own row stride
+    pl.Pmax_plain = max_partitions(max_ctx, P, pl.Q, 0);
+    pl.Pmax = max(pl.Pmax_plain, max_partitions(max_ctx, P, pl.Q, kTailHold));
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     const size_t units = (size_t)S * Hq * pl.Pmax;
     pl.ml_offset = kWorkspaceHeaderBytes;
@@ -191,7 +208,8 @@ pkv_status pkv_paged_attention_decode_ex(void* out, const void* query, pkv_dtype
     p.S = S; p.MB = MB; p.Hq = Hq; p.Hkv = Hkv; p.g = Hq / Hkv; p.d = d; p.bs = bs; p.NB = NB;
     p.P = pl.P > 0 ? pl.P : MB * bs;      // no split: one partition covers the whole table
     p.Q = pl.P > 0 ? pl.Q : p.P;
-    p.Pmax = pl.Pmax;
+    p.hold = tail_hold(cache_dtype, use_tc);
+    p.Pmax = p.hold ? pl.Pmax : pl.Pmax_plain;
     p.max_ctx = max_context_len;
     const float ks = cache_dtype == PKV_FP8_E4M3 ? k_scale : 1.f;
     p.logit_scale_log2 = scale * ks * kLog2e;
@@ -252,7 +270,8 @@ pkv_status pkv_paged_kv_write_decode(void* out, const void* query, pkv_dtype q_d
     p.S = S; p.MB = MB; p.Hq = Hq; p.Hkv = Hkv; p.g = Hq / Hkv; p.d = d; p.bs = bs; p.NB = NB;
     p.P = pl.P > 0 ? pl.P : MB * bs;
     p.Q = pl.P > 0 ? pl.Q : p.P;
-    p.Pmax = pl.Pmax;
+    p.hold = tail_hold(cache_dtype, true);
+    p.Pmax = p.hold ? pl.Pmax : pl.Pmax_plain;
     p.max_ctx = max_context_len;
     const float ks = cache_dtype == PKV_FP8_E4M3 ? k_scale : 1.f;
     p.logit_scale_log2 = scale * ks * kLog2e;
@@ -309,7 +328,8 @@ pkv_status pkv_token_attention_decode(void* out, const void* query, pkv_dtype q_
     p.S = S; p.MB = 1; p.Hq = Hq; p.Hkv = Hkv; p.g = Hq / Hkv; p.d = d; p.bs = bs; p.NB = NB;
     p.P = pl.P > 0 ? pl.P : (max_tokens > 0 ? max_tokens : 1);
     p.Q = pl.P > 0 ? pl.Q : p.P;
-    p.Pmax = pl.Pmax;
+    p.hold = tail_hold(cache_dtype, true);
+    p.Pmax = p.hold ? pl.Pmax : pl.Pmax_plain;
     p.max_ctx = max_tokens;
     const float ks = cache_dtype == PKV_FP8_E4M3 ? k_scale : 1.f;
     p.logit_scale_log2 = scale * ks * kLog2e;

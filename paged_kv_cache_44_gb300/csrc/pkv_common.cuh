@@ -38,23 +38,34 @@ __device__ __forceinline__ void st_l2_hint(float* p, float v, uint64_t pol) {
     asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
 }
 
-// Split-K layout of a sequence of n tokens: n / P full partitions of P
-// tokens, then the remainder cut into chunks of Q tokens (Q = P: one partial
-// partition); a sequence with no tokens has one, empty, partition.
-__device__ __forceinline__ int num_partitions(int n, int P, int Q) {
-    if (n <= 0) return 1;
+// Split-K layout of a sequence of n tokens: full partitions of P tokens,
+// then the rest cut into chunks of Q tokens (Q = P: one partial partition);
+// a sequence with no tokens has one, empty, partition.  With hold > 0 (and
+// Q < P), a sequence of at least kTailHoldMin full partitions has its last
+// `hold` full partitions cut into chunks as well: more of the work is in
+// the small units handed out last.
+constexpr int kTailHoldMin = 4;
+
+__host__ __device__ __forceinline__ int whole_partitions(int n, int P, int Q, int hold) {
     const int full = n / P;
-    return full + (n - full * P + Q - 1) / Q;
+    return Q < P && hold > 0 && full >= kTailHoldMin ? full - hold : full;
+}
+
+__host__ __device__ __forceinline__ int num_partitions(int n, int P, int Q, int hold) {
+    if (n <= 0) return 1;
+    const int fa = whole_partitions(n, P, Q, hold);
+    return fa + (n - fa * P + Q - 1) / Q;
 }
 
 // Tokens [t0, t1) of partition `part` of a sequence of n tokens.
-__device__ __forceinline__ void partition_range(int n, int P, int Q, int part, int& t0, int& t1) {
-    const int full = n / P;
-    if (part < full) {
+__host__ __device__ __forceinline__ void partition_range(int n, int P, int Q, int hold, int part, int& t0,
+                                                        int& t1) {
+    const int fa = whole_partitions(n, P, Q, hold);
+    if (part < fa) {
         t0 = part * P;
         t1 = t0 + P;
     } else {
-        t0 = full * P + (part - full) * Q;
+        t0 = fa * P + (part - fa) * Q;
         t1 = min(t0 + Q, n);
     }
 }

@@ -44,10 +44,10 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
         if (part == 0 && blockIdx.y == 0 && threadIdx.x == 0) report(p.err, PKV_DEVERR_CONTEXT_LEN);
         n = n < 0 ? 0 : p.max_ctx;
     }
-    const int np = num_partitions(n, p.P, p.Q);
+    const int np = num_partitions(n, p.P, p.Q, p.hold);
     if (part >= np) return;
     int t0, t1;
-    partition_range(n, p.P, p.Q, part, t0, t1);
+    partition_range(n, p.P, p.Q, p.hold, part, t0, t1);
 
     __shared__ float q_s[kHeads][D];
     __shared__ float x_s[kHeads][kChunk];
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_reduce_kernel(DecodeP
     const int s = (int)(gw / p.Hq), h = (int)(gw % p.Hq);
     int n = p.context_lens[s];
     n = n < 0 ? 0 : min(n, p.max_ctx);     // same clamp as the decode kernel: np <= Pmax
-    const int np = num_partitions(n, p.P, p.Q);
+    const int np = num_partitions(n, p.P, p.Q, p.hold);
     if (np <= 1) return;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t u0 = ((size_t)s * p.Hq + h) * p.Pmax;

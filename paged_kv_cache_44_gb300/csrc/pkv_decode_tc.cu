@@ -122,6 +122,13 @@ struct Cfg {
 
 // ------------------------------------------------------------------- units
 
+// Region B ids per (sequence, head set): the full-size chunks of the longest
+// remainder (hold * P + P - 1 tokens), then one for the partial chunk.
+__host__ __device__ __forceinline__ int chunk_slots(int P, int Q, int hold) {
+    const int held = Q < P ? hold : 0;
+    return (held * P + P - 1) / Q + 1;
+}
+
 struct __align__(16) Unit {
     int s, kvh, h0, nh, part, t0, t1, np;
 };
@@ -155,10 +162,10 @@ __device__ __forceinline__ bool unit_of(const DecodeParams& p, unsigned long lon
         if (!in_a && idx == 0 && r2 == 0) report(p.err, PKV_DEVERR_CONTEXT_LEN);
         n = n < 0 ? 0 : p.max_ctx;
     }
-    x.np = num_partitions(n, p.P, p.Q);
-    const int full = n / p.P;
+    x.np = num_partitions(n, p.P, p.Q, p.hold);
+    const int full = whole_partitions(n, p.P, p.Q, p.hold);
     const int tail = n - full * p.P;
-    const int cfull = (p.P - 1) / p.Q;                     // full-size chunks of the longest remainder
+    const int cfull = chunk_slots(p.P, p.Q, p.hold) - 1;           // full-size chunks of the longest remainder
     if (in_a) {
         if (idx >= full) return false;
         x.part = idx;
@@ -170,7 +177,7 @@ __device__ __forceinline__ bool unit_of(const DecodeParams& p, unsigned long lon
         if (n > 0 && tail % p.Q == 0) return false;        // then the remainder's partial chunk
         x.part = full + tail / p.Q;
     }
-    partition_range(n, p.P, p.Q, x.part, x.t0, x.t1);
+    partition_range(n, p.P, p.Q, p.hold, x.part, x.t0, x.t1);
     return true;
 }
 
@@ -768,8 +775,7 @@ cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t st) {
     const int nsets = (p.g + kHeadsPerUnit - 1) / kHeadsPerUnit;
     const unsigned long long per_part = (unsigned long long)p.S * p.Hkv * nsets;
     const unsigned long long region_a = (unsigned long long)(p.max_ctx / p.P) * per_part;   // full partitions
-    const int cfull = (p.P - 1) / p.Q;                               // full-size chunks, then one partial
-    const unsigned long long units = region_a + (unsigned long long)(cfull + 1) * per_part;
+    const unsigned long long units = region_a + (unsigned long long)chunk_slots(p.P, p.Q, p.hold) * per_part;
     unsigned long long want = (units + C::kWarps - 1) / C::kWarps;
     int grid = (int)(want < (unsigned long long)num_sms ? want : (unsigned long long)num_sms);
     if (grid < 1) grid = 1;

@@ -62,6 +62,7 @@ struct DecodeParams {
     int MT;               // row length of token_slots
     int P;                // tokens per partition (> 0)
     int Q;                // a sequence's last, partial partition is cut into chunks of Q tokens (Q <= P)
+    int hold;             // full partitions at a long sequence's end also cut into chunks (num_partitions)
     int Pmax;             // partitions (and chunks) of the longest sequence: partial results per row
     int max_ctx;
     float logit_scale_log2;   // scale * k_scale * log2(e)
@@ -80,7 +81,8 @@ struct DecodeParams {
 struct DecodePlan {
     int P;            // tokens per partition; 0 = one partition per sequence
     int Q;            // chunk of the last, partial partition (= P when not split)
-    int Pmax;
+    int Pmax;         // partial results per row the workspace holds (either layout)
+    int Pmax_plain;   // ... needed without held-back partitions
     bool split;       // a reduce pass is needed
     size_t ml_offset, acc_offset, bytes;
 };

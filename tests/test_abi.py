@@ -47,18 +47,21 @@ def test_status_strings_and_version(pkv):
 
 
 def test_workspace_plan(pkv):
-    # 72B-shaped: 32 seqs x 64 heads x 67 partial results x (128 + 2) floats
-    # + header.  A length of up to 32,768 tokens in partitions of 512 has at
-    # most 63 full partitions and 4 chunks of 128 tokens (32,767 tokens), or
-    # 64 full ones.
+    # 72B-shaped: 32 seqs x 64 heads x 70 partial results x (128 + 2) floats
+    # + header.  The workspace fits both layouts of a sequence: in partitions
+    # of 512, a length of up to 32,768 tokens has at most 63 full partitions
+    # and 4 chunks of 128 tokens (67); with its last full partition also cut
+    # into chunks (E4M3 caches, sequences of 4 or more full partitions), 62
+    # full partitions and 8 chunks (70, at 32,767 tokens).
     n = pkv.decode_workspace_size(32, 64, 8, 128, 16, 32768, 512)
-    units = 32 * 64 * 67
+    units = 32 * 64 * 70
     assert n >= 256 + units * 130 * 4
     assert n < 256 + units * 130 * 4 + 1024
     # partitions of 64 tokens are not cut further: ceil(1000 / 64) = 16 per row
     n = pkv.decode_workspace_size(4, 8, 2, 64, 16, 1000, 64)
     assert 256 + 4 * 8 * 16 * 66 * 4 <= n < 256 + 4 * 8 * 16 * 66 * 4 + 1024
     # 1,000 tokens in partitions of 256 (chunks of 64): 3 full + 4 chunks of the last 232 tokens = 7
+    # (3 full partitions are too few for one to be held back)
     n = pkv.decode_workspace_size(4, 8, 2, 64, 16, 1000, 256)
     assert 256 + 4 * 8 * 7 * 66 * 4 <= n < 256 + 4 * 8 * 7 * 66 * 4 + 1024
     # no split -> header only

@@ -110,7 +110,10 @@ def test_decode_sweep(cfg):
     ref = oracle_decode(c)
     assert (ref[0] == 0).all()
     for kernel in _kernels_for(w):
-        for P in (0, -1, w.bs, 256):
+        # 128 and 256 cut partial partitions into chunks; at 128 the longer
+        # sequences (4+ full partitions) also have their last full one cut
+        # (E4M3 caches on tensor cores)
+        for P in (0, -1, w.bs, 128, 256):
             out = gpu_decode(c, partition_size=P, kernel=kernel)
             assert_close(out, ref, w.cache_dtype, f"{kernel} P={P}")
             assert (out[0] == 0).all()
@@ -124,7 +127,7 @@ def test_split_decode_reuses_workspace(cfg):
     w = _sweep_workload(*cfg, seed=77)
     c = build_case(w)
     ref = oracle_decode(c)
-    for P in (w.bs, 64, 512):
+    for P in (w.bs, 64, 128, 512):
         ws = pkv.make_workspace(w.S, w.Hq, w.Hkv, w.d, w.bs, w.max_context_len, P)
         zero = 256
         outs = []
