@@ -396,6 +396,57 @@ def device_caches(w: W.Workload, seed: int, dev, stream):
     return caches[0], caches[1], k_scale, v_scale
 
 
+E2E_LOOP = "every step copies its inputs in and its result out (copy streams beside the compute stream); " \
+           "two steps in flight"
+
+
+def overlapped_e2e(dev, stream, h_in: dict, out_like, enqueue, steps: int, barrier=lambda: None):
+    """Seconds per step of an end-to-end loop through the public API, run as
+    a serving loop would: every step copies its inputs in from pinned host
+    memory and its result out, each copy on a stream of its own beside the
+    compute stream (step i + 1's inputs go into a second set of device
+    buffers while step i computes; step i's result comes out while step
+    i + 1 computes), and the host takes step i's result before it queues
+    step i + 2.  enqueue(d_in, d_out) queues one step on `stream`.
+    Returns (seconds per step, bytes in per step, bytes out per step)."""
+    import torch
+    d_ins = [{k: torch.empty_like(v, device=dev) for k, v in h_in.items()} for _ in range(2)]
+    d_outs = [torch.empty_like(out_like) for _ in range(2)]
+    h_outs = [torch.empty(out_like.shape, dtype=out_like.dtype, pin_memory=True) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def one(i):
+        b = i % 2
+        if i >= 2:
+            ev_out[b].synchronize()        # step i - 2's result is on the host; its buffers are free
+        with torch.cuda.stream(s_in):
+            for k in h_in:
+                d_ins[b][k].copy_(h_in[k], non_blocking=True)
+            ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        enqueue(d_ins[b], d_outs[b])
+        ev_done[b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[b])
+            h_outs[b].copy_(d_outs[b], non_blocking=True)
+            ev_out[b].record(s_out)
+
+    for i in range(2):
+        one(i)
+    torch.cuda.synchronize(dev)
+    barrier()
+    w0 = time.perf_counter()
+    for i in range(steps):
+        one(i)
+    torch.cuda.synchronize(dev)
+    secs = (time.perf_counter() - w0) / steps
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    return secs, h2d, h_outs[0].numel() * h_outs[0].element_size()
+
+
 def run_ours(args, w: W.Workload):
     import torch
     import paged_kv_cache_44_gb300 as pkv
@@ -519,51 +570,14 @@ def run_ours(args, w: W.Workload):
     write_ms = None if fused else statistics.mean(a.elapsed_time(b) for a, b in evw)
     copy_ms = statistics.mean(a.elapsed_time(b) for a, b in evc) if len(w.cow_pairs) else None
 
-    # ---- end to end: host buffers in, host result out, through the public API.  As a serving
-    # loop would: step i + 1's inputs are copied in (their own stream, their own device buffers)
-    # while step i computes, step i's result is copied out (a third stream) while step i + 1
-    # computes, and the host takes step i's result before it queues step i + 2.
+    # ---- end to end: host buffers in, host result out, through the public API
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
     h_in = {k: pin(v) for k, v in dict(q=q, nk=new_k, nv=new_v, bt=bt, cl=cl, sm=sm, cow=cow).items()}
-    d_ins = [{k: torch.empty_like(v, device=dev) for k, v in h_in.items()} for _ in range(2)]
-    d_outs = [torch.empty_like(out) for _ in range(2)]
-    h_outs = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
-    s_in = torch.cuda.Stream(device=dev)
-    s_out = torch.cuda.Stream(device=dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_done = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
-    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
-    d2h = h_outs[0].numel() * h_outs[0].element_size()
-    e2e_steps = max(3, min(args.steps, 200))
-
-    def e2e_step(i):
-        b = i % 2
-        if i >= 2:
-            ev_out[b].synchronize()        # step i - 2's result is on the host; its buffers are free
-        with torch.cuda.stream(s_in):
-            for k in h_in:
-                d_ins[b][k].copy_(h_in[k], non_blocking=True)
-            ev_in[b].record(s_in)
-        stream.wait_event(ev_in[b])
-        d = d_ins[b]
-        step(qq=d["q"], nk=d["nk"], nv=d["nv"], btab=d["bt"], clen=d["cl"], slots=d["sm"], pairs=d["cow"],
-             o=d_outs[b])
-        ev_done[b].record(stream)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_done[b])
-            h_outs[b].copy_(d_outs[b], non_blocking=True)
-            ev_out[b].record(s_out)
-
-    for i in range(2):
-        e2e_step(i)
-    torch.cuda.synchronize(dev)
-    barrier()
-    w0 = time.perf_counter()
-    for i in range(e2e_steps):
-        e2e_step(i)
-    torch.cuda.synchronize(dev)
-    e2e_s = (time.perf_counter() - w0) / e2e_steps
+    e2e_s, h2d, d2h = overlapped_e2e(
+        dev, stream, h_in, out,
+        lambda d, o: step(qq=d["q"], nk=d["nk"], nv=d["nv"], btab=d["bt"], clen=d["cl"], slots=d["sm"],
+                          pairs=d["cow"], o=o),
+        max(3, min(args.steps, 200)), barrier)
     (e2e_s,) = max_over_ranks([e2e_s], dev)
 
     # ---- numbers
@@ -602,8 +616,7 @@ def run_ours(args, w: W.Workload):
                      "algorithmic_bytes_per_launch": dbytes, "launch_ms": round(dec_ms, 5)},
         "e2e": {"value": round(whole_job_gbs(ws, sbytes, e2e_s * 1e3), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4),
-                "loop": "every step copies its inputs in and its result out (copy streams beside the "
-                        "compute stream); two steps in flight"},
+                "loop": E2E_LOOP},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
@@ -679,8 +692,8 @@ def run_prefill(args, w: W.Workload):
     split = wsb > 256
     torch.cuda.synchronize(dev)
 
-    def step(qq=q, btab=bt, clen=cl, qst=qs):
-        pkv.paged_attention_prefill(out, qq, kc, vc, btab, clen, qst, mq, mc, scale=w.scale, partition_size=P,
+    def step(qq=q, btab=bt, clen=cl, qst=qs, o=out):
+        pkv.paged_attention_prefill(o, qq, kc, vc, btab, clen, qst, mq, mc, scale=w.scale, partition_size=P,
                                     workspace=wsp, stream=stream, kernel=args.prefill_kernel)
 
     def barrier():
@@ -708,28 +721,10 @@ def run_prefill(args, w: W.Workload):
 
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
     h_in = {k: pin(v) for k, v in dict(q=q, bt=bt, cl=cl, qs=qs).items()}
-    d_in = {k: torch.empty_like(v, device=dev) for k, v in h_in.items()}
-    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
-    d2h = h_out.numel() * h_out.element_size()
-    e2e_steps = max(3, min(args.steps, 100))
-
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            for k in h_in:
-                d_in[k].copy_(h_in[k], non_blocking=True)
-        step(qq=d_in["q"], btab=d_in["bt"], clen=d_in["cl"], qst=d_in["qs"])
-        with torch.cuda.stream(stream):
-            h_out.copy_(out, non_blocking=True)
-        stream.synchronize()
-
-    for _ in range(2):
-        e2e_step()
-    barrier()
-    w0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-    (e2e_s,) = max_over_ranks([(time.perf_counter() - w0) / e2e_steps], dev)
+    e2e_s, h2d, d2h = overlapped_e2e(
+        dev, stream, h_in, out, lambda d, o: step(qq=d["q"], btab=d["bt"], clen=d["cl"], qst=d["qs"], o=o),
+        max(3, min(args.steps, 100)), barrier)
+    (e2e_s,) = max_over_ranks([e2e_s], dev)
 
     flops, nbytes = prefill_flops(w, qlens), prefill_bytes(w, qlens)
     tflops = ws * flops / (ms_step * 1e-3) / 1e12
@@ -768,7 +763,7 @@ def run_prefill(args, w: W.Workload):
         "query_tokens_per_s": round(ws * T / (ms_step * 1e-3), 1),
         "roofline": roof,
         "e2e": {"value": round(e2e_v, 2), "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_s * 1e3, 4)},
+                "ms_per_step": round(e2e_s * 1e3, 4), "loop": E2E_LOOP},
         "gpu_launches": (2 if split else 1) * args.steps,
         "clocks": clk.summary(),
     }
@@ -860,8 +855,8 @@ def run_vtoken(args, w: W.Workload):
     torch.cuda.synchronize(dev)
     nbytes = token_decode_bytes(w, nt_h)
 
-    def decode(ts, qq=q, ntt=nt):
-        pkv.token_attention_decode(out, qq, kc, vc, ts, ntt, mx, scale=w.scale, k_scale=k_scale, v_scale=v_scale,
+    def decode(ts, qq=q, ntt=nt, o=out):
+        pkv.token_attention_decode(o, qq, kc, vc, ts, ntt, mx, scale=w.scale, k_scale=k_scale, v_scale=v_scale,
                                    partition_size=P, workspace=wsp, stream=stream)
 
     def timed_decode(ts):
@@ -905,25 +900,10 @@ def run_vtoken(args, w: W.Workload):
 
     # end to end: host query and tables in, output out, through the public API
     h_in = {k: v.cpu().pin_memory() for k, v in dict(q=q, ts=ts, nt=nt).items()}
-    d_in = {k: torch.empty_like(v, device=dev) for k, v in h_in.items()}
-    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    e2e_steps = max(3, min(args.steps, 100))
-
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            for k in h_in:
-                d_in[k].copy_(h_in[k], non_blocking=True)
-        decode(d_in["ts"], qq=d_in["q"], ntt=d_in["nt"])
-        with torch.cuda.stream(stream):
-            h_out.copy_(out, non_blocking=True)
-        stream.synchronize()
-
-    for _ in range(2):
-        e2e_step()
-    w0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-    (e2e_s,) = max_over_ranks([(time.perf_counter() - w0) / e2e_steps], dev)
+    e2e_s, h2d, d2h = overlapped_e2e(dev, stream, h_in, out,
+                                     lambda d, o: decode(d["ts"], qq=d["q"], ntt=d["nt"], o=o),
+                                     max(3, min(args.steps, 100)))
+    (e2e_s,) = max_over_ranks([e2e_s], dev)
 
     gbs_sparse = whole_job_gbs(ws, nbytes, ms_sparse)
     gbs_dense = whole_job_gbs(ws, nbytes, ms_dense)
@@ -949,8 +929,8 @@ def run_vtoken(args, w: W.Workload):
                      "kernel": "token_attention_decode (tensor cores, cp.async row gather)",
                      "algorithmic_bytes_per_launch": nbytes, "launch_ms": round(ms_dense, 5)},
         "e2e": {"value": round(whole_job_gbs(ws, nbytes, e2e_s * 1e3), 2), "unit": "GB/s",
-                "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in h_in.values()),
-                "d2h_bytes_per_step": h_out.numel() * h_out.element_size(), "ms_per_step": round(e2e_s * 1e3, 4)},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4),
+                "loop": E2E_LOOP},
         "gpu_launches": (2 if wsp.numel() > 256 else 1) * args.steps,
         "clocks": clocks,
     }
