@@ -962,7 +962,7 @@ def run_block_manager(args):
     for _ in range(steps):
         pool.append_tokens(ids, toks)          # one call per decode step: slots + copy pairs
     t2 = time.perf_counter()
-    tabs, cl = pool.block_tables(ids, (prompt + steps + bs - 1) // bs)
+    _, cl = pool.block_tables(ids, (prompt + steps + bs - 1) // bs)
     t2b = time.perf_counter()
     step_us, tables_us = (t2 - t1) / steps * 1e6, (t2b - t2) * 1e6
     assert int(cl.min()) == prompt + steps

@@ -223,6 +223,10 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
     }
     __syncwarp();
 
+    // K/V is streamed: its lines go first when L2 needs room, so the partial
+    // results (kept with "evict last") and the lines of blocks shared by
+    // several sequences, read again soon, stay longer
+    const uint64_t kv_pol = l2_policy_evict_first();
     const unsigned long long total_warps = (unsigned long long)gridDim.x * kWarps;
     const unsigned long long my_warp = (unsigned long long)blockIdx.x * kWarps + warp;
     unsigned long long static_next = my_warp;
@@ -326,8 +330,8 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
                 const int sl = __shfl_sync(0xffffffffu, tslot, t);
                 if (sl >= 0) {
                     const size_t row = ((size_t)sl * p.Hkv + iu.kvh) * C::kRowBytes + 16 * j;
-                    cp_async16(swz<C::kRowBytes, kTok>(stage_k(slot), t, 16 * j), kcb + row);
-                    cp_async16(swz<C::kRowBytes, kTok>(stage_v(slot), t, 16 * j), vcb + row);
+                    cp_async16_hint(swz<C::kRowBytes, kTok>(stage_k(slot), t, 16 * j), kcb + row, kv_pol);
+                    cp_async16_hint(swz<C::kRowBytes, kTok>(stage_v(slot), t, 16 * j), vcb + row, kv_pol);
                 }
             }
             cp_async_mbar_arrive_noinc(bar(slot));
@@ -376,8 +380,8 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
             const int t0b = ts + b * box_rows;                 // first token of the box
             const uint32_t dst = (kv ? stage_v(slot) : stage_k(slot)) + h * (kTok * C::kBoxRow) +
                                  b * box_rows * C::kBoxRow;
-            tensor_load_2d(dst, kv ? &vmap : &kmap, iu.kvh * D + h * (C::kBoxRow / (FP8 ? 1 : 2)),
-                           pb_box * p.bs + t0b % p.bs, bar(slot));
+            tensor_load_2d_hint(dst, kv ? &vmap : &kmap, iu.kvh * D + h * (C::kBoxRow / (FP8 ? 1 : 2)),
+                                pb_box * p.bs + t0b % p.bs, bar(slot), kv_pol);
         }
         ++g_issue;
         ++i_stage;
