@@ -41,7 +41,9 @@ CONFIGS = [
 
 
 @pytest.mark.parametrize("cfg", CONFIGS, ids=[f"{c[0]}-{c[1]}-{c[2]}-d{c[3]}-bs{c[4]}" for c in CONFIGS])
-@pytest.mark.parametrize("P", [-1, 0, 64])
+# 128: partial partitions cut into 32-token chunks; with an E4M3 cache the
+# longer sequences' last full partition too
+@pytest.mark.parametrize("P", [-1, 0, 64, 128])
 def test_fused_equals_write_then_decode(cfg, P):
     name, cache, qdt, d, bs = cfg
     lens = np.array([1, 16, 17, 100, 513, 1000, 2049])

@@ -65,7 +65,9 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-{c[5]}-g{c[2] // c[3]}-d{c[4]}-k{c[6]}" for c in CASES])
-@pytest.mark.parametrize("P", [-1, 0, 64])
+# 128: partial partitions cut into 32-token chunks; with an E4M3 cache the
+# longer sequences' last full partition too
+@pytest.mark.parametrize("P", [-1, 0, 64, 128])
 def test_token_decode_matches_oracle(case, P):
     name, lens, Hq, Hkv, d, cache, keep = case
     w, hv, slots, nt = _case(name, lens, Hq, Hkv, d, cache, keep)
