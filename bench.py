@@ -298,6 +298,12 @@ def measured_traffic(workload: str, kernel: str, table: str = "decode_traffic.js
     return rec.get("dram_bytes_per_launch")
 
 
+def default_shape(args) -> bool:
+    """The stored traffic records were taken on each workload's own size and
+    partition; a run with fewer sequences or another partition reports none."""
+    return args.S is None and args.partition is None
+
+
 def max_over_ranks(values, device=None):
     """Element-wise maximum of `values` over all ranks (the job's time is the
     slowest rank's); a no-op without a process group."""
@@ -586,7 +592,7 @@ def run_ours(args, w: W.Workload):
     value = whole_job_gbs(ws, sbytes, ms_step)
     achieved = dbytes / (dec_ms * 1e-3) / 1e9
     peak, peak_kind = peak_hbm()
-    traffic = measured_traffic(w.name, args.kernel)
+    traffic = measured_traffic(w.name, args.kernel) if default_shape(args) else None
     clocks = clk.summary()
     kname = decode_kernel_name(args.kernel, w)
     line = {
@@ -745,7 +751,8 @@ def run_prefill(args, w: W.Workload):
                 "frac": round(per_launch_gbs / hbm, 4), "peak_kind": hbm_kind}
         e2e_v = whole_job_gbs(ws, nbytes, e2e_s * 1e3)
     kname = "tcgen05" if args.prefill_kernel == "auto" else args.prefill_kernel
-    roof.update({"traffic": measured_traffic(w.name, kname, "prefill_traffic.json", "pkv_prefill"),
+    roof.update({"traffic": measured_traffic(w.name, kname, "prefill_traffic.json", "pkv_prefill")
+                 if default_shape(args) else None,
                  "kernel": "paged_attention_prefill (%s)" % kname,
                  "algorithmic_flops_per_launch": flops,
                  "algorithmic_bytes_per_launch": nbytes, "launch_ms": round(ms_step, 5)})
@@ -925,7 +932,8 @@ def run_vtoken(args, w: W.Workload):
                    "plan_ms_host": round(plan_s * 1e3, 2), "layers": 1},
         "roofline": {"bound": "hbm", "achieved": round(gbs_dense / ws, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(gbs_dense / ws / peak, 4), "peak_kind": peak_kind,
-                     "traffic": measured_traffic(w.name, "vtoken", "vtoken_traffic.json", "pkv_vtoken"),
+                     "traffic": measured_traffic(w.name, "vtoken", "vtoken_traffic.json", "pkv_vtoken")
+                     if default_shape(args) else None,
                      "kernel": "token_attention_decode (tensor cores, cp.async row gather)",
                      "algorithmic_bytes_per_launch": nbytes, "launch_ms": round(ms_dense, 5)},
         "e2e": {"value": round(whole_job_gbs(ws, nbytes, e2e_s * 1e3), 2), "unit": "GB/s",
