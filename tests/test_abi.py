@@ -74,6 +74,40 @@ def test_workspace_plan(pkv):
     assert P > 0 and P % 16 == 0
 
 
+def _layout_rows(n, P, hold):
+    """Partial results of a sequence of n tokens, restated from the layout
+    include/pkv.h describes: full partitions of P tokens, the rest in chunks
+    of a quarter partition (a multiple of 32 tokens; partitions under 128
+    tokens are not cut); with `hold`, a sequence of four or more full
+    partitions has its last full one cut into chunks as well."""
+    Q = (P // 4) // 32 * 32 if P >= 128 else P
+    if n <= 0:
+        return 1
+    full = n // P
+    if hold and Q < P and full >= 4:
+        full -= 1
+    return full + -(-(n - full * P) // Q)
+
+
+@pytest.mark.parametrize("P", [16, 64, 128, 256, 512, 768, 1024])
+def test_workspace_rows_cover_every_length(pkv, P):
+    """When a sequence may span more than one partition, the workspace holds,
+    per (sequence, query head), as many partial results as the longest
+    layout of any length up to max_context_len needs (brute force over every
+    length), and no more."""
+    S, Hq, d = 1, 1, 64
+    for mc in sorted({P - 1, P, 2 * P + 1, 4 * P - 1, 4 * P, 4 * P + 33, 5 * P - 1, 9 * P, 9 * P + 7, 3000}):
+        if mc <= 0:
+            continue
+        n_bytes = pkv.decode_workspace_size(S, Hq, 1, d, 16, mc, P)
+        if mc <= P:
+            assert n_bytes == 256, (P, mc)           # one partition holds every length: no split
+            continue
+        want = max(max(_layout_rows(n, P, h) for h in (0, 1)) for n in range(mc + 1))
+        up = lambda x: (x + 255) // 256 * 256     # noqa: E731
+        assert n_bytes == up(up(256 + want * 8) + want * d * 4), (P, mc, want, n_bytes)
+
+
 FAKE = 0x10000   # aligned, never dereferenced: every call below fails validation first
 
 
