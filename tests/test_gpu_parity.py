@@ -233,6 +233,43 @@ def test_bad_slot_is_skipped_and_reported():
     np.testing.assert_array_equal(_np_cache(c.k_cache), c.o_k)
 
 
+def _guarded(cache, G=4):
+    """The pool as the middle of a larger buffer: G blocks of a byte pattern
+    on each side catch any write past either end of the pool."""
+    NB = cache.shape[0]
+    big = torch.empty((NB + 2 * G,) + tuple(cache.shape[1:]), dtype=cache.dtype, device=cache.device)
+    big.view(torch.uint8).fill_(0x5A)
+    big[G:G + NB].copy_(cache)
+    return big, big[G:G + NB]
+
+
+def _guards_intact(big, G=4):
+    raw = big.view(torch.uint8)
+    return bool((raw[:G] == 0x5A).all()) and bool((raw[-G:] == 0x5A).all())
+
+
+def test_bad_slots_and_pairs_write_nothing_outside_the_pool():
+    """Slots and copy pairs past the pool are skipped: the blocks around the
+    pool keep their pattern, and the pool is what the oracle says."""
+    w = W.make("tiny")
+    c = build_case(w)
+    big_k, kc = _guarded(c.k_cache)
+    big_v, vc = _guarded(c.v_cache)
+    sm = c.slot_mapping.clone()
+    sm[0] = w.NB * w.bs + 3                 # one block past the end
+    sm[1] = w.NB * w.bs                     # the first slot past the end
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.paged_kv_write(c.new_k, c.new_v, kc, vc, sm, err_word=err)
+    pairs = torch.tensor([[1, w.NB], [2, w.NB + 3], [w.NB, 5]], dtype=torch.int64, device="cuda")
+    before = kc.clone()
+    err2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.copy_blocks([kc], [vc], pairs, err_word=err2)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 3 and int(err2.item()) == 4
+    assert _guards_intact(big_k) and _guards_intact(big_v)
+    assert torch.equal(before, kc)
+
+
 def test_bad_copy_pair_is_skipped_and_reported():
     w = W.make("tiny")
     c = build_case(w)
