@@ -9,11 +9,14 @@
 // empty and released.  A block several sequences reference (a shared
 // prefix) stays where it is and lends no free slots.
 #include <algorithm>
-#include <unordered_map>
-#include <unordered_set>
 #include <vector>
 
 #include "../../include/pkv.h"
+
+// Flat arrays indexed by slot and by block instead of hash sets: a pass over
+// every live token (a stamp per slot catches a sequence listing a slot
+// twice), then per sequence a count per block it touches, reset through the
+// list of blocks touched.
 
 extern "C" {
 
@@ -24,18 +27,20 @@ pkv_status pkv_vtoken_plan(const int32_t* token_slots, int MT, const int32_t* nu
         return PKV_ERR_INVALID_ARG;
     if (S > 0 && (!token_slots || !num_tokens)) return PKV_ERR_INVALID_ARG;
     const long long slots = (long long)NB * bs;
-    // which sequences reference each block (1 = private; 2 = two or more)
+    // which sequences reference each block (1 = private; 2 = two or more),
+    // and the last sequence to list each slot
     std::vector<uint8_t> users(NB, 0);
     std::vector<int32_t> last_user(NB, -1);
+    std::vector<int32_t> lister((size_t)slots, -1);
     for (int s = 0; s < S; ++s) {
         const int n = num_tokens[s];
         if (n < 0 || n > MT) return PKV_ERR_INVALID_ARG;
-        std::unordered_set<int32_t> seen;
-        seen.reserve(n * 2 + 1);
+        const int32_t* row = token_slots + (size_t)s * MT;
         for (int t = 0; t < n; ++t) {
-            const int32_t sl = token_slots[(size_t)s * MT + t];
+            const int32_t sl = row[t];
             if (sl < 0 || sl >= slots) return PKV_ERR_INVALID_ARG;
-            if (!seen.insert(sl).second) return PKV_ERR_INVALID_ARG;
+            if (lister[sl] == s) return PKV_ERR_INVALID_ARG;      // listed twice by one sequence
+            lister[sl] = s;
             const int b = sl / bs;
             if (last_user[b] != s) {
                 last_user[b] = s;
@@ -43,44 +48,54 @@ pkv_status pkv_vtoken_plan(const int32_t* token_slots, int MT, const int32_t* nu
             }
         }
     }
+    long long total = 0;
+    for (int s = 0; s < S; ++s) total += num_tokens[s];
     std::vector<int64_t> mv;
     std::vector<int32_t> fr;
+    mv.reserve((size_t)std::min<long long>(4 * total, 4 * (long long)max_moves + 4));
+    std::vector<int32_t> count(NB, 0);       // live tokens of the current sequence per private block
+    std::vector<uint8_t> dropped(NB, 0);
+    std::vector<int32_t> touched, keep, drop, holes;
     for (int s = 0; s < S; ++s) {
         const int n = num_tokens[s];
         const int32_t* row = token_slots + (size_t)s * MT;
-        std::unordered_map<int, int> count;
+        touched.clear();
+        long long live = 0;
         for (int t = 0; t < n; ++t) {
             const int b = row[t] / bs;
-            if (users[b] == 1) ++count[b];
+            if (users[b] != 1) continue;
+            if (count[b]++ == 0) touched.push_back(b);
+            ++live;
         }
-        if (count.empty()) continue;
-        long long live = 0;
-        for (auto& kv : count) live += kv.second;
         const size_t k = (size_t)((live + bs - 1) / bs);
-        if (count.size() <= k) continue;
-        std::vector<std::pair<int, int>> order(count.begin(), count.end());   // (block, live)
-        std::sort(order.begin(), order.end(), [](const std::pair<int, int>& a, const std::pair<int, int>& b) {
-            return a.second != b.second ? a.second > b.second : a.first < b.first;
-        });
-        std::vector<int> keep, drop;
-        for (size_t i = 0; i < order.size(); ++i) (i < k ? keep : drop).push_back(order[i].first);
-        std::sort(keep.begin(), keep.end());
-        std::sort(drop.begin(), drop.end());
-        std::unordered_set<int32_t> used(row, row + n);
-        std::vector<int32_t> holes;
-        for (int b : keep)
-            for (int o = 0; o < bs; ++o)
-                if (!used.count(b * bs + o)) holes.push_back(b * bs + o);
-        std::unordered_set<int> dropset(drop.begin(), drop.end());
-        size_t hi = 0;
-        for (int t = 0; t < n; ++t) {
-            if (!dropset.count(row[t] / bs)) continue;
-            mv.push_back(s);
-            mv.push_back(t);
-            mv.push_back(row[t]);
-            mv.push_back(holes[hi++]);
+        if (touched.size() > k) {
+            // the k blocks with the most live tokens stay (lower id first on ties)
+            std::sort(touched.begin(), touched.end(), [&](int a, int b) {
+                return count[a] != count[b] ? count[a] > count[b] : a < b;
+            });
+            keep.assign(touched.begin(), touched.begin() + k);
+            drop.assign(touched.begin() + k, touched.end());
+            std::sort(keep.begin(), keep.end());
+            std::sort(drop.begin(), drop.end());
+            // free slots of the kept blocks, lowest first (a private block's
+            // slots are listed by this sequence only)
+            holes.clear();
+            for (int b : keep)
+                for (int o = 0; o < bs; ++o)
+                    if (lister[(size_t)b * bs + o] != s) holes.push_back(b * bs + o);
+            for (int b : drop) dropped[b] = 1;
+            size_t hi = 0;
+            for (int t = 0; t < n; ++t) {
+                if (!dropped[row[t] / bs]) continue;
+                mv.push_back(s);
+                mv.push_back(t);
+                mv.push_back(row[t]);
+                mv.push_back(holes[hi++]);
+            }
+            for (int b : drop) dropped[b] = 0;
+            fr.insert(fr.end(), drop.begin(), drop.end());
         }
-        fr.insert(fr.end(), drop.begin(), drop.end());
+        for (int b : touched) count[b] = 0;
     }
     *num_moves = (int64_t)(mv.size() / 4);
     *num_freed = (int64_t)fr.size();
