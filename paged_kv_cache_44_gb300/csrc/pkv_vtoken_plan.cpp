@@ -13,10 +13,11 @@
 
 #include "../../include/pkv.h"
 
-// Flat arrays indexed by slot and by block instead of hash sets: a pass over
-// every live token (a stamp per slot catches a sequence listing a slot
-// twice), then per sequence a count per block it touches, reset through the
-// list of blocks touched.
+// Flat arrays instead of hash sets: one bit per slot of the pool marks the
+// slots the current sequence lists (set while a sequence is examined, then
+// cleared through its own row), and per-block counters are reset through
+// the list of blocks the sequence touched.  Host memory: one bit per slot
+// and about ten bytes per block.
 
 extern "C" {
 
@@ -27,11 +28,20 @@ pkv_status pkv_vtoken_plan(const int32_t* token_slots, int MT, const int32_t* nu
         return PKV_ERR_INVALID_ARG;
     if (S > 0 && (!token_slots || !num_tokens)) return PKV_ERR_INVALID_ARG;
     const long long slots = (long long)NB * bs;
-    // which sequences reference each block (1 = private; 2 = two or more),
-    // and the last sequence to list each slot
+    std::vector<uint64_t> listed((size_t)((slots + 63) / 64), 0);
+    auto test_set = [&](int32_t sl) {                     // true if the bit was already set
+        uint64_t& w = listed[(size_t)sl >> 6];
+        const uint64_t bit = 1ull << (sl & 63);
+        const bool was = (w & bit) != 0;
+        w |= bit;
+        return was;
+    };
+    auto clear_row = [&](const int32_t* row, int n) {
+        for (int t = 0; t < n; ++t) listed[(size_t)row[t] >> 6] = 0;
+    };
+    // which sequences reference each block (1 = private; 2 = two or more)
     std::vector<uint8_t> users(NB, 0);
     std::vector<int32_t> last_user(NB, -1);
-    std::vector<int32_t> lister((size_t)slots, -1);
     for (int s = 0; s < S; ++s) {
         const int n = num_tokens[s];
         if (n < 0 || n > MT) return PKV_ERR_INVALID_ARG;
@@ -39,14 +49,14 @@ pkv_status pkv_vtoken_plan(const int32_t* token_slots, int MT, const int32_t* nu
         for (int t = 0; t < n; ++t) {
             const int32_t sl = row[t];
             if (sl < 0 || sl >= slots) return PKV_ERR_INVALID_ARG;
-            if (lister[sl] == s) return PKV_ERR_INVALID_ARG;      // listed twice by one sequence
-            lister[sl] = s;
+            if (test_set(sl)) return PKV_ERR_INVALID_ARG;     // listed twice by one sequence
             const int b = sl / bs;
             if (last_user[b] != s) {
                 last_user[b] = s;
                 if (users[b] < 2) ++users[b];
             }
         }
+        clear_row(row, n);
     }
     long long total = 0;
     for (int s = 0; s < S; ++s) total += num_tokens[s];
@@ -62,6 +72,7 @@ pkv_status pkv_vtoken_plan(const int32_t* token_slots, int MT, const int32_t* nu
         touched.clear();
         long long live = 0;
         for (int t = 0; t < n; ++t) {
+            test_set(row[t]);
             const int b = row[t] / bs;
             if (users[b] != 1) continue;
             if (count[b]++ == 0) touched.push_back(b);
@@ -77,12 +88,13 @@ pkv_status pkv_vtoken_plan(const int32_t* token_slots, int MT, const int32_t* nu
             drop.assign(touched.begin() + k, touched.end());
             std::sort(keep.begin(), keep.end());
             std::sort(drop.begin(), drop.end());
-            // free slots of the kept blocks, lowest first (a private block's
-            // slots are listed by this sequence only)
+            // free slots of the kept blocks, lowest first
             holes.clear();
             for (int b : keep)
-                for (int o = 0; o < bs; ++o)
-                    if (lister[(size_t)b * bs + o] != s) holes.push_back(b * bs + o);
+                for (int o = 0; o < bs; ++o) {
+                    const long long sl = (long long)b * bs + o;
+                    if (!((listed[(size_t)sl >> 6] >> (sl & 63)) & 1ull)) holes.push_back((int32_t)sl);
+                }
             for (int b : drop) dropped[b] = 1;
             size_t hi = 0;
             for (int t = 0; t < n; ++t) {
@@ -96,6 +108,7 @@ pkv_status pkv_vtoken_plan(const int32_t* token_slots, int MT, const int32_t* nu
             fr.insert(fr.end(), drop.begin(), drop.end());
         }
         for (int b : touched) count[b] = 0;
+        clear_row(row, n);
     }
     *num_moves = (int64_t)(mv.size() / 4);
     *num_freed = (int64_t)fr.size();
