@@ -427,7 +427,9 @@ PKV_API pkv_status pkv_repack_tokens(void* const* key_caches, void* const* value
  * max_moves moves [.., 4] and max_freed block ids, and the counts needed in
  * *num_moves / *num_freed.  Returns PKV_ERR_INVALID_ARG for a slot outside
  * the pool or a sequence holding one slot twice, PKV_ERR_WORKSPACE when an
- * output array is too small (counts still set, arrays untouched).
+ * output array is too small (counts still set, arrays untouched).  Scratch
+ * host memory during the call: one bit per slot of the pool and about ten
+ * bytes per block, plus the moves found.
  */
 PKV_API pkv_status pkv_vtoken_plan(const int32_t* token_slots, int MT, const int32_t* num_tokens, int S, int bs,
                                    int NB, int64_t* moves, int64_t max_moves, int64_t* num_moves,
