@@ -269,16 +269,44 @@ KERNEL_SOURCES = {
 }
 
 
+def code_only(text: str) -> str:
+    """C/C++/CUDA source with its comments removed and every run of white
+    space made one space: what the compiler sees, so that editing a comment
+    does not disown a measurement.  String and character literals are kept
+    as they are."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(prefix: str = "pkv_decode") -> str:
-    """Hash of the sources a traffic record was taken on: the kernels' files,
-    the headers they include, and the parameter struct they read."""
+    """Hash of the code a traffic record was taken on (comments aside): the
+    kernels' files, the headers they include, and the parameter struct they
+    read."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_44_gb300", "csrc")
     for f in KERNEL_SOURCES[prefix]:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
-    with open(os.path.join(csrc, "pkv_internal.h")) as fh:
-        txt = fh.read()
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update((f + "\n" + code_only(fh.read())).encode())
+    with open(os.path.join(csrc, "pkv_internal.h"), encoding="utf-8") as fh:
+        txt = code_only(fh.read())
     i0 = txt.index("struct DecodeParams {")
     h.update(txt[i0: txt.index("};", i0)].encode())
     return h.hexdigest()[:16]

@@ -134,10 +134,11 @@ struct __align__(16) Unit {
 };
 
 // Unit id -> coordinates.  The ids run over two regions:
-//   A: every full partition (P tokens), partition-major -- the same
+//   A: every full partition (P tokens) not held back, partition-major -- the same
 //      partition of every sequence is claimed close together in time, so
 //      shared prefix blocks are read while still in L2;
-//   B: the chunks of each sequence's last, partial partition: first every
+//   B: the chunks of each sequence's last, partial partition (and, with
+//      p.hold, of the full partitions held back before it): first every
 //      full-size chunk (Q tokens), chunk-major, then each sequence's
 //      shorter last chunk (and the empty unit of a sequence with no tokens).
 // Claimed in id order, the long units go first and the short ones last, so
@@ -165,7 +166,7 @@ __device__ __forceinline__ bool unit_of(const DecodeParams& p, unsigned long lon
     x.np = num_partitions(n, p.P, p.Q, p.hold);
     const int full = whole_partitions(n, p.P, p.Q, p.hold);
     const int tail = n - full * p.P;
-    const int cfull = chunk_slots(p.P, p.Q, p.hold) - 1;           // full-size chunks of the longest remainder
+    const int cfull = chunk_slots(p.P, p.Q, p.hold) - 1;   // full-size chunks of the longest remainder
     if (in_a) {
         if (idx >= full) return false;
         x.part = idx;
