@@ -69,7 +69,8 @@ enum {
     PKV_DEVERR_BLOCK_ID = 1,      /* a block table entry outside [0, NB) */
     PKV_DEVERR_CONTEXT_LEN = 2,   /* context_lens[s] < 0 or > max_context_len (clamped) */
     PKV_DEVERR_SLOT = 3,          /* slot_mapping[i] >= NB * bs, or a token-table slot outside [0, NB * bs) */
-    PKV_DEVERR_COPY_PAIR = 4,     /* a copy pair with an id outside [0, NB) */
+    PKV_DEVERR_COPY_PAIR = 4,     /* a copy pair with an id outside [0, NB), or whose destination another
+                                     pair also writes or any pair reads (see pkv_copy_blocks) */
     PKV_DEVERR_TIMEOUT = 5,       /* a staged copy did not land within ~2 s; the kernel gave up */
     PKV_DEVERR_QUERY_LEN = 6,     /* prefill: a sequence's queries are < 0, more than its length or
                                      than max_query_len, or outside [0, T) (the sequence is skipped) */
@@ -241,10 +242,19 @@ PKV_API pkv_status pkv_paged_attention_decode_ex(void* out, const void* query, p
  * value_caches[l] becomes a byte copy of block src (block_bytes bytes each,
  * = bs * Hkv * d * element size).  key_caches / value_caches are HOST arrays
  * of num_layers device pointers (at most 256 layers); the call copies them
- * into the launch, so the arrays may be freed when it returns.  The
- * destinations must be distinct and must not be sources (the host that
- * decides copy-on-write guarantees this; it is not checked).  block_bytes
+ * into the launch, so the arrays may be freed when it returns.  block_bytes
  * must be a multiple of 16.
+ *
+ * The pairs are copied in no fixed order, so the destinations must be
+ * distinct and must not be sources (the host that decides copy-on-write
+ * guarantees this).  A pair with an id outside [0, NB) is always skipped.
+ * When err_word is not NULL the pairs are also checked against each other:
+ * a pair whose destination another in-pool pair also writes, or any
+ * in-pool pair (itself included) reads, is skipped, and PKV_DEVERR_COPY_PAIR
+ * is reported; the other pairs are copied.  This check scans the whole
+ * mapping in every CTA of the copy (16 bytes per pair, from L2), which is
+ * negligible for tens of pairs and grows with P * P for thousands.  With
+ * err_word NULL nothing is checked and such pairs race.
  */
 PKV_API pkv_status pkv_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
                            const int64_t* block_mapping, int P, int NB, size_t block_bytes,
@@ -273,13 +283,20 @@ PKV_API pkv_status pkv_copy_blocks(void* const* key_caches, void* const* value_c
  * still passes and owns every input and output.
  *
  * Limits and behaviour:
+ *  - The arguments are checked as pkv_paged_attention_decode checks them,
+ *    with the same status codes, before anything is enqueued.
  *  - The scratch the call needs is pkv_decode_workspace_size(...) for the
  *    same sizes and partition request.  If that exceeds
  *    PKV_STATIC_SCRATCH_BYTES the call returns PKV_ERR_WORKSPACE and
  *    enqueues nothing; a larger partition_size needs less scratch.
+ *  - `stream` must belong to the current device (the array used is the
+ *    current device's); a stream of another device gives
+ *    PKV_ERR_INVALID_ARG and nothing is enqueued.
  *  - The first call on a device looks up the array's device address (with
- *    that device current) and caches it; make that first call before any
- *    stream capture.
+ *    that device current) and caches it with the device's CUDA context;
+ *    make that first call before any stream capture.  After a device reset
+ *    (a new context) the next call looks the address up again, so it too
+ *    should come before any capture.
  *  - Each call clears the array's 256-byte work-counter header on `stream`
  *    (a memset) before the decode; the rest keeps the previous call's
  *    contents and needs no clearing.

@@ -19,12 +19,31 @@ constexpr int kCopyThreads = 256;
 constexpr long long kChunkVecs = 1024;              // 16-byte vectors per CTA
 constexpr int kPerThread = (int)(kChunkVecs / kCopyThreads);
 
+// kCheck (the caller passed an error word): besides ids outside the pool,
+// a pair is skipped when its destination is also written by another pair or
+// read by any pair, since the copies run in no fixed order and the result
+// would depend on it.  Every CTA of the pair decides the same way from the
+// read-only mapping: its threads scan all P pairs (16 bytes each, from L2).
+template <bool kCheck>
 __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(const __grid_constant__ CopyParams p) {
     const int pair = blockIdx.x, layer = blockIdx.y, which = blockIdx.z & 1, chunk = blockIdx.z >> 1;
     const long long src = p.mapping[2 * pair], dst = p.mapping[2 * pair + 1];
+    const bool first = layer == 0 && blockIdx.z == 0 && threadIdx.x == 0;
     if (src < 0 || src >= p.NB || dst < 0 || dst >= p.NB) {
-        if (layer == 0 && blockIdx.z == 0 && threadIdx.x == 0) report(p.err, PKV_DEVERR_COPY_PAIR);
+        if (first) report(p.err, PKV_DEVERR_COPY_PAIR);
         return;
+    }
+    if constexpr (kCheck) {
+        bool clash = false;
+        for (int q = threadIdx.x; q < p.P; q += kCopyThreads) {
+            const long long s2 = p.mapping[2 * q], d2 = p.mapping[2 * q + 1];
+            const bool in_pool = s2 >= 0 && s2 < p.NB && d2 >= 0 && d2 < p.NB;
+            clash |= in_pool && (s2 == dst || (q != pair && d2 == dst));
+        }
+        if (__syncthreads_or(clash)) {
+            if (first) report(p.err, PKV_DEVERR_COPY_PAIR);
+            return;
+        }
     }
     char* base = static_cast<char*>(which ? p.v[layer] : p.k[layer]);
     const uint4* s = reinterpret_cast<const uint4*>(base + (size_t)src * p.block_bytes);
@@ -52,7 +71,10 @@ cudaError_t launch_copy(const CopyParams& p, cudaStream_t st) {
     const long long chunks = (n + kChunkVecs - 1) / kChunkVecs;
     if (chunks < 1 || 2 * chunks > 65535) return cudaErrorInvalidValue;
     dim3 grid(p.P, p.L, (unsigned)(2 * chunks));
-    copy_blocks_kernel<<<grid, kCopyThreads, 0, st>>>(p);
+    if (p.err != nullptr)
+        copy_blocks_kernel<true><<<grid, kCopyThreads, 0, st>>>(p);
+    else
+        copy_blocks_kernel<false><<<grid, kCopyThreads, 0, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -14,7 +14,7 @@ if torch.cuda.is_available():
     import oracle as O
     import paged_kv_cache_44_gb300 as pkv
     from tests.gpu_cases import (ODT, assert_close, build_case, gpu_decode, gpu_write, oracle_decode,
-                                 oracle_write)
+                                 oracle_write, tolerance)
 
 KERNELS = ["cuda_cores", "tensor_cores"]
 
@@ -282,6 +282,65 @@ def test_bad_copy_pair_is_skipped_and_reported():
     assert torch.equal(before, c.k_cache)
 
 
+def _conflict_free_pairs(pairs, NB):
+    """The pairs copy_blocks copies when it checks them: in the pool, and
+    with a destination no other in-pool pair writes and no in-pool pair
+    (itself included) reads."""
+    inpool = [(int(s), int(d)) for s, d in pairs if 0 <= s < NB and 0 <= d < NB]
+    keep = []
+    for i, (s, d) in enumerate(pairs):
+        if not (0 <= s < NB and 0 <= d < NB):
+            continue
+        dsts = [d2 for j, (_, d2) in enumerate(pairs) if j != i and 0 <= pairs[j][0] < NB and 0 <= d2 < NB]
+        if d in dsts or d in [s2 for s2, _ in inpool]:
+            continue
+        keep.append((s, d))
+    return np.array(keep, np.int64).reshape(-1, 2)
+
+
+@pytest.mark.parametrize("layers", [1, 3])
+def test_conflicting_copy_pairs_are_skipped_and_reported(layers):
+    """With an error word, a pair whose destination is another pair's
+    destination or any pair's source is skipped and reported; the other
+    pairs are copied bit for bit as the oracle copies them, and the blocks
+    around the pool keep their pattern."""
+    w = W.make("tiny")
+    c = build_case(w)
+    pairs = np.array([[1, 5], [2, 5],            # the same destination twice: both skipped
+                      [3, 6], [6, 7],            # 6 is written and read: the first skipped, the second copied
+                      [4, 8], [9, 9],            # a plain copy; a block copied onto itself: skipped
+                      [10, w.NB], [11, 12]],     # out of the pool: skipped; a plain copy
+                     np.int64)
+    keep = _conflict_free_pairs(pairs, w.NB)
+    assert keep.tolist() == [[6, 7], [4, 8], [11, 12]]
+    bigs, kcs, vcs, oks, ovs = [], [], [], [], []
+    for layer in range(layers):
+        k_l, v_l = (c.k_cache, c.v_cache) if layer == 0 else (c.k_cache * (layer + 1), c.v_cache - layer)
+        bk, kc = _guarded(k_l.contiguous())
+        bv, vc = _guarded(v_l.contiguous())
+        bigs += [bk, bv]
+        kcs.append(kc)
+        vcs.append(vc)
+        oks.append(_np_cache(kc).copy())
+        ovs.append(_np_cache(vc).copy())
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.copy_blocks(kcs, vcs, torch.from_numpy(pairs).cuda(), err_word=err)
+    O.copy_blocks(oks, ovs, keep)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 4
+    for layer in range(layers):
+        np.testing.assert_array_equal(_np_cache(kcs[layer]), oks[layer])
+        np.testing.assert_array_equal(_np_cache(vcs[layer]), ovs[layer])
+    assert all(_guards_intact(b) for b in bigs)
+    # the same pairs without the conflicts: nothing to report, same caches
+    err.zero_()
+    pkv.copy_blocks(kcs, vcs, torch.from_numpy(keep).cuda(), err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for layer in range(layers):
+        np.testing.assert_array_equal(_np_cache(kcs[layer]), oks[layer])
+
+
 # ------------------------------------------------------------ full-size runs
 
 FULL = [("qwen2.5-1.5b", None), ("qwen2.5-7b-prefix", None), ("qwen2.5-72b-long", 3), ("fp8-bs16", 4),
@@ -310,7 +369,8 @@ def test_full_size_step(name, sample):
     ref = oracle_decode(c)
     for kernel in _kernels_for(w):
         out = gpu_decode(c, kernel=kernel)
-        assert_close(out[torch.from_numpy(c.seqs).cuda()], ref, w.cache_dtype, f"{name} {kernel}")
+        err = assert_close(out[torch.from_numpy(c.seqs).cuda()], ref, w.cache_dtype, f"{name} {kernel}")
+        print(f"max |gpu - oracle| {name} {kernel}: {err:.3e} (tolerance {tolerance(w.cache_dtype, out.dtype)})")
         of = out.float()
         assert torch.isfinite(of).all()
         if w.cache_dtype == W.DT_E4M3:
