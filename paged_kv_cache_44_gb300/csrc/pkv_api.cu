@@ -164,13 +164,15 @@ size_t pkv_decode_workspace_size(int S, int Hq, int Hkv, int d, int bs, int max_
     return make_plan(S, Hq, d, max_context_len, P).bytes;
 }
 
-pkv_status pkv_paged_attention_decode_ex(void* out, const void* query, pkv_dtype q_dtype, const void* key_cache,
-                                         const void* value_cache, pkv_dtype cache_dtype,
-                                         const int32_t* block_tables, int MB, const int32_t* context_lens, int S,
-                                         int max_context_len, int Hq, int Hkv, int d, int bs, int NB, float scale,
-                                         float k_scale, float v_scale, int partition_size, void* workspace,
-                                         size_t workspace_bytes, int32_t* err_word, pkv_stream_t stream,
-                                         int kernel) {
+}  // extern "C"
+
+namespace pkv {
+
+pkv_status check_decode_args(const void* out, const void* query, pkv_dtype q_dtype, const void* key_cache,
+                             const void* value_cache, pkv_dtype cache_dtype, const int32_t* block_tables, int MB,
+                             const int32_t* context_lens, int S, int max_context_len, int Hq, int Hkv, int d,
+                             int bs, int NB, float scale, float k_scale, float v_scale, int partition_size,
+                             int kernel) {
     if (S < 0 || MB < 1 || NB < 1 || Hkv < 1 || Hq < 1 || max_context_len < 0) return PKV_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return PKV_ERR_INVALID_ARG;
     if (q_dtype != PKV_F32 && q_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
@@ -188,14 +190,30 @@ pkv_status pkv_paged_attention_decode_ex(void* out, const void* query, pkv_dtype
     if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache) ||
         (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
         return PKV_ERR_INVALID_ARG;
+    if (resolve_partition(S, Hq, Hkv, d, bs, max_context_len, partition_size) < 0) return PKV_ERR_INVALID_ARG;
+    if (kernel == PKV_DECODE_TENSOR_CORES && !decode_tc_supports(q_dtype, cache_dtype, d, bs, NB))
+        return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status pkv_paged_attention_decode_ex(void* out, const void* query, pkv_dtype q_dtype, const void* key_cache,
+                                         const void* value_cache, pkv_dtype cache_dtype,
+                                         const int32_t* block_tables, int MB, const int32_t* context_lens, int S,
+                                         int max_context_len, int Hq, int Hkv, int d, int bs, int NB, float scale,
+                                         float k_scale, float v_scale, int partition_size, void* workspace,
+                                         size_t workspace_bytes, int32_t* err_word, pkv_stream_t stream,
+                                         int kernel) {
+    const pkv_status chk = check_decode_args(out, query, q_dtype, key_cache, value_cache, cache_dtype, block_tables,
+                                             MB, context_lens, S, max_context_len, Hq, Hkv, d, bs, NB, scale,
+                                             k_scale, v_scale, partition_size, kernel);
+    if (chk != PKV_OK || S == 0) return chk;
 
     const int P = resolve_partition(S, Hq, Hkv, d, bs, max_context_len, partition_size);
-    if (P < 0) return PKV_ERR_INVALID_ARG;
-    const bool tc_ok = decode_tc_supports(q_dtype, cache_dtype, d, bs, NB);
-    bool use_tc;
-    if (kernel == PKV_DECODE_AUTO) use_tc = tc_ok;
-    else if (kernel == PKV_DECODE_TENSOR_CORES) { if (!tc_ok) return PKV_ERR_UNSUPPORTED; use_tc = true; }
-    else use_tc = false;
+    const bool use_tc = kernel != PKV_DECODE_CUDA_CORES && decode_tc_supports(q_dtype, cache_dtype, d, bs, NB);
     const DecodePlan pl = make_plan(S, Hq, d, max_context_len, P);
     if (pl.split) {
         if (!workspace || workspace_bytes < pl.bytes) return PKV_ERR_WORKSPACE;

@@ -764,16 +764,9 @@ template <int D, bool FP8, typename QF, bool TT>
 cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t st) {
     using C = Cfg<D, FP8, QF::bytes>;
     auto kern = decode_tc_kernel<D, FP8, QF, TT>;
-    // the shared-memory opt-in is per device: remember it per device ordinal
-    static bool configured[64] = {false};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static SmemOptIn optin;
+    cudaError_t e = optin.ensure(reinterpret_cast<const void*>(kern), C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev] = true;
-    }
     CUtensorMap kmap, vmap;
     if (!encode_cache_map<D, FP8>(&kmap, p.kc, p) || !encode_cache_map<D, FP8>(&vmap, p.vc, p))
         return cudaErrorInvalidValue;

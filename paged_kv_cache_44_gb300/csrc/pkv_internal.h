@@ -6,9 +6,36 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/pkv.h"
 
 namespace pkv {
+
+// A kernel's opt-in to more than 48 KB of dynamic shared memory, made once
+// per device (the attribute is per device and context).  One instance per
+// kernel; safe when several host threads make their first call at once.
+class SmemOptIn {
+  public:
+    cudaError_t ensure(const void* kernel, int bytes) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        const bool cached = dev >= 0 && dev < kDevices;
+        if (cached && done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+        std::lock_guard<std::mutex> lock(mu_);
+        if (cached && done_[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e == cudaSuccess && cached) done_[dev].store(true, std::memory_order_release);
+        return e;
+    }
+
+  private:
+    static constexpr int kDevices = 64;
+    std::atomic<bool> done_[kDevices] = {};
+    std::mutex mu_;
+};
 
 constexpr int kMaxCopyLayers = 256;
 constexpr size_t kWorkspaceHeaderBytes = 256;   // scheduler counters, zero between calls
@@ -87,7 +114,15 @@ struct DecodePlan {
     size_t ml_offset, acc_offset, bytes;
 };
 
-enum class DecodeKernel { Simt = 0, TensorCore = 1 };
+// Host checks of pkv_paged_attention_decode_ex's arguments, with its status
+// codes, short of the workspace: PKV_OK when the decode can be enqueued (or,
+// with S == 0, has nothing to do).  Touches neither the GPU nor the CUDA
+// runtime, so a caller can run it before enqueueing anything of its own.
+pkv_status check_decode_args(const void* out, const void* query, pkv_dtype q_dtype, const void* key_cache,
+                             const void* value_cache, pkv_dtype cache_dtype, const int32_t* block_tables, int MB,
+                             const int32_t* context_lens, int S, int max_context_len, int Hq, int Hkv, int d,
+                             int bs, int NB, float scale, float k_scale, float v_scale, int partition_size,
+                             int kernel);
 
 cudaError_t launch_decode_simt(const DecodeParams& p, pkv_dtype q_dt, pkv_dtype c_dt, cudaStream_t st);
 cudaError_t launch_decode_tc(const DecodeParams& p, pkv_dtype q_dt, pkv_dtype c_dt, int num_sms,

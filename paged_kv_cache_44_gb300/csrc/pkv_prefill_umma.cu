@@ -671,15 +671,9 @@ cudaError_t launch_umma_d(const DecodeParams& p, const int32_t* query_start, int
                           bool merge, cudaStream_t st) {
     using C = UCfg<D>;
     auto kern = prefill_umma_kernel<D>;
-    static bool configured[64] = {false};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static SmemOptIn optin;
+    cudaError_t e = optin.ensure(reinterpret_cast<const void*>(kern), C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev] = true;
-    }
     CUtensorMap kmap, vmap;
     if (!prefill_encode_kv_map(&kmap, p.kc, p) || !prefill_encode_kv_map(&vmap, p.vc, p)) return cudaErrorInvalidValue;
     int rt_max = (max_q_len * p.g + kURows - 1) / kURows;

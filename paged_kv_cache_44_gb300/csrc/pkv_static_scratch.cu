@@ -9,6 +9,9 @@
 // raw pointers and has no device allocator.  This entry point serves them
 // with scratch that lives in a fixed array in device memory, owned by the
 // library for the life of the process.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "pkv_internal.h"
@@ -20,22 +23,52 @@ static __device__ __align__(256) unsigned char g_decode_scratch[PKV_STATIC_SCRAT
 namespace {
 
 constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
 
-// Device address of g_decode_scratch on the current device.  In host code
-// the array's name is only a host-side stand-in, so the address is looked up
-// once per device, with that device current, and cached.
-pkv_status scratch_on_current_device(void** addr) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+// Per device ordinal: the context the address was looked up in, and the
+// address.  A device reset gives the ordinal a new primary context in which
+// the library's module, and so the array, is loaded again at another
+// address; the context tells the two apart.
+struct ScratchSlot {
+    CUcontext ctx;
+    void* addr;
+};
+std::mutex g_mu;
+ScratchSlot g_slots[kMaxDevices] = {};
+
+PFN_cuCtxGetCurrent_v4000 ctx_get_current() {
+    static std::once_flag once;
+    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    });
+    return fn;
+}
+
+// Device address of g_decode_scratch on device `dev`, which must be the
+// current device.  In host code the array's name is only a host-side
+// stand-in, so the address is looked up with cudaGetSymbolAddress, once per
+// device and context, and cached.
+pkv_status scratch_on_device(int dev, void** addr) {
+    if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_UNSUPPORTED;
+    auto get_ctx = ctx_get_current();
+    if (get_ctx == nullptr) return PKV_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    CUcontext ctx = nullptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS) return PKV_ERR_CUDA;
+    ScratchSlot& slot = g_slots[dev];
+    if (slot.addr == nullptr || ctx == nullptr || ctx != slot.ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return PKV_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+        // the lookup makes the device's primary context current if it was not yet
+        if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return PKV_ERR_CUDA;
+        slot.ctx = ctx;
+        slot.addr = p;
     }
-    *addr = g_scratch_addr[dev];
+    *addr = slot.addr;
     return PKV_OK;
 }
 
@@ -46,20 +79,28 @@ extern "C" pkv_status pkv_paged_attention_decode_static(
     pkv_dtype cache_dtype, const int32_t* block_tables, int MB, const int32_t* context_lens, int S,
     int max_context_len, int Hq, int Hkv, int d, int bs, int NB, float scale, float k_scale, float v_scale,
     int partition_size, int32_t* err_word, pkv_stream_t stream) {
-    if (S < 0) return PKV_ERR_INVALID_ARG;
-    if (S == 0) return PKV_OK;
+    // the allocating entry point's checks and status codes, before anything touches the GPU
+    const pkv_status chk = pkv::check_decode_args(out, query, q_dtype, key_cache, value_cache, cache_dtype,
+                                                  block_tables, MB, context_lens, S, max_context_len, Hq, Hkv, d,
+                                                  bs, NB, scale, k_scale, v_scale, partition_size,
+                                                  PKV_DECODE_AUTO);
+    if (chk != PKV_OK || S == 0) return chk;
     const size_t need = pkv_decode_workspace_size(S, Hq, Hkv, d, bs, max_context_len, partition_size);
-    if (need == 0) return PKV_ERR_INVALID_ARG;                       // sizes the decode would reject
+    if (need == 0) return PKV_ERR_INVALID_ARG;
     if (need > (size_t)PKV_STATIC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;   // beyond the fixed maximum
+    // the scratch must be the one on the stream's device
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int dev = -1, stream_dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaStreamGetDevice(st, &stream_dev) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (stream_dev != dev) return PKV_ERR_INVALID_ARG;
     void* scratch = nullptr;
-    const pkv_status st = scratch_on_current_device(&scratch);
-    if (st != PKV_OK) return st;
+    const pkv_status got = scratch_on_device(dev, &scratch);
+    if (got != PKV_OK) return got;
     // The array keeps whatever the previous call left.  The work counter at
     // its start must be zero; a completed decode leaves it zero, but clear it
     // anyway so that one interrupted call cannot disturb the next.
-    if (cudaMemsetAsync(scratch, 0, pkv::kWorkspaceHeaderBytes, reinterpret_cast<cudaStream_t>(stream)) !=
-        cudaSuccess)
-        return PKV_ERR_CUDA;
+    if (cudaMemsetAsync(scratch, 0, pkv::kWorkspaceHeaderBytes, st) != cudaSuccess) return PKV_ERR_CUDA;
     return pkv_paged_attention_decode(out, query, q_dtype, key_cache, value_cache, cache_dtype, block_tables, MB,
                                       context_lens, S, max_context_len, Hq, Hkv, d, bs, NB, scale, k_scale,
                                       v_scale, partition_size, scratch, (size_t)PKV_STATIC_SCRATCH_BYTES,

@@ -143,6 +143,38 @@ def test_decode_host_validation(pkv):
     assert _decode(pkv, S=0) == 0                  # empty batch is a no-op
 
 
+def _decode_static(pkv, **kw):
+    a = dict(out=FAKE, q=FAKE, qdt=1, k=FAKE, v=FAKE, cdt=1, bt=FAKE, MB=4, cl=FAKE, S=2, maxctx=64, Hq=8, Hkv=2,
+             d=128, bs=16, NB=10, scale=0.088, ks=1.0, vs=1.0, P=32, err=None, stream=None)
+    a.update(kw)
+    return pkv.lib.pkv_paged_attention_decode_static(
+        a["out"], a["q"], a["qdt"], a["k"], a["v"], a["cdt"], a["bt"], a["MB"], a["cl"], a["S"], a["maxctx"],
+        a["Hq"], a["Hkv"], a["d"], a["bs"], a["NB"], a["scale"], a["ks"], a["vs"], a["P"], a["err"], a["stream"])
+
+
+@pytest.mark.parametrize("bad", [
+    dict(Hq=7), dict(d=96), dict(bs=8), dict(qdt=2), dict(cdt=7), dict(out=None), dict(q=FAKE + 4),
+    dict(maxctx=65), dict(P=24), dict(scale=float("nan")), dict(cdt=2, ks=0.0), dict(S=70000), dict(S=-1),
+    dict(MB=0), dict(S=0)])
+def test_static_decode_checks_arguments_like_the_allocating_call(pkv, bad):
+    """The allocation-free decode returns the allocating decode's status for
+    every rejected argument, and does so before it touches the CUDA runtime:
+    this process has no GPU, so a call that got as far as looking up its
+    scratch or enqueueing the header clear would return PKV_ERR_CUDA (4)."""
+    want = _decode(pkv, **bad)
+    got = _decode_static(pkv, **bad)
+    assert got == want, (bad, got, want)
+    assert got != 4
+
+
+def test_static_decode_rejects_sizes_beyond_its_scratch(pkv):
+    """A decode whose partition triples would not fit the fixed scratch gets
+    PKV_ERR_WORKSPACE before anything is enqueued (72B-shaped, partitions of
+    16 tokens: far more than 32 MiB of triples)."""
+    assert pkv.decode_workspace_size(32, 64, 8, 128, 16, 32768, 16) > pkv.STATIC_SCRATCH_BYTES
+    assert _decode_static(pkv, S=32, Hq=64, Hkv=8, maxctx=32768, MB=2048, P=16) == 3
+
+
 def test_write_and_copy_host_validation(pkv):
     L = pkv.lib
     assert L.pkv_paged_kv_write(FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 4, 10, 16, 2, 12, 1.0, 1.0, None, None) == 2
