@@ -17,7 +17,6 @@ section 4):
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 from typing import Optional, Sequence
 
@@ -203,7 +202,7 @@ def make_workspace(S: int, Hq: int, Hkv: int, d: int, bs: int, max_context_len: 
 
 def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                            value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
-                           max_context_len: int, scale: Optional[float] = None, k_scale: float = 1.0,
+                           max_context_len: int, scale: float, k_scale: float = 1.0,
                            v_scale: float = 1.0, partition_size: int = 0,
                            workspace: Optional[torch.Tensor] = None, err_word: Optional[torch.Tensor] = None,
                            stream=None, kernel: str = "auto") -> torch.Tensor:
@@ -216,8 +215,6 @@ def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 or block_tables.dim() != 2:
         raise ValueError("block_tables and context_lens must be int32")
     MB = block_tables.shape[1]
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
     if workspace is None:          # convenience: a fresh one per call (pass one in to avoid the allocation)
         workspace = make_workspace(S, Hq, Hkv, d, bs, max_context_len, partition_size, device=query.device)
     ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
@@ -231,7 +228,7 @@ def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
 
 def paged_attention_decode_static(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                                   value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
-                                  max_context_len: int, scale: Optional[float] = None, k_scale: float = 1.0,
+                                  max_context_len: int, scale: float, k_scale: float = 1.0,
                                   v_scale: float = 1.0, partition_size: int = 0,
                                   err_word: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """paged_attention_decode without a workspace: the library's fixed device
@@ -243,8 +240,6 @@ def paged_attention_decode_static(out: torch.Tensor, query: torch.Tensor, key_ca
         raise ValueError("shape or dtype mismatch")
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 or block_tables.dim() != 2:
         raise ValueError("block_tables and context_lens must be int32")
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
     _check("paged_attention_decode_static", lib.pkv_paged_attention_decode_static(
         _ptr(out), _ptr(query), dtype_code(query.dtype), _ptr(key_cache), _ptr(value_cache),
         dtype_code(key_cache.dtype), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), S,
@@ -265,7 +260,7 @@ def prefill_workspace_size(S: int, num_query_tokens: int, max_query_len: int, Hq
 def paged_attention_prefill(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                             value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
                             query_start: torch.Tensor, max_query_len: int, max_context_len: int,
-                            scale: Optional[float] = None, partition_size: int = 0,
+                            scale: float, partition_size: int = 0,
                             workspace: Optional[torch.Tensor] = None, err_word: Optional[torch.Tensor] = None,
                             stream=None, kernel: str = "auto") -> torch.Tensor:
     """Several query tokens per sequence, causal.  query/out [T, Hq, d];
@@ -280,8 +275,6 @@ def paged_attention_prefill(out: torch.Tensor, query: torch.Tensor, key_cache: t
         raise ValueError("shape or dtype mismatch")
     if query_start.dtype != torch.int32 or context_lens.dtype != torch.int32 or block_tables.dtype != torch.int32:
         raise ValueError("query_start, context_lens and block_tables must be int32")
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
     if workspace is None:
         n = prefill_workspace_size(S, T, max_query_len, Hq, Hkv, d, bs, max_context_len, partition_size)
         workspace = torch.zeros(max(n, 256), dtype=torch.uint8, device=query.device)
@@ -318,7 +311,7 @@ def copy_blocks(key_caches: Sequence[torch.Tensor], value_caches: Sequence[torch
 def paged_kv_write_decode(out: torch.Tensor, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
                           key_cache: torch.Tensor, value_cache: torch.Tensor, slot_mapping: torch.Tensor,
                           block_tables: torch.Tensor, context_lens: torch.Tensor, max_context_len: int,
-                          scale: Optional[float] = None, k_scale: float = 1.0, v_scale: float = 1.0,
+                          scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
                           partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
                           err_word: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """paged_kv_write of each sequence's new token (key/value [S, Hkv, d],
@@ -334,8 +327,6 @@ def paged_kv_write_decode(out: torch.Tensor, query: torch.Tensor, key: torch.Ten
         raise ValueError("slot_mapping must be int64 [S]")
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 or block_tables.dim() != 2:
         raise ValueError("block_tables and context_lens must be int32")
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
     if workspace is None:
         workspace = make_workspace(S, Hq, Hkv, d, bs, max_context_len, partition_size, device=query.device)
     ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
@@ -349,7 +340,7 @@ def paged_kv_write_decode(out: torch.Tensor, query: torch.Tensor, key: torch.Ten
 
 def token_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                            value_cache: torch.Tensor, token_slots: torch.Tensor, num_tokens: torch.Tensor,
-                           max_tokens: int, scale: Optional[float] = None, k_scale: float = 1.0, v_scale: float = 1.0,
+                           max_tokens: int, scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
                            partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
                            err_word: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Decode through a token table: token_slots int32 [S, MT] lists each
@@ -361,8 +352,6 @@ def token_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
         raise ValueError("shape or dtype mismatch")
     if token_slots.dtype != torch.int32 or num_tokens.dtype != torch.int32 or token_slots.dim() != 2:
         raise ValueError("token_slots and num_tokens must be int32")
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
     if workspace is None:
         workspace = make_workspace(S, Hq, Hkv, d, bs, max_tokens, partition_size, device=query.device)
     ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()

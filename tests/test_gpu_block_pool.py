@@ -103,9 +103,9 @@ def test_manager_drives_write_copy_decode(cache):
     q = W.bf16_bits(q32)
     out = torch.empty((len(sids), Hq, d), dtype=torch.bfloat16, device=dev)
     ws = pkv.make_workspace(len(sids), Hq, Hkv, d, bs, int(cl.max()), 32)
+    scale = float(np.float32(1) / np.sqrt(np.float32(d)))
     pkv.paged_attention_decode(out, torch.from_numpy(q.view(np.int16)).to(dev).view(torch.bfloat16), kc, vc,
                                torch.from_numpy(tab).to(dev), torch.from_numpy(cl).to(dev), int(cl.max()),
-                               k_scale=ks, v_scale=vs, partition_size=32, workspace=ws)
-    ref = O.paged_attention_decode(q, O.BF16, ok_, ov_, odt, tab, cl, float(np.float32(1) / np.sqrt(np.float32(d))),
-                                   ks, vs)
+                               scale=scale, k_scale=ks, v_scale=vs, partition_size=32, workspace=ws)
+    ref = O.paged_attention_decode(q, O.BF16, ok_, ov_, odt, tab, cl, scale, ks, vs)
     assert_close(out, ref, "e4m3" if cache == "e4m3" else "bf16", "manager-driven decode")
