@@ -10,6 +10,12 @@ far larger than L2, so every step streams it from HBM.
 Prints one JSON line (rank 0).  `value` is algorithmic bytes per step
 (query + K/V of the unique blocks read + output + block tables, plus the
 write and copy bytes) over the device-timed step, in GB/s, summed over ranks.
+A default run (no --workload, --S, --partition or --no-workloads) also
+times the same step on the other decode configurations -- the
+Qwen2.5-1.5B-shaped, the 7B-shaped shared-prefix and the two fp8 ones --
+each with at least 200 steps, its own roofline, clocks and a short oracle
+baseline, under the line's `workloads` key; the headline numbers stay
+those of the 72B-shaped workload.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--kernel auto|cuda_cores|tensor_cores] [--impl ours|reference]
@@ -481,20 +487,12 @@ def overlapped_e2e(dev, stream, h_in: dict, out_like, enqueue, steps: int, barri
     return secs, h2d, h_outs[0].numel() * h_outs[0].element_size()
 
 
-def run_ours(args, w: W.Workload):
+def measure_step(args, w: W.Workload, dev, stream, steps: int, warmup: int, ws: int, rank: int, barrier,
+                 e2e: bool = True, partition=None) -> dict:
+    """Time `steps` decode steps of workload `w` (after `warmup` untimed
+    ones) with the K/V pools resident in HBM; returns the line's numbers."""
     import torch
     import paged_kv_cache_44_gb300 as pkv
-
-    ws, rank, local = dist_setup()
-    if ws > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local if ws > 1 else 0)
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.Stream(device=dev)
-    global L2_BYTES
-    L2_BYTES = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or L2_BYTES)
 
     # ---- inputs, resident in HBM before timing
     seed = w.seed + 7919 * rank
@@ -513,7 +511,7 @@ def run_ours(args, w: W.Workload):
     sm = torch.from_numpy(w.slot_mapping).to(dev)
     cow = torch.from_numpy(w.cow_pairs.astype(np.int64)).to(dev)
     out = torch.empty_like(q)
-    P = args.partition if args.partition is not None else w.partition_size
+    P = partition if partition is not None else w.partition_size
     Pres = pkv.decode_partition_size(w.S, w.Hq, w.Hkv, w.d, w.bs, w.max_context_len, P)
     wsp = pkv.make_workspace(w.S, w.Hq, w.Hkv, w.d, w.bs, w.max_context_len, P, device=dev)
     mc = w.max_context_len
@@ -564,19 +562,14 @@ def run_ours(args, w: W.Workload):
             if evc is not None:
                 evc[1].record(stream)
 
-    def barrier():
-        if ws > 1:
-            import torch.distributed as dist
-            dist.barrier(device_ids=[dev.index])
-
     # ---- warm-up
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize(dev)
 
     # ---- timed region: K steps, events on the launching stream
-    dec0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    dec1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    dec0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    dec1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -584,7 +577,7 @@ def run_ours(args, w: W.Workload):
     torch.cuda.synchronize(dev)
     with ClockSampler(uuid) as clk:
         t0.record(stream)
-        for i in range(args.steps):
+        for i in range(steps):
             step(dec0[i], dec1[i])
         t1.record(stream)
         torch.cuda.synchronize(dev)
@@ -592,10 +585,10 @@ def run_ours(args, w: W.Workload):
     ms_total = t0.elapsed_time(t1)
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(dec0, dec1))
     ms_total, dec_ms = max_over_ranks([ms_total, dec_ms], dev)
-    ms_step = ms_total / args.steps
+    ms_step = ms_total / steps
 
     # ---- the step's other calls, timed on their own (outside the timed region)
-    n_parts = max(3, min(args.steps, 200))
+    n_parts = max(3, min(steps, 200))
     evw = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_parts)]
     evc = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_parts)]
     for i in range(n_parts):
@@ -605,29 +598,26 @@ def run_ours(args, w: W.Workload):
     copy_ms = statistics.mean(a.elapsed_time(b) for a, b in evc) if len(w.cow_pairs) else None
 
     # ---- end to end: host buffers in, host result out, through the public API
-    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-    h_in = {k: pin(v) for k, v in dict(q=q, nk=new_k, nv=new_v, bt=bt, cl=cl, sm=sm, cow=cow).items()}
-    e2e_s, h2d, d2h = overlapped_e2e(
-        dev, stream, h_in, out,
-        lambda d, o: step(qq=d["q"], nk=d["nk"], nv=d["nv"], btab=d["bt"], clen=d["cl"], slots=d["sm"],
-                          pairs=d["cow"], o=o),
-        max(3, min(args.steps, 200)), barrier)
-    (e2e_s,) = max_over_ranks([e2e_s], dev)
+    e2e_s = h2d = d2h = None
+    if e2e:
+        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+        h_in = {k: pin(v) for k, v in dict(q=q, nk=new_k, nv=new_v, bt=bt, cl=cl, sm=sm, cow=cow).items()}
+        e2e_s, h2d, d2h = overlapped_e2e(
+            dev, stream, h_in, out,
+            lambda d, o: step(qq=d["q"], nk=d["nk"], nv=d["nv"], btab=d["bt"], clen=d["cl"], slots=d["sm"],
+                              pairs=d["cow"], o=o),
+            max(3, min(steps, 200)), barrier)
+        (e2e_s,) = max_over_ranks([e2e_s], dev)
 
     # ---- numbers
     dbytes = decode_bytes(w) + (write_bytes(w) if fused else 0)
     sbytes = decode_bytes(w) + write_bytes(w) + copy_bytes(w)
-    value = whole_job_gbs(ws, sbytes, ms_step)
     achieved = dbytes / (dec_ms * 1e-3) / 1e9
     peak, peak_kind = peak_hbm()
-    traffic = measured_traffic(w.name, args.kernel) if default_shape(args) else None
-    clocks = clk.summary()
+    traffic = measured_traffic(w.name, args.kernel) if default_shape(args) and partition is None else None
     kname = decode_kernel_name(args.kernel, w)
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if w.cache_dtype == W.DT_BF16 else w.cache_dtype,
-        "data": "synthetic",
+    res = {
+        "value": whole_job_gbs(ws, sbytes, ms_step), "ms_per_step": ms_step, "steps": steps, "warmup": warmup,
         "config": {"workload": w.name, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "bs": w.bs,
                    "cache_dtype": w.cache_dtype, "q_dtype": w.q_dtype, "max_context_len": mc,
                    "partition_size": Pres, "decode_kernel": kname, "fused_write_decode": bool(fused),
@@ -639,6 +629,7 @@ def run_ours(args, w: W.Workload):
         "seq_steps_per_s": round(ws * w.S / (ms_step * 1e-3), 1),
         "decode_gbs": round(achieved, 2),
         "decode_ms": round(dec_ms, 5),
+        "decode_seq_steps_per_s": round(ws * w.S / (dec_ms * 1e-3), 1),
         "write_ms": None if write_ms is None else round(write_ms, 5),
         "copy_blocks_ms": None if copy_ms is None else round(copy_ms, 5),
         "hbm_frac_of_measured": round(achieved / peak, 4),
@@ -648,24 +639,94 @@ def run_ours(args, w: W.Workload):
                      "traffic": None if fused else traffic,
                      "kernel": ("paged_kv_write_decode (" if fused else "paged_attention_decode (") + kname + ")",
                      "algorithmic_bytes_per_launch": dbytes, "launch_ms": round(dec_ms, 5)},
-        "e2e": {"value": round(whole_job_gbs(ws, sbytes, e2e_s * 1e3), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4),
-                "loop": E2E_LOOP},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks,
+        "gpu_launches": launches_per_step * steps,
+        "clocks": clk.summary(),
     }
+    if w.shared_seqs:
+        res["roofline"]["logical_bytes_per_launch"] = decode_bytes(w, unique=False)
+    if e2e:
+        res["e2e"] = {"value": round(whole_job_gbs(ws, sbytes, e2e_s * 1e3), 2), "unit": "GB/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4),
+                      "loop": E2E_LOOP}
+    del pools, kc, vc, wsp
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return res
+
+
+def cpu_baseline(w: W.Workload, seconds: float, one_thread: bool = True) -> dict:
+    """The oracle on a bounded sample of workload `w` (see OracleSampler)."""
+    threads = cpu_threads()
+    sampler = OracleSampler(w, threads)
+    b, spent, n = sampler.run(seconds)
+    rec = {"value": round(b / spent / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+           "sample": sampler.describe(n, spent),
+           "seq_steps_per_s": round(sampler.seq_steps_per_s(b / spent / 1e9), 4)}
+    if one_thread and threads > 1:
+        one = OracleSampler(w, 1)
+        b1, spent1, n1 = one.run(max(1.0, seconds / 4))
+        rec["one_thread"] = {"value": round(b1 / spent1 / 1e9, 4), "unit": "GB/s", "sample": one.describe(n1, spent1)}
+    return rec
+
+
+# The configurations reported beside the headline one in a default run.
+OTHER_WORKLOADS = ("qwen2.5-1.5b", "qwen2.5-7b-prefix", "fp8-bs16", "fp8-bs32")
+OTHER_MIN_STEPS = 200     # short steps (the 1.5B-shaped one is ~40 us): more of them for a stable mean
+
+
+def run_ours(args, w: W.Workload):
+    import torch
+
+    ws, rank, local = dist_setup()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    global L2_BYTES
+    L2_BYTES = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or L2_BYTES)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier(device_ids=[dev.index])
+
+    m = measure_step(args, w, dev, stream, args.steps, args.warmup, ws, rank, barrier, e2e=True,
+                     partition=args.partition)
+    line = {
+        "metric": METRIC, "value": round(m["value"], 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(m["ms_per_step"], 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.cache_dtype == W.DT_BF16 else w.cache_dtype, "data": "synthetic",
+    }
+    for k, v in m.items():
+        if k not in ("value", "ms_per_step", "steps", "warmup"):
+            line[k] = v
     if rank == 0 and not args.no_cpu_baseline:
-        threads = cpu_threads()
-        sampler = OracleSampler(w, threads)
-        b, spent, n = sampler.run(args.cpu_seconds)
-        line["cpu_baseline"] = {"value": round(b / spent / 1e9, 4), "unit": "GB/s", "cores": threads,
-                                "kind": "oracle", "sample": sampler.describe(n, spent),
-                                "seq_steps_per_s": round(sampler.seq_steps_per_s(b / spent / 1e9), 4)}
-        if threads > 1:
-            one = OracleSampler(w, 1)
-            b1, spent1, n1 = one.run(max(1.0, args.cpu_seconds / 4))
-            line["cpu_baseline"]["one_thread"] = {"value": round(b1 / spent1 / 1e9, 4), "unit": "GB/s",
-                                                  "sample": one.describe(n1, spent1)}
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if args.all_workloads:
+        # the other configurations, each as its own decode step (same contract, more steps when short)
+        line["workloads"] = {w.name: {k: line[k] for k in ("decode_ms", "decode_gbs", "hbm_frac_of_measured",
+                                                           "hbm_frac_of_nominal_8tbs", "seq_steps_per_s",
+                                                           "decode_seq_steps_per_s", "roofline", "clocks")}}
+        line["workloads"][w.name].update(steps=args.steps, partition_size=line["config"]["partition_size"],
+                                         headline=True)
+        for name in OTHER_WORKLOADS:
+            w2 = W.make(name)
+            steps2 = max(args.steps, OTHER_MIN_STEPS)
+            m2 = measure_step(args, w2, dev, stream, steps2, args.warmup, ws, rank, barrier, e2e=False)
+            ent = {k: m2[k] for k in ("decode_ms", "decode_gbs", "hbm_frac_of_measured", "hbm_frac_of_nominal_8tbs",
+                                      "seq_steps_per_s", "decode_seq_steps_per_s", "roofline", "clocks",
+                                      "write_ms", "copy_blocks_ms", "gpu_launches")}
+            ent["step_gbs"] = round(m2["value"], 2)
+            ent["ms_per_step"] = round(m2["ms_per_step"], 5)
+            ent["steps"] = steps2
+            ent["config"] = m2["config"]
+            if rank == 0 and not args.no_cpu_baseline:
+                ent["cpu_baseline"] = cpu_baseline(w2, args.other_cpu_seconds, one_thread=False)
+            line["workloads"][name] = ent
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -1035,6 +1096,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--S", type=int, default=None, help="fewer sequences (small profiling cases)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="decode-step: time only the headline workload (a default run also reports the "
+                         "1.5B-, 7B- and fp8-shaped ones under 'workloads')")
+    ap.add_argument("--other-cpu-seconds", type=float, default=3.0,
+                    help="oracle seconds for each of the other workloads' cpu_baseline")
     ap.add_argument("--component", default="decode-step", choices=["decode-step", "prefill", "vtoken",
                                                                    "block-manager"],
                     help="prefill: paged attention over query chunks; block-manager: the host block "
@@ -1045,6 +1111,8 @@ def main():
     if args.component == "block-manager":
         run_block_manager(args)
         return
+    args.all_workloads = (args.component == "decode-step" and args.workload is None and args.S is None and
+                          args.partition is None and not args.no_workloads and args.impl == "ours")
     if args.workload is None:
         args.workload = "qwen2.5-7b-chunked" if args.component == "prefill" else "qwen2.5-72b-long"
     w = W.make(args.workload, S=args.S) if args.S else W.make(args.workload)
