@@ -127,7 +127,7 @@ def test_split_decode_reuses_workspace(cfg):
     w = _sweep_workload(*cfg, seed=77)
     c = build_case(w)
     ref = oracle_decode(c)
-    for P in (w.bs, 64, 128, 512):
+    for P in (w.bs, 64, 128, 512, 0):
         ws = pkv.make_workspace(w.S, w.Hq, w.Hkv, w.d, w.bs, w.max_context_len, P)
         zero = 256
         outs = []

@@ -87,7 +87,7 @@ def test_stale_scratch_does_not_leak_into_a_later_call():
     other sizes and another partition plan then reads only what it wrote."""
     big = _case("qwen2.5-72b-long", [32768, 9000, 4100, 300])
     small = _case("qwen2.5-1.5b", [1, 700, 1500, 3000, 64, 2049])
-    for c, P in ((big, 256), (big, 512), (small, 128), (small, 512), (big, 512)):
+    for c, P in ((big, 256), (big, 512), (small, 0), (small, 128), (small, 512), (big, 512)):
         ref = _allocating_call(c, P)
         out = torch.full_like(c.q, float("nan"))
         assert _static_call(c, out, P) == 0
