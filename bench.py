@@ -567,9 +567,9 @@ def measure_step(args, w: W.Workload, dev, stream, steps: int, warmup: int, ws: 
         step()
     torch.cuda.synchronize(dev)
 
-    # ---- timed region: K steps, events on the launching stream
-    dec0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    dec1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    # ---- timed region: K steps back to back, events on the launching stream around them only
+    # (an event between two kernels keeps the second from starting early: every call after
+    # the first is launched as a programmatic dependent of the one before)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -578,22 +578,25 @@ def measure_step(args, w: W.Workload, dev, stream, steps: int, warmup: int, ws: 
     with ClockSampler(uuid) as clk:
         t0.record(stream)
         for i in range(steps):
-            step(dec0[i], dec1[i])
+            step()
         t1.record(stream)
         torch.cuda.synchronize(dev)
     barrier()
     ms_total = t0.elapsed_time(t1)
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(dec0, dec1))
-    ms_total, dec_ms = max_over_ranks([ms_total, dec_ms], dev)
+    (ms_total,) = max_over_ranks([ms_total], dev)
     ms_step = ms_total / steps
 
-    # ---- the step's other calls, timed on their own (outside the timed region)
+    # ---- each call of the step timed on its own, events around it (outside the timed region)
     n_parts = max(3, min(steps, 200))
-    evw = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_parts)]
-    evc = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_parts)]
+    ev = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))  # noqa: E731
+    evd = [ev() for _ in range(n_parts)]
+    evw = [ev() for _ in range(n_parts)]
+    evc = [ev() for _ in range(n_parts)]
     for i in range(n_parts):
-        step(evw=None if fused else evw[i], evc=evc[i] if len(w.cow_pairs) else None)
+        step(evd[i][0], evd[i][1], evw=None if fused else evw[i], evc=evc[i] if len(w.cow_pairs) else None)
     torch.cuda.synchronize(dev)
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in evd)
+    (dec_ms,) = max_over_ranks([dec_ms], dev)
     write_ms = None if fused else statistics.mean(a.elapsed_time(b) for a, b in evw)
     copy_ms = statistics.mean(a.elapsed_time(b) for a, b in evc) if len(w.cow_pairs) else None
 

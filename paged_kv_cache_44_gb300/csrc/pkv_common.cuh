@@ -15,6 +15,16 @@ struct F32 { using T = float; static constexpr int bytes = 4; };
 struct BF16 { using T = __nv_bfloat16; static constexpr int bytes = 2; };
 struct E4M3 { using T = uint8_t; static constexpr int bytes = 1; };
 
+// Programmatic dependent launch.  The library's kernels are launched so
+// that each may be scheduled while the previous kernel of the stream is
+// still running (once that kernel has called pdl_trigger()).  Every such
+// kernel calls pdl_wait() in every thread before its first access to global
+// memory: it returns once the previous kernel has completed and its writes
+// are visible.  Since no grid can then complete before its predecessor, the
+// stream keeps its order through any chain of such launches.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // Record the first device-side problem; never traps.
 __device__ __forceinline__ void report(int32_t* err, int code) {
     if (err != nullptr) atomicCAS(err, 0, code);

@@ -26,6 +26,8 @@ constexpr int kPerThread = (int)(kChunkVecs / kCopyThreads);
 // read-only mapping: its threads scan all P pairs (16 bytes each, from L2).
 template <bool kCheck>
 __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(const __grid_constant__ CopyParams p) {
+    pdl_trigger();
+    pdl_wait();
     const int pair = blockIdx.x, layer = blockIdx.y, which = blockIdx.z & 1, chunk = blockIdx.z >> 1;
     const long long src = p.mapping[2 * pair], dst = p.mapping[2 * pair + 1];
     const bool first = layer == 0 && blockIdx.z == 0 && threadIdx.x == 0;
@@ -71,11 +73,8 @@ cudaError_t launch_copy(const CopyParams& p, cudaStream_t st) {
     const long long chunks = (n + kChunkVecs - 1) / kChunkVecs;
     if (chunks < 1 || 2 * chunks > 65535) return cudaErrorInvalidValue;
     dim3 grid(p.P, p.L, (unsigned)(2 * chunks));
-    if (p.err != nullptr)
-        copy_blocks_kernel<true><<<grid, kCopyThreads, 0, st>>>(p);
-    else
-        copy_blocks_kernel<false><<<grid, kCopyThreads, 0, st>>>(p);
-    return cudaGetLastError();
+    if (p.err != nullptr) return launch_pdl(copy_blocks_kernel<true>, grid, dim3(kCopyThreads), 0, st, p);
+    return launch_pdl(copy_blocks_kernel<false>, grid, dim3(kCopyThreads), 0, st, p);
 }
 
 }  // namespace pkv

@@ -37,7 +37,8 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
     const int nh = min(kHeads, p.g - set * kHeads);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     // the partition merge that may follow can be scheduled now; it waits for this grid's results
-    asm volatile("griddepcontrol.launch_dependents;");
+    pdl_trigger();
+    pdl_wait();
 
     int n = p.context_lens[s];
     if (n < 0 || n > p.max_ctx) {   // max_ctx <= MB * bs was checked on the host
@@ -167,8 +168,9 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
 // O = sum 2^(m_p - M) acc_p / L, one warp per (sequence, query head), eight
 // warps per CTA (merge_partitions).  Sequences that fit one partition were
 // finished by the decode kernel.  Launched as a programmatic dependent of
-// the decode kernel, which lets it start at once: the lengths are an input
-// of the decode, so they are read before waiting for the decode's results.
+// the decode kernel, so it is resident when the decode ends; every thread
+// waits for the decode before it reads anything, so that this grid never
+// completes before the decode (pdl_wait).
 constexpr int kMergeWarps = 8;
 
 template <int D, typename QF>
@@ -176,13 +178,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_reduce_kernel(DecodeP
     constexpr int E = D / 32;
     const int lane = threadIdx.x & 31;
     const long long gw = (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+    pdl_trigger();
+    pdl_wait();         // the decode's partial results
     if (gw >= (long long)p.S * p.Hq) return;
     const int s = (int)(gw / p.Hq), h = (int)(gw % p.Hq);
     int n = p.context_lens[s];
     n = n < 0 ? 0 : min(n, p.max_ctx);     // same clamp as the decode kernel: np <= Pmax
     const int np = num_partitions(n, p.P, p.Q, p.hold);
     if (np <= 1) return;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t u0 = ((size_t)s * p.Hq + h) * p.Pmax;
     float o[E];
     const float L = merge_partitions<D>(p.part_ml + 2 * u0, p.part_acc + u0 * D, np, lane, o);
@@ -209,10 +212,9 @@ cudaError_t launch_reduce(const DecodeParams& p, cudaStream_t st) {
 
 template <int D, typename QF>
 cudaError_t launch_simt_q(const DecodeParams& p, pkv_dtype c_dt, dim3 grid, cudaStream_t st) {
-    if (c_dt == PKV_F32) decode_simt_kernel<D, QF, F32><<<grid, kThreads, 0, st>>>(p);
-    else if (c_dt == PKV_BF16) decode_simt_kernel<D, QF, BF16><<<grid, kThreads, 0, st>>>(p);
-    else decode_simt_kernel<D, QF, E4M3><<<grid, kThreads, 0, st>>>(p);
-    return cudaGetLastError();
+    if (c_dt == PKV_F32) return launch_pdl(decode_simt_kernel<D, QF, F32>, grid, dim3(kThreads), 0, st, p);
+    if (c_dt == PKV_BF16) return launch_pdl(decode_simt_kernel<D, QF, BF16>, grid, dim3(kThreads), 0, st, p);
+    return launch_pdl(decode_simt_kernel<D, QF, E4M3>, grid, dim3(kThreads), 0, st, p);
 }
 
 }  // namespace

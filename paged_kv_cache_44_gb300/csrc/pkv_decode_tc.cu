@@ -216,13 +216,15 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
     auto lds64 = [&](uint32_t a) { return *reinterpret_cast<const uint2*>(ws + (a - ws_addr)); };
 
     // the partition merge that may follow can be scheduled now; it waits for this grid's results
-    asm volatile("griddepcontrol.launch_dependents;");
+    pdl_trigger();
     if (lane == 0) {
         // through a token table every lane's copies arrive on the stage barrier, and lane 0 once more
         for (int i = 0; i < C::kStages; ++i) mbar_init(bar(i), TT ? 33 : 1);
         fence_barrier_init();
     }
     __syncwarp();
+    // the previous kernel of the stream (a write of the step's tokens, say) is complete from here on
+    pdl_wait();
 
     // K/V is streamed: its lines go first when L2 needs room, so the partial
     // results (kept with "evict last") and the lines of blocks shared by
@@ -777,8 +779,8 @@ cudaError_t launch_one(const DecodeParams& p, int num_sms, cudaStream_t st) {
     unsigned long long want = (units + C::kWarps - 1) / C::kWarps;
     int grid = (int)(want < (unsigned long long)num_sms ? want : (unsigned long long)num_sms);
     if (grid < 1) grid = 1;
-    kern<<<grid, C::kWarps * 32, C::kSmemBytes, st>>>(p, kmap, vmap, units, region_a, nsets);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(C::kWarps * 32), C::kSmemBytes, st, p, kmap, vmap, units, region_a,
+                      nsets);
 }
 
 }  // namespace

@@ -8,6 +8,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <utility>
 
 #include "../../include/pkv.h"
 
@@ -36,6 +37,24 @@ class SmemOptIn {
     std::atomic<bool> done_[kDevices] = {};
     std::mutex mu_;
 };
+
+// Launch `kernel` on `st` as a programmatic dependent of the stream's
+// previous kernel (pdl_wait / pdl_trigger in pkv_common.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 constexpr int kMaxCopyLayers = 256;
 constexpr size_t kWorkspaceHeaderBytes = 256;   // scheduler counters, zero between calls

@@ -409,14 +409,16 @@ __global__ void __launch_bounds__(kPWarps * 32, 1)
 // (merge_partitions): the token's sequence by binary search over
 // query_start, its tile's partition count from the same formula the decode
 // units use.  Launched as a programmatic dependent of the prefill kernel;
-// the lengths and query offsets are inputs of that kernel, so they are read
-// before waiting for its results.
+// every thread waits for that kernel before it reads anything, so that this
+// grid never completes before it (pdl_wait).
 template <int D>
 __global__ void __launch_bounds__(256) prefill_merge_kernel(DecodeParams p, const int32_t* __restrict__ query_start,
                                                             int T, int tile_rows, int max_q) {
     constexpr int E = D / 32;
     const int lane = threadIdx.x & 31;
     const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    pdl_trigger();
+    pdl_wait();
     if (gw >= (long long)T * p.Hq) return;
     const int tq = (int)(gw / p.Hq), h = (int)(gw % p.Hq);
     int lo = 0, hi = p.S;                      // largest s with query_start[s] <= tq
@@ -434,7 +436,6 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(DecodeParams p, cons
     const int key_end = n - ql + last_row / p.g + 1;
     const int np = (key_end + p.P - 1) / p.P;
     if (np <= 1) return;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t u0 = ((size_t)tq * p.Hq + h) * p.Pmax;
     float acc[E];
     const float L = merge_partitions<D>(p.part_ml + 2 * u0, p.part_acc + u0 * D, np, lane, acc);

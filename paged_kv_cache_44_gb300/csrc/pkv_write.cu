@@ -14,6 +14,8 @@ namespace {
 
 template <typename In, typename Out>
 __global__ void __launch_bounds__(256) write_kernel(WriteParams p) {
+    pdl_trigger();
+    pdl_wait();
     const int chunks = p.d / 8;
     const long long total = (long long)p.T * 2 * p.Hkv * chunks;
     const long long slots = (long long)p.NB * p.bs;
@@ -42,6 +44,8 @@ __global__ void __launch_bounds__(256) write_kernel(WriteParams p) {
 
 // bf16 -> bf16 is a pure copy of the bits.
 __global__ void __launch_bounds__(256) write_copy16_kernel(WriteParams p, int elem_bytes) {
+    pdl_trigger();
+    pdl_wait();
     const int chunks = p.d * elem_bytes / 16;
     const long long total = (long long)p.T * 2 * p.Hkv * chunks;
     const long long slots = (long long)p.NB * p.bs;
@@ -77,20 +81,13 @@ cudaError_t launch_write(const WriteParams& p, pkv_dtype in_dt, pkv_dtype cache_
     const long long items = (long long)p.T * 2 * p.Hkv * (same ? p.d * (in_dt == PKV_F32 ? 4 : 2) / 16 : p.d / 8);
     const long long want = (items + threads - 1) / threads;
     const int blocks = (int)(want < 65536 ? want : 65536);
-    if (same) {
-        write_copy16_kernel<<<blocks, threads, 0, st>>>(p, in_dt == PKV_F32 ? 4 : 2);
-    } else if (in_dt == PKV_F32 && cache_dt == PKV_BF16) {
-        write_kernel<F32, BF16><<<blocks, threads, 0, st>>>(p);
-    } else if (in_dt == PKV_BF16 && cache_dt == PKV_F32) {
-        write_kernel<BF16, F32><<<blocks, threads, 0, st>>>(p);
-    } else if (in_dt == PKV_F32 && cache_dt == PKV_FP8_E4M3) {
-        write_kernel<F32, E4M3><<<blocks, threads, 0, st>>>(p);
-    } else if (in_dt == PKV_BF16 && cache_dt == PKV_FP8_E4M3) {
-        write_kernel<BF16, E4M3><<<blocks, threads, 0, st>>>(p);
-    } else {
-        return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
+    const dim3 g(blocks), b(threads);
+    if (same) return launch_pdl(write_copy16_kernel, g, b, 0, st, p, in_dt == PKV_F32 ? 4 : 2);
+    if (in_dt == PKV_F32 && cache_dt == PKV_BF16) return launch_pdl(write_kernel<F32, BF16>, g, b, 0, st, p);
+    if (in_dt == PKV_BF16 && cache_dt == PKV_F32) return launch_pdl(write_kernel<BF16, F32>, g, b, 0, st, p);
+    if (in_dt == PKV_F32 && cache_dt == PKV_FP8_E4M3) return launch_pdl(write_kernel<F32, E4M3>, g, b, 0, st, p);
+    if (in_dt == PKV_BF16 && cache_dt == PKV_FP8_E4M3) return launch_pdl(write_kernel<BF16, E4M3>, g, b, 0, st, p);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace pkv
