@@ -268,7 +268,7 @@ def peak_hbm():
 
 KERNEL_SOURCES = {
     "pkv_decode": ["pkv_decode_tc.cu", "pkv_decode_simt.cu", "pkv_common.cuh", "pkv_tc_common.cuh", "pkv_merge.cuh"],
-    "pkv_prefill": ["pkv_prefill_umma.cu", "pkv_prefill_tc.cu", "pkv_qtile.cuh", "pkv_umma.cuh", "pkv_common.cuh",
+    "pkv_prefill": ["pkv_prefill_umma.cu", "pkv_prefill_umma2.cu", "pkv_prefill_tc.cu", "pkv_qtile.cuh", "pkv_umma.cuh", "pkv_common.cuh",
                     "pkv_tc_common.cuh", "pkv_merge.cuh"],
     "pkv_vtoken": ["pkv_decode_tc.cu", "pkv_decode_simt.cu", "pkv_repack.cu", "pkv_common.cuh", "pkv_tc_common.cuh",
                    "pkv_merge.cuh"],
@@ -754,6 +754,15 @@ def peak_bf16(sustained: bool):
         return (1700.0 if sustained else 1900.0), "fallback"
 
 
+def prefill_kernel_name(kernel: str, w: W.Workload, T: int) -> str:
+    """The kernel a prefill call runs: the library's automatic choice takes
+    two 128-row query tiles per unit when the (sequence, K/V head) pairs
+    average 256 or more (query, head) rows."""
+    if kernel != "auto":
+        return kernel
+    return "tcgen05_2tile" if T * (w.Hq // w.Hkv) >= 2 * 128 * w.S else "tcgen05"
+
+
 def run_prefill(args, w: W.Workload):
     """Paged attention over query chunks: a step is one call over the
     workload's packed queries (chunked prefill next to decodes, or
@@ -842,7 +851,7 @@ def run_prefill(args, w: W.Workload):
         roof = {"bound": "hbm", "achieved": round(per_launch_gbs, 2), "peak": hbm, "unit": "GB/s",
                 "frac": round(per_launch_gbs / hbm, 4), "peak_kind": hbm_kind}
         e2e_v = whole_job_gbs(ws, nbytes, e2e_s * 1e3)
-    kname = "tcgen05" if args.prefill_kernel == "auto" else args.prefill_kernel
+    kname = prefill_kernel_name(args.prefill_kernel, w, T)
     roof.update({"traffic": measured_traffic(w.name, kname, "prefill_traffic.json", "pkv_prefill")
                  if default_shape(args) else None,
                  "kernel": "paged_attention_prefill (%s)" % kname,
@@ -1092,7 +1101,7 @@ def main():
                     help="default: qwen2.5-72b-long (decode-step), qwen2.5-7b-chunked (prefill)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "cuda_cores", "tensor_cores"])
     ap.add_argument("--partition", type=int, default=None)
-    ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "tcgen05", "mma_sync"])
+    ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "tcgen05", "tcgen05_2tile", "mma_sync"])
     ap.add_argument("--fused", action="store_true",
                     help="decode-step: write the new tokens and decode in one launch")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -336,7 +336,7 @@ PKV_API pkv_status pkv_paged_attention_decode_static(void* out, const void* quer
  * 256 bytes zero before first use.  max_query_len >= every q_len and
  * max_context_len >= every length (host values that size the launch).
  * Supported: bf16 query and bf16 cache (tensor cores), d in {64, 128}, bs in
- * {16, 32}; anything else returns PKV_ERR_UNSUPPORTED.  Runs the tcgen05
+ * {16, 32}; anything else returns PKV_ERR_UNSUPPORTED.  Runs a tcgen05
  * kernel (PKV_PREFILL_AUTO of pkv_paged_attention_prefill_ex).
  */
 PKV_API size_t pkv_prefill_workspace_size(int S, int num_query_tokens, int max_query_len, int Hq, int Hkv, int d,
@@ -354,10 +354,13 @@ PKV_API pkv_status pkv_paged_attention_prefill(void* out, const void* query, pkv
 
 /* Kernel choice for pkv_paged_attention_prefill_ex. */
 typedef enum {
-    PKV_PREFILL_AUTO = 0,         /* the tcgen05 kernel */
+    PKV_PREFILL_AUTO = 0,         /* a tcgen05 kernel: two tiles per unit when the (sequence, K/V head)
+                                     pairs average 256 or more (query, head) rows, else one */
     PKV_PREFILL_MMA_SYNC = 1,     /* warp-level mma.sync: tiles of 16 (query, head) rows, one warp each */
-    PKV_PREFILL_TCGEN05 = 2       /* tcgen05.mma with tensor-memory accumulators: tiles of 128 rows,
+    PKV_PREFILL_TCGEN05 = 2,      /* tcgen05.mma with tensor-memory accumulators: tiles of 128 rows,
                                      one CTA each */
+    PKV_PREFILL_TCGEN05_2TILE = 3 /* the same with two 128-row tiles per unit reading each K/V stage
+                                     once, each tile with its own softmax warpgroup */
 } pkv_prefill_kernel;
 
 /*

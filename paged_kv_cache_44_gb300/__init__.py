@@ -248,7 +248,7 @@ def paged_attention_decode_static(out: torch.Tensor, query: torch.Tensor, key_ca
     return out
 
 
-PREFILL_KERNELS = {"auto": 0, "mma_sync": 1, "tcgen05": 2}
+PREFILL_KERNELS = {"auto": 0, "mma_sync": 1, "tcgen05": 2, "tcgen05_2tile": 3}
 
 
 def prefill_workspace_size(S: int, num_query_tokens: int, max_query_len: int, Hq: int, Hkv: int, d: int,
@@ -265,7 +265,8 @@ def paged_attention_prefill(out: torch.Tensor, query: torch.Tensor, key_cache: t
                             stream=None, kernel: str = "auto") -> torch.Tensor:
     """Several query tokens per sequence, causal.  query/out [T, Hq, d];
     query_start int32 [S+1] (device); caches [NB, bs, Hkv, d].  kernel:
-    "auto" / "tcgen05" (tensor-memory accumulators) or "mma_sync"."""
+    "auto", "tcgen05" (tensor-memory accumulators, one 128-row tile per
+    unit), "tcgen05_2tile" (two tiles per unit) or "mma_sync"."""
     if kernel not in PREFILL_KERNELS:
         raise ValueError(f"kernel must be one of {sorted(PREFILL_KERNELS)}")
     T, Hq, d = query.shape

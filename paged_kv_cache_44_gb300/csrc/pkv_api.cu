@@ -21,6 +21,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kTargetUnits = 152LL * 8 * 4;
 constexpr int kMinDefaultPartition = 512;
 constexpr long long kPrefillTargetUnits = 152LL * 4;
+constexpr int kPrefillTileRows = 128;       // (query, head) rows per tcgen05 tile
 constexpr int kHeadSet = 8;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -477,7 +478,7 @@ pkv_status pkv_paged_attention_prefill_ex(void* out, const void* query, pkv_dtyp
                                           int NB, float scale, int partition_size, void* workspace,
                                           size_t workspace_bytes, int32_t* err_word, pkv_stream_t stream,
                                           int kernel) {
-    if (kernel < PKV_PREFILL_AUTO || kernel > PKV_PREFILL_TCGEN05) return PKV_ERR_INVALID_ARG;
+    if (kernel < PKV_PREFILL_AUTO || kernel > PKV_PREFILL_TCGEN05_2TILE) return PKV_ERR_INVALID_ARG;
     if (S < 0 || MB < 1 || NB < 1 || Hkv < 1 || Hq < 1 || max_context_len < 0 || num_query_tokens < 0 ||
         max_query_len < 0 || max_query_len > max_context_len)
         return PKV_ERR_INVALID_ARG;
@@ -520,6 +521,14 @@ pkv_status pkv_paged_attention_prefill_ex(void* out, const void* query, pkv_dtyp
     if (kernel == PKV_PREFILL_MMA_SYNC)
         return from_cuda(launch_prefill_tc(p, query_start, num_query_tokens, max_query_len, num_sms_current(),
                                            pl.split, st));
+    // two query tiles per unit pay when a (sequence, K/V head) has 256 or
+    // more (query, head) rows on average: prompt chunks, not speculative tokens
+    const bool two_tiles = kernel == PKV_PREFILL_TCGEN05_2TILE ||
+                           (kernel == PKV_PREFILL_AUTO &&
+                            (long long)num_query_tokens * (Hq / Hkv) >= 2LL * kPrefillTileRows * S);
+    if (two_tiles)
+        return from_cuda(launch_prefill_umma2(p, query_start, num_query_tokens, max_query_len, num_sms_current(),
+                                              pl.split, st));
     return from_cuda(launch_prefill_umma(p, query_start, num_query_tokens, max_query_len, num_sms_current(),
                                          pl.split, st));
 }

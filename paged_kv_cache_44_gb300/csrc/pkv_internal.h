@@ -152,6 +152,9 @@ cudaError_t launch_prefill_tc(const DecodeParams& p, const int32_t* query_start,
                               bool merge, cudaStream_t st);
 cudaError_t launch_prefill_umma(const DecodeParams& p, const int32_t* query_start, int T, int max_q_len, int num_sms,
                                 bool merge, cudaStream_t st);
+// the same with two 128-row query tiles per unit sharing each K/V stage
+cudaError_t launch_prefill_umma2(const DecodeParams& p, const int32_t* query_start, int T, int max_q_len,
+                                 int num_sms, bool merge, cudaStream_t st);
 cudaError_t launch_prefill_merge(const DecodeParams& p, const int32_t* query_start, int T, int tile_rows,
                                  int max_q, cudaStream_t st);
 // 2-D tensor map over a bf16 K or V cache [NB * bs tokens, Hkv * d]: boxes of

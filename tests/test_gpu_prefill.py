@@ -26,7 +26,7 @@ def _case(name, lens, qlens, Hq=None, Hkv=None, d=None, seed=7):
     return w, hv, qs, q32
 
 
-KERNELS = ["tcgen05", "mma_sync"]
+KERNELS = ["tcgen05", "tcgen05_2tile", "mma_sync"]
 
 
 def _run(w, hv, qs, q32, partition, dev="cuda", query_start=None, err=None, max_query_len=None, kernel="auto"):
