@@ -20,9 +20,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 // workspace size and the launch always agree.
 constexpr long long kTargetUnits = 152LL * 8 * 4;
 constexpr int kMinDefaultPartition = 512;
-// 1.5 units per worker warp of a full GB300 (152 SMs x 6 bf16 workers)
-constexpr long long kSmallLaunchUnits = 152LL * 6 * 3 / 2;
-constexpr int kMinSmallPartition = 256;
 constexpr long long kPrefillTargetUnits = 152LL * 4;
 constexpr int kPrefillTileRows = 128;       // (query, head) rows per tcgen05 tile
 constexpr int kHeadSet = 8;
@@ -45,12 +42,6 @@ int resolve_partition(int S, int Hq, int Hkv, int d, int bs, int max_ctx, int re
     if (sets == 0 || max_ctx <= kMinDefaultPartition) return 0;
     int P = 1 << 20;
     while (P > kMinDefaultPartition && sets * ((max_ctx + P - 1) / P) < kTargetUnits) P >>= 1;
-    // A small launch -- fewer than 1.5 units per worker warp even if every
-    // sequence had the maximum length -- gives each warp one long unit
-    // streamed at a single warp's latency-bound rate: take the largest
-    // partition, in steps of 128 tokens down to 256, that gives 1.5 units per
-    // warp at the maximum length.
-    while (P > kMinSmallPartition && sets * ((max_ctx + P - 1) / P) < kSmallLaunchUnits) P -= 128;
     if (P >= max_ctx) return 0;
     return P;
 }
