@@ -135,9 +135,14 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.uuid, "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
+            # the sampler is live before the timed region starts: wait for its first reading
+            t0 = time.perf_counter()
+            while not self.lines and time.perf_counter() - t0 < 3.0 and self.proc.poll() is None:
+                time.sleep(0.005)
+            self._skip = len(self.lines)
         except (OSError, ValueError):
             self.proc = None
         return self
@@ -159,7 +164,13 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        # readings taken during the timed region; a region shorter than the sampling
+        # interval may have none, and then the reading taken just before it stands in
+        lines = self.lines[getattr(self, "_skip", 0):]
+        before = not lines
+        if before:
+            lines = self.lines[-1:]
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -173,8 +184,10 @@ class ClockSampler:
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        if before:
+            out["sampled_before_region"] = True
+        return out
 
 
 # ----------------------------------------------------------- CPU baseline
@@ -488,9 +501,10 @@ def overlapped_e2e(dev, stream, h_in: dict, out_like, enqueue, steps: int, barri
 
 
 def measure_step(args, w: W.Workload, dev, stream, steps: int, warmup: int, ws: int, rank: int, barrier,
-                 e2e: bool = True, partition=None) -> dict:
+                 e2e: bool = True, partition=None, min_seconds: float = 0.0) -> dict:
     """Time `steps` decode steps of workload `w` (after `warmup` untimed
-    ones) with the K/V pools resident in HBM; returns the line's numbers."""
+    ones; more steps if they would take under `min_seconds`) with the K/V
+    pools resident in HBM; returns the line's numbers."""
     import torch
     import paged_kv_cache_44_gb300 as pkv
 
@@ -562,10 +576,17 @@ def measure_step(args, w: W.Workload, dev, stream, steps: int, warmup: int, ws: 
             if evc is not None:
                 evc[1].record(stream)
 
-    # ---- warm-up
+    # ---- warm-up (timed, to size a timed region that must last a minimum time)
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
     for _ in range(warmup):
         step()
+    w1.record(stream)
     torch.cuda.synchronize(dev)
+    if min_seconds > 0:
+        est = w0.elapsed_time(w1) / max(1, warmup) * 1e-3
+        steps = max(steps, int(math.ceil(min_seconds / max(est, 1e-6))))
+        (steps,) = (int(v) for v in max_over_ranks([steps], dev))   # every rank times the same count
 
     # ---- timed region: K steps back to back, events on the launching stream around them only
     # (an event between two kernels keeps the second from starting early: every call after
@@ -675,6 +696,7 @@ def cpu_baseline(w: W.Workload, seconds: float, one_thread: bool = True) -> dict
 # The configurations reported beside the headline one in a default run.
 OTHER_WORKLOADS = ("qwen2.5-1.5b", "qwen2.5-7b-prefix", "fp8-bs16", "fp8-bs32")
 OTHER_MIN_STEPS = 200     # short steps (the 1.5B-shaped one is ~40 us): more of them for a stable mean
+OTHER_MIN_SECONDS = 0.3   # and a timed region long enough for the clock sampler to read the clocks in it
 
 
 def run_ours(args, w: W.Workload):
@@ -719,13 +741,14 @@ def run_ours(args, w: W.Workload):
         for name in OTHER_WORKLOADS:
             w2 = W.make(name)
             steps2 = max(args.steps, OTHER_MIN_STEPS)
-            m2 = measure_step(args, w2, dev, stream, steps2, args.warmup, ws, rank, barrier, e2e=False)
+            m2 = measure_step(args, w2, dev, stream, steps2, args.warmup, ws, rank, barrier, e2e=False,
+                              min_seconds=OTHER_MIN_SECONDS)
             ent = {k: m2[k] for k in ("decode_ms", "decode_gbs", "hbm_frac_of_measured", "hbm_frac_of_nominal_8tbs",
                                       "seq_steps_per_s", "decode_seq_steps_per_s", "roofline", "clocks",
                                       "write_ms", "copy_blocks_ms", "gpu_launches")}
             ent["step_gbs"] = round(m2["value"], 2)
             ent["ms_per_step"] = round(m2["ms_per_step"], 5)
-            ent["steps"] = steps2
+            ent["steps"] = m2["steps"]
             ent["config"] = m2["config"]
             if rank == 0 and not args.no_cpu_baseline:
                 ent["cpu_baseline"] = cpu_baseline(w2, args.other_cpu_seconds, one_thread=False)
