@@ -60,6 +60,7 @@ def l2_note(pool_bytes: int, n_pools: int) -> str:
     return "not flushed: %d copies of a %.0f MB pool" % (n_pools, pool_bytes / 1e6)
 FALLBACK_HBM_GBS = 6800.0
 ELEM = {W.DT_F32: 4, W.DT_BF16: 2, W.DT_E4M3: 1}
+TORCH_DT = {W.DT_F32: "float32", W.DT_BF16: "bfloat16", W.DT_E4M3: "float8_e4m3fn"}   # torch dtype names
 
 
 # ------------------------------------------------------------- byte counts
@@ -526,7 +527,11 @@ def measure_step(args, w: W.Workload, dev, stream, steps: int, warmup: int, ws: 
     cow = torch.from_numpy(w.cow_pairs.astype(np.int64)).to(dev)
     out = torch.empty_like(q)
     P = partition if partition is not None else w.partition_size
-    Pres = pkv.decode_partition_size(w.S, w.Hq, w.Hkv, w.d, w.bs, w.max_context_len, P)
+    # the partition the decode launches with (for an E4M3 cache on the tensor cores it may be
+    # twice the one the workspace is planned for)
+    Pres = pkv.decode_launch_partition_size(w.S, w.Hq, w.Hkv, w.d, w.bs, w.NB, w.max_context_len, P,
+                                            getattr(torch, TORCH_DT[w.q_dtype]),
+                                            getattr(torch, TORCH_DT[w.cache_dtype]), args.kernel)
     wsp = pkv.make_workspace(w.S, w.Hq, w.Hkv, w.d, w.bs, w.max_context_len, P, device=dev)
     mc = w.max_context_len
     split = Pres > 0 and -(-mc // Pres) > 1
@@ -607,8 +612,12 @@ def measure_step(args, w: W.Workload, dev, stream, steps: int, warmup: int, ws: 
     (ms_total,) = max_over_ranks([ms_total], dev)
     ms_step = ms_total / steps
 
-    # ---- each call of the step timed on its own, events around it (outside the timed region)
+    # ---- each call of the step timed on its own, events around it (outside the timed region).
+    # A sleep kernel holds the stream while the host queues the calls, so that no interval
+    # includes the GPU waiting for the host (a 40 us call is about as long as queueing it).
     n_parts = max(3, min(steps, 200))
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(0.02 * 2.0e9))
     ev = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))  # noqa: E731
     evd = [ev() for _ in range(n_parts)]
     evw = [ev() for _ in range(n_parts)]

@@ -121,7 +121,9 @@ PKV_API size_t pkv_decode_workspace_size(int S, int Hq, int Hkv, int d, int bs,
 /*
  * Partition size (tokens) that a decode with these arguments will use:
  * the request itself when it is > 0, no split (returns 0) when it is -1,
- * and the library's choice when it is 0.  Returns -1 for invalid arguments.
+ * and the library's choice when it is 0 (an E4M3 cache on the tensor-core
+ * kernel may then take twice this size, in the same workspace; see
+ * pkv_paged_attention_decode).  Returns -1 for invalid arguments.
  */
 PKV_API int pkv_decode_partition_size(int S, int Hq, int Hkv, int d, int bs,
                               int max_context_len, int partition_size);
@@ -155,7 +157,12 @@ PKV_API int pkv_decode_partition_size(int S, int Hq, int Hkv, int d, int bs,
  * pieces of work.  With an E4M3 cache on the tensor-core kernel, a sequence
  * of four or more full partitions has its last full partition cut into
  * chunks too.  partition_size: 0 = library choice,
- * -1 = never split, > 0 = that size.  When any sequence may span more than
+ * -1 = never split, > 0 = that size.  The library's choice depends on the
+ * sizes alone (so does the workspace size); an E4M3 cache on the
+ * tensor-core kernel then takes twice that partition where the launch keeps
+ * at least half as many units and the same workspace holds its partial
+ * results (its units are bound by their own arithmetic, and fewer, longer
+ * ones end the launch sooner).  When any sequence may span more than
  * one partition, `workspace` must hold pkv_decode_workspace_size(...) bytes,
  * else PKV_ERR_WORKSPACE is returned.
  *
@@ -228,6 +235,20 @@ PKV_API pkv_status pkv_paged_attention_decode_ex(void* out, const void* query, p
                                          int partition_size,
                                          void* workspace, size_t workspace_bytes,
                                          int32_t* err_word, pkv_stream_t stream, int kernel);
+
+/*
+ * Partition size (tokens) a decode launch with these arguments uses:
+ * pkv_decode_partition_size's answer, except that with the library's choice
+ * (partition_size 0) an E4M3 cache on the tensor-core kernel may take twice
+ * it (see pkv_paged_attention_decode; the workspace size is the same).
+ * `kernel` is a pkv_decode_kernel; NB is the number of cache blocks.  The
+ * paged decode, the fused write + decode and the token-table decode follow
+ * the same rule.  Returns 0 for no split, -1 for invalid arguments.
+ * Touches no device memory.
+ */
+PKV_API int pkv_decode_launch_partition_size(int S, int Hq, int Hkv, int d, int bs, int NB,
+                                             int max_context_len, int partition_size,
+                                             pkv_dtype q_dtype, pkv_dtype cache_dtype, int kernel);
 
 /*
  * copy_blocks -- copy-on-write duplication of physical blocks.

@@ -33,6 +33,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported dtype or shape",
           3: "workspace missing or too small", 4: "CUDA launch failed"}
 
 EXPORTED = ("pkv_paged_kv_write", "pkv_decode_workspace_size", "pkv_decode_partition_size",
+            "pkv_decode_launch_partition_size",
             "pkv_paged_attention_decode", "pkv_paged_attention_decode_ex", "pkv_copy_blocks",
             "pkv_status_string", "pkv_version", "pkv_paged_attention_decode_static",
             "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_set_extra_key", "pkv_pool_num_free_blocks",
@@ -64,6 +65,8 @@ def _load() -> ctypes.CDLL:
     lib.pkv_decode_workspace_size.restype = sz
     lib.pkv_decode_partition_size.argtypes = [i32] * 7
     lib.pkv_decode_partition_size.restype = i32
+    lib.pkv_decode_launch_partition_size.argtypes = [i32] * 11
+    lib.pkv_decode_launch_partition_size.restype = i32
     dec = [vp, vp, i32, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, f32, f32, f32, i32,
            vp, sz, vp, vp]
     lib.pkv_paged_attention_decode.argtypes = dec
@@ -185,6 +188,14 @@ def paged_kv_write(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tens
 def decode_partition_size(S: int, Hq: int, Hkv: int, d: int, bs: int, max_context_len: int,
                           partition_size: int = 0) -> int:
     return int(lib.pkv_decode_partition_size(S, Hq, Hkv, d, bs, max_context_len, partition_size))
+
+
+def decode_launch_partition_size(S: int, Hq: int, Hkv: int, d: int, bs: int, NB: int, max_context_len: int,
+                                 partition_size: int, q_dtype: torch.dtype, cache_dtype: torch.dtype,
+                                 kernel: str = "auto") -> int:
+    return int(lib.pkv_decode_launch_partition_size(S, Hq, Hkv, d, bs, NB, max_context_len, partition_size,
+                                                    dtype_code(q_dtype), dtype_code(cache_dtype),
+                                                    KERNELS[kernel]))
 
 
 def decode_workspace_size(S: int, Hq: int, Hkv: int, d: int, bs: int, max_context_len: int,

@@ -9,6 +9,7 @@ import re
 import subprocess
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -74,6 +75,27 @@ def test_workspace_plan(pkv):
     assert P > 0 and P % 16 == 0
 
 
+
+def test_launch_partition(pkv):
+    """The decode launch's partition: the plan's, except that an E4M3 cache
+    on the tensor-core kernel with the library's choice takes twice it where
+    half the planned units remain (128 sequences of up to 16,384 tokens, 4
+    K/V heads: 1,024 planned, 2,048 launched); never for a request, a bf16
+    cache, the CUDA-core kernel, or a batch too small to keep the units."""
+    bf, e4 = torch.bfloat16, torch.float8_e4m3fn
+    args = (128, 28, 4, 128, 16, 65536, 16384)
+    assert pkv.decode_partition_size(*args[:5], 16384, 0) == 1024
+    assert pkv.decode_launch_partition_size(*args, 0, bf, e4) == 2048
+    assert pkv.decode_launch_partition_size(*args, 0, bf, e4, "tensor_cores") == 2048
+    assert pkv.decode_launch_partition_size(*args, 0, bf, e4, "cuda_cores") == 1024
+    assert pkv.decode_launch_partition_size(*args, 0, bf, bf) == 1024
+    assert pkv.decode_launch_partition_size(*args, 512, bf, e4) == 512
+    assert pkv.decode_launch_partition_size(*args, -1, bf, e4) == 0
+    # 16 sequences: 512 planned (the floor); 1,024 would leave too few units
+    assert pkv.decode_launch_partition_size(16, 28, 4, 128, 16, 65536, 16384, 0, bf, e4) == 512
+    assert pkv.decode_launch_partition_size(*args, 24, bf, e4) == -1
+
+
 def _layout_rows(n, P, hold):
     """Partial results of a sequence of n tokens, restated from the layout
     include/pkv.h describes: full partitions of P tokens, the rest in chunks
@@ -87,6 +109,19 @@ def _layout_rows(n, P, hold):
     if hold and Q < P and full >= 4:
         full -= 1
     return full + -(-(n - full * P) // Q)
+
+
+def test_doubled_partition_fits_the_planned_workspace():
+    """An E4M3 decode on the tensor-core kernel may run with twice the
+    planned partition in the workspace planned for it: for every maximum
+    length, no sequence up to it has more partial results with partitions of
+    2P (held back or not) than the plan's rows for P hold."""
+    for P in (256, 512, 1024, 2048):
+        plan = doubled = 0
+        for n in range(0, 13 * P + 1):
+            plan = max(plan, _layout_rows(n, P, False), _layout_rows(n, P, True))
+            doubled = max(doubled, _layout_rows(n, 2 * P, False), _layout_rows(n, 2 * P, True))
+            assert doubled <= plan, (P, n)
 
 
 @pytest.mark.parametrize("P", [16, 64, 128, 256, 512, 768, 1024])
