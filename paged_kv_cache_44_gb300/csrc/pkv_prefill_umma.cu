@@ -597,23 +597,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // fast path x = scl * s enters through one fused multiply-add
                 const float mb = m_ref == -CUDART_INF_F ? 0.f : m_ref;
                 const float xs = whole ? scl : 1.f;
-                float ls[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+                // pairs of columns through paired fp32 instructions: the same roundings
+                // and the same eight partial sums as one scalar lane at a time
+                const uint64_t xs2 = umma::f2_pack(xs, xs), nmb2 = umma::f2_pack(-mb, -mb);
+                uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int hq = 0; hq < 2; ++hq) {
                     uint32_t pw[32];
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
                         const int t = 64 * hq + 2 * k;
-                        const float a0 = fast_exp2(fmaf(__uint_as_float(sr[t >> 5][t & 31]), xs, -mb));
-                        const float a1 = fast_exp2(fmaf(__uint_as_float(sr[(t + 1) >> 5][(t + 1) & 31]), xs, -mb));
-                        ls[(2 * k) & 7] += a0;
-                        ls[(2 * k + 1) & 7] += a1;
+                        const uint64_t s01 = umma::f2_pack(__uint_as_float(sr[t >> 5][t & 31]),
+                                                           __uint_as_float(sr[(t + 1) >> 5][(t + 1) & 31]));
+                        float x0, x1;
+                        umma::f2_unpack(umma::f2_fma(s01, xs2, nmb2), x0, x1);
+                        const float a0 = fast_exp2(x0), a1 = fast_exp2(x1);
+                        ls2[k & 3] = umma::f2_add(ls2[k & 3], umma::f2_pack(a0, a1));
                         pw[k] = pack2<false>(a0, a1);
                     }
                     umma::tmem_st32(tmem + lane_base + b * kTok + 32 * hq, pw);
                 }
+                float ls[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) umma::f2_unpack(ls2[k], ls[2 * k], ls[2 * k + 1]);
                 l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
                 umma::tmem_wait_st();
                 umma::fence_before_sync();

@@ -1,8 +1,9 @@
 // Fifth-generation tensor core building blocks (tcgen05, sm_100 family):
 // shared-memory matrix descriptors, the instruction descriptor of a bf16
 // MMA with fp32 accumulation, the MMA itself (both operands in shared
-// memory), completion tracking through an mbarrier, and tensor-memory
-// (TMEM) allocation, loads and stores.
+// memory), completion tracking through an mbarrier, tensor-memory (TMEM)
+// allocation, loads and stores, and the paired fp32 arithmetic of the same
+// SM generation.
 //
 // Operand layout used throughout: 128-byte swizzled, rows of 128 bytes,
 // 8-row atoms of 1024 bytes.
@@ -88,6 +89,27 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// two fp32 values in one 64-bit register, for the paired arithmetic of the
+// fifth-generation SM (fma.rn.f32x2, add.rn.f32x2: one instruction, two
+// lanes, each rounded as its scalar form)
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
