@@ -75,6 +75,25 @@ def test_workspace_plan(pkv):
     assert P > 0 and P % 16 == 0
 
 
+def test_default_partition_rules(pkv):
+    """The library's partition from the sizes alone: about four units per
+    worker warp of a full GB300 (halving from 2^20 down to 512 tokens); a
+    small launch (under 1.5 units per bf16 worker warp at the maximum
+    length) then shrinks in 128-token steps down to 256."""
+    # 72B-shaped: 32 x 8 head sets, 32K tokens -> 1024 (the bench's 512 is a request)
+    assert pkv.decode_partition_size(32, 64, 8, 128, 16, 32768, 0) == 1024
+    # 7B-shaped: 256 x 4 head sets, 8K tokens -> 1024
+    assert pkv.decode_partition_size(256, 28, 4, 128, 16, 8192, 0) == 1024
+    # 1.5B-shaped: 64 x 2 head sets, 4K tokens: 512 gives 1,024 units < 1,368 -> 384 (1,408 units)
+    assert pkv.decode_partition_size(64, 12, 2, 128, 16, 4096, 0) == 384
+    # a handful of sequences: down to the 256-token floor
+    assert pkv.decode_partition_size(4, 12, 2, 128, 16, 4096, 0) == 256
+    # short contexts are not split
+    assert pkv.decode_partition_size(64, 12, 2, 128, 16, 512, 0) == 0
+    # the workspace follows the same choice
+    assert pkv.decode_workspace_size(64, 12, 2, 128, 16, 4096, 0) == pkv.decode_workspace_size(64, 12, 2, 128, 16, 4096, 384)
+
+
 
 def test_launch_partition(pkv):
     """The decode launch's partition: the plan's, except that an E4M3 cache
