@@ -3,6 +3,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "pkv_common.cuh"
@@ -151,6 +153,22 @@ int num_sms_current() {
 }
 
 }  // namespace
+
+CUcontext current_context() {
+    static std::once_flag once;
+    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    });
+    CUcontext ctx = nullptr;
+    if (fn == nullptr || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+    return ctx;
+}
+
 }  // namespace pkv
 
 using namespace pkv;

@@ -14,9 +14,17 @@
 
 namespace pkv {
 
+// The calling thread's current CUDA context (the driver's cuCtxGetCurrent,
+// reached through the runtime's entry-point query), or nullptr when there is
+// none or the query is unavailable.  A device reset gives a device ordinal a
+// new primary context, in which per-context state (module globals, kernel
+// attributes) starts afresh: caches keyed by ordinal alone would outlive it.
+CUcontext current_context();
+
 // A kernel's opt-in to more than 48 KB of dynamic shared memory, made once
-// per device (the attribute is per device and context).  One instance per
-// kernel; safe when several host threads make their first call at once.
+// per device and context (the attribute belongs to the context).  One
+// instance per kernel; safe when several host threads make their first call
+// at once.
 class SmemOptIn {
   public:
     cudaError_t ensure(const void* kernel, int bytes) {
@@ -24,17 +32,19 @@ class SmemOptIn {
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
         const bool cached = dev >= 0 && dev < kDevices;
-        if (cached && done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+        CUcontext ctx = current_context();
+        if (cached && ctx != nullptr && done_[dev].load(std::memory_order_acquire) == ctx) return cudaSuccess;
         std::lock_guard<std::mutex> lock(mu_);
-        if (cached && done_[dev].load(std::memory_order_relaxed)) return cudaSuccess;
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e == cudaSuccess && cached) done_[dev].store(true, std::memory_order_release);
+        // the call makes the device's primary context current if it was not yet
+        if (e == cudaSuccess && cached && (ctx = current_context()) != nullptr)
+            done_[dev].store(ctx, std::memory_order_release);
         return e;
     }
 
   private:
     static constexpr int kDevices = 64;
-    std::atomic<bool> done_[kDevices] = {};
+    std::atomic<CUcontext> done_[kDevices] = {};
     std::mutex mu_;
 };
 

@@ -10,7 +10,6 @@
 // with scratch that lives in a fixed array in device memory, owned by the
 // library for the life of the process.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 
 #include <mutex>
 
@@ -35,36 +34,25 @@ struct ScratchSlot {
 std::mutex g_mu;
 ScratchSlot g_slots[kMaxDevices] = {};
 
-PFN_cuCtxGetCurrent_v4000 ctx_get_current() {
-    static std::once_flag once;
-    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
-    });
-    return fn;
-}
-
 // Device address of g_decode_scratch on device `dev`, which must be the
 // current device.  In host code the array's name is only a host-side
 // stand-in, so the address is looked up with cudaGetSymbolAddress, once per
 // device and context, and cached.
 pkv_status scratch_on_device(int dev, void** addr) {
     if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_UNSUPPORTED;
-    auto get_ctx = ctx_get_current();
-    if (get_ctx == nullptr) return PKV_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);
-    CUcontext ctx = nullptr;
-    if (get_ctx(&ctx) != CUDA_SUCCESS) return PKV_ERR_CUDA;
+    CUcontext ctx = pkv::current_context();
     ScratchSlot& slot = g_slots[dev];
     if (slot.addr == nullptr || ctx == nullptr || ctx != slot.ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return PKV_ERR_CUDA;
-        // the lookup makes the device's primary context current if it was not yet
-        if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return PKV_ERR_CUDA;
+        // the lookup makes the device's primary context current if it was not yet; without a
+        // context to key it by, the address is used for this call and not kept
+        ctx = pkv::current_context();
+        if (ctx == nullptr) {
+            *addr = p;
+            return PKV_OK;
+        }
         slot.ctx = ctx;
         slot.addr = p;
     }
