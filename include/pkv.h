@@ -243,8 +243,9 @@ PKV_API pkv_status pkv_paged_attention_decode_ex(void* out, const void* query, p
  * it (see pkv_paged_attention_decode; the workspace size is the same).
  * `kernel` is a pkv_decode_kernel; NB is the number of cache blocks.  The
  * paged decode, the fused write + decode and the token-table decode follow
- * the same rule.  Returns 0 for no split, -1 for invalid arguments.
- * Touches no device memory.
+ * the same rule.  Returns 0 for no split, -1 for invalid arguments (and
+ * for PKV_DECODE_TENSOR_CORES where that kernel does not apply).  Touches
+ * no device memory.
  */
 PKV_API int pkv_decode_launch_partition_size(int S, int Hq, int Hkv, int d, int bs, int NB,
                                              int max_context_len, int partition_size,

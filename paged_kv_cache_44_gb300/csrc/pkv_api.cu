@@ -218,9 +218,13 @@ int pkv_decode_partition_size(int S, int Hq, int Hkv, int d, int bs, int max_con
 int pkv_decode_launch_partition_size(int S, int Hq, int Hkv, int d, int bs, int NB, int max_context_len,
                                      int partition_size, pkv_dtype q_dtype, pkv_dtype cache_dtype, int kernel) {
     if (kernel < PKV_DECODE_AUTO || kernel > PKV_DECODE_TENSOR_CORES || NB < 1) return -1;
+    if (q_dtype != PKV_F32 && q_dtype != PKV_BF16) return -1;
+    if (cache_dtype != PKV_F32 && cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3) return -1;
     const int P = resolve_partition(S, Hq, Hkv, d, bs, max_context_len, partition_size);
     if (P < 0) return -1;
-    const bool use_tc = kernel != PKV_DECODE_CUDA_CORES && decode_tc_supports(q_dtype, cache_dtype, d, bs, NB);
+    const bool tc_ok = decode_tc_supports(q_dtype, cache_dtype, d, bs, NB);
+    if (kernel == PKV_DECODE_TENSOR_CORES && !tc_ok) return -1;      // the decode would refuse it
+    const bool use_tc = kernel != PKV_DECODE_CUDA_CORES && tc_ok;
     const DecodePlan pl = make_plan(S, Hq, d, max_context_len, P);
     return launch_partition(pl, S, Hq, Hkv, max_context_len, partition_size, use_tc && cache_dtype == PKV_FP8_E4M3);
 }

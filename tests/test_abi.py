@@ -113,6 +113,10 @@ def test_launch_partition(pkv):
     # 16 sequences: 512 planned (the floor); 1,024 would leave too few units
     assert pkv.decode_launch_partition_size(16, 28, 4, 128, 16, 65536, 16384, 0, bf, e4) == 512
     assert pkv.decode_launch_partition_size(*args, 24, bf, e4) == -1
+    # the tensor-core kernel needs a bf16 query with a bf16 cache, or an E4M3 cache
+    assert pkv.decode_launch_partition_size(*args, 0, torch.float32, torch.float32, "tensor_cores") == -1
+    assert pkv.decode_launch_partition_size(*args, 0, torch.float32, torch.float32) == 1024
+    assert pkv.lib.pkv_decode_launch_partition_size(*args, 0, 1, 7, 0) == -1      # no such cache dtype
 
 
 def _layout_rows(n, P, hold):
