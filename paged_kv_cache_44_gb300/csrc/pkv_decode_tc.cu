@@ -60,7 +60,9 @@ using namespace tc;
 
 // Tuning knobs: workers per CTA, stages per worker, tokens per stage, for
 // bf16 and for E4M3 caches (E4M3 does more arithmetic per byte and wants
-// more workers).
+// more workers).  With two stages, 11 E4M3 workers with a bf16 query are as
+// many as shared memory holds (20 KB each: stages and query slots); an fp32
+// query's larger slots leave room for 9.
 #ifndef PKV_TC_WARPS_BF16
 #define PKV_TC_WARPS_BF16 6
 #endif
@@ -71,7 +73,7 @@ using namespace tc;
 #define PKV_TC_TOK_BF16 32
 #endif
 #ifndef PKV_TC_WARPS_FP8
-#define PKV_TC_WARPS_FP8 10
+#define PKV_TC_WARPS_FP8 11
 #endif
 #ifndef PKV_TC_STAGES_FP8
 #define PKV_TC_STAGES_FP8 2
