@@ -22,9 +22,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 // workspace size and the launch always agree.
 constexpr long long kTargetUnits = 152LL * 8 * 4;
 constexpr int kMinDefaultPartition = 512;
-// A small launch: fewer than 1.5 units per worker warp of a full GB300
-// (152 SMs x 6 bf16 workers) even if every sequence had the maximum length.
-constexpr long long kSmallLaunchUnits = 152LL * 6 * 3 / 2;
+// A small launch: fewer than about 1.3 units per worker warp of a full
+// GB300 (152 SMs x 7 bf16 workers) even if every sequence had the maximum
+// length.
+constexpr long long kSmallLaunchUnits = 152LL * 9;
 constexpr int kMinSmallPartition = 256;
 constexpr long long kPrefillTargetUnits = 152LL * 4;
 constexpr int kPrefillTileRows = 128;       // (query, head) rows per tcgen05 tile
@@ -51,9 +52,9 @@ int resolve_partition(int S, int Hq, int Hkv, int d, int bs, int max_ctx, int re
     // A small launch gives each worker warp about one long unit, streamed at
     // a single warp's latency-bound rate, and the longest units set the
     // launch's length: take the largest partition, in steps of 128 tokens
-    // down to 256, that gives 1.5 units per warp at the maximum length.
+    // down to 256, that gives that many units at the maximum length.
     // 64 sequences of 512..4096 tokens, 2 K/V heads: 384 instead of 512,
-    // decode 35.4-35.7 vs 37.7-38.0 us over three runs each.
+    // decode 35.3-35.4 vs 37.5-37.9 us (256: 38.1, 320: 35.6, 448: 36.0).
     while (P > kMinSmallPartition && sets * ((max_ctx + P - 1) / P) < kSmallLaunchUnits) P -= 128;
     if (P >= max_ctx) return 0;
     return P;

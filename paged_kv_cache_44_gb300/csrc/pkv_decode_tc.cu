@@ -17,7 +17,9 @@
 // the 128-byte swizzle (64-byte for 64-byte rows) so that tensor-core
 // operand loads are free of bank conflicts.  Copies complete on the stage's
 // mbarrier.  The warp keeps up to kStages-1 stages in flight while it works
-// on one, and it prefetches across unit boundaries.
+// on one, and it prefetches across unit boundaries: the next unit's first
+// stage, and (bf16 query) its query fragments, loaded into registers when
+// the unit is claimed.
 //
 // Math per stage (mma.sync m16n8k16, fp32 accumulate):
 //   S^T[16 tokens x 8 heads] = K[16 x d] . Q^T[d x 8]          (d/16 MMAs per 16 tokens)
@@ -60,11 +62,11 @@ using namespace tc;
 
 // Tuning knobs: workers per CTA, stages per worker, tokens per stage, for
 // bf16 and for E4M3 caches (E4M3 does more arithmetic per byte and wants
-// more workers).  With two stages, 11 E4M3 workers with a bf16 query are as
-// many as shared memory holds (20 KB each: stages and query slots); an fp32
-// query's larger slots leave room for 9.
+// more workers).  With two stages a bf16 worker takes 32 KB of shared
+// memory, so 7 are as many as fit; 11 E4M3 workers (16 KB each) keep within
+// the registers of a 170-register thread.
 #ifndef PKV_TC_WARPS_BF16
-#define PKV_TC_WARPS_BF16 6
+#define PKV_TC_WARPS_BF16 7
 #endif
 #ifndef PKV_TC_STAGES_BF16
 #define PKV_TC_STAGES_BF16 2
@@ -99,13 +101,10 @@ struct Cfg {
     // queued units (claimed, first stage issued, not yet started): at most
     // one per stage in flight
     static constexpr int kQueue = kStages;
-    // each queued unit's query rows (up to 8 heads) land in a slot of their own
-    static constexpr int kQSlotBytes = kHeadsPerUnit * D * QB;
-    // shared memory: every worker's stages and query slots (1024-byte
-    // aligned), then one trailer with each worker's barriers, stage masks and
-    // unit queue
-    static constexpr int kQOff = kStages * kStageBytes;
-    static constexpr int kWarpBytes = (kQOff + kQueue * kQSlotBytes + 1023) / 1024 * 1024;
+    // shared memory: every worker's stages (1024-byte aligned), then one
+    // trailer with each worker's barriers, stage masks and unit queue.  The
+    // query goes to registers (see qn in the kernel), not to shared memory.
+    static constexpr int kWarpBytes = (kStages * kStageBytes + 1023) / 1024 * 1024;
     // trailer per worker: barriers (8 B each), stage masks (4 B each), then
     // the unit queue (32-byte entries, 16-byte aligned)
     static constexpr int kQueueCtlOff = (8 * kStages + 4 * kStages + 15) / 16 * 16;
@@ -216,6 +215,36 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
     auto stage_v = [&](int i) { return ws_addr + i * C::kStageBytes + C::kPartBytes; };
     auto lds128 = [&](uint32_t a) { return *reinterpret_cast<const uint4*>(ws + (a - ws_addr)); };
     auto lds64 = [&](uint32_t a) { return *reinterpret_cast<const uint2*>(ws + (a - ws_addr)); };
+    // query column of fragment k-step ks: this lane's pairs (d0, d0 + 1) and (d1, d1 + 1)
+    auto q_cols = [&](int ks, int& d0, int& d1) {
+        if constexpr (FP8) {
+            d0 = 64 * (ks / 4) + 16 * c + 4 * (ks % 4);      // 4 consecutive d: j = 0..3
+            d1 = d0 + 2;
+        } else {
+            d0 = 16 * ks + 2 * c;
+            d1 = d0 + 8;
+        }
+    };
+    // A bf16 query's fragments for the oldest claimed unit that has not started, as the
+    // 32-bit words (bf16 pairs) of head r of the lane, zero past the unit's heads: loaded
+    // when that unit is claimed, or when the unit before it starts, so they are in
+    // registers by the unit's start.
+    uint32_t qn[C::KS][2];
+    int qn_for = -1;                      // queue index of the unit they belong to; -1: free
+    auto load_qn = [&](int s, int h0, int nh) {
+        if constexpr (QF::bytes == 2) {
+            const bool hv = r < nh;
+            const uint32_t* qw = reinterpret_cast<const uint32_t*>(
+                static_cast<const unsigned char*>(p.q) + ((size_t)s * p.Hq + h0 + (hv ? r : 0)) * D * 2);
+#pragma unroll
+            for (int ks = 0; ks < C::KS; ++ks) {
+                int d0, d1;
+                q_cols(ks, d0, d1);
+                qn[ks][0] = hv ? __ldg(qw + d0 / 2) : 0u;
+                qn[ks][1] = hv ? __ldg(qw + d1 / 2) : 0u;
+            }
+        }
+    };
 
     // the partition merge that may follow can be scheduled now; it waits for this grid's results
     pdl_trigger();
@@ -243,7 +272,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
     bool claiming = true;
     bool i_have = false;
     Unit iu{};
-    int i_stage = 0, i_nst = 0, i_qslot = 0;
+    int i_stage = 0, i_nst = 0;
     unsigned g_issue = 0, q_tail = 0;
 
     auto claim = [&](unsigned long long& u) -> bool {
@@ -289,11 +318,14 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
                 return false;
             }
             unit_of(p, u, nsets, region_a, iu);
-            i_qslot = q_tail % C::kQueue;
             if (lane == 0) {
-                int4* e = reinterpret_cast<int4*>(queue + i_qslot);
+                int4* e = reinterpret_cast<int4*>(queue + q_tail % C::kQueue);
                 e[0] = make_int4(iu.s, iu.kvh, iu.h0, iu.nh);
                 e[1] = make_int4(iu.part, iu.t0, iu.t1, iu.np);
+            }
+            if (qn_for < 0) {
+                load_qn(iu.s, iu.h0, iu.nh);
+                qn_for = (int)q_tail;
             }
             ++q_tail;
             i_have = true;
@@ -306,8 +338,6 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
                 tab_next = load_chunk(1);
             }
         }
-        // the unit's query rows ride on its first stage
-        const uint32_t q_bytes = i_stage == 0 ? (uint32_t)(iu.nh * D * QF::bytes) : 0u;
         const int slot = g_issue % C::kStages;
         const int ts = iu.t0 + i_stage * kTok;
         const int tn = min(kTok, iu.t1 - ts);
@@ -342,11 +372,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
             cp_async_mbar_arrive_noinc(bar(slot));
             if (lane == 0) {
                 masks[slot] = m;
-                mbar_arrive_expect_tx(bar(slot), q_bytes);
-                if (q_bytes)
-                    bulk_load(ws_addr + C::kQOff + i_qslot * C::kQSlotBytes,
-                              static_cast<const unsigned char*>(p.q) + ((size_t)iu.s * p.Hq + iu.h0) * D * QF::bytes,
-                              q_bytes, bar(slot));
+                mbar_arrive_expect_tx(bar(slot), 0u);
             }
             ++g_issue;
             ++i_stage;
@@ -374,11 +400,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
         const int pb_box = __shfl_sync(0xffffffffu, tab, ((rs + b * box_rows) / p.bs) & 31);
         if (lane == 0) {
             masks[slot] = m;
-            mbar_arrive_expect_tx(bar(slot), nissue * box_bytes + q_bytes);
-            if (q_bytes)
-                bulk_load(ws_addr + C::kQOff + i_qslot * C::kQSlotBytes,
-                          static_cast<const unsigned char*>(p.q) + ((size_t)iu.s * p.Hq + iu.h0) * D * QF::bytes,
-                          q_bytes, bar(slot));
+            mbar_arrive_expect_tx(bar(slot), nissue * box_bytes);
         }
         __syncwarp();
         if (box_live) {
@@ -397,7 +419,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
     unsigned g_cons = 0, q_head = 0;
     bool have_unit = false, need_q = false;
     Unit cu{};
-    int c_stage = 0, c_nst = 0, c_qslot = 0;
+    int c_stage = 0, c_nst = 0;
     uint32_t qf[C::KS][2];                // Q^T fragments (n = head r)
     float o[C::KS][4];                    // O^T accumulators, m-tile t of d
     float m_run[2], l_run[2];             // heads 2c, 2c+1
@@ -463,7 +485,6 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
             c_stage = 0;
             c_nst = (cu.t1 - cu.t0 + kTok - 1) / kTok;
             have_unit = true;
-            c_qslot = (q_head - 1) % C::kQueue;
             need_q = true;
 #pragma unroll
             for (int t = 0; t < C::KS; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
@@ -485,29 +506,43 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
         }
         if (__any_sync(0xffffffffu, bail)) break;
         if (need_q) {
-            // Q^T fragments of head r from the unit's query slot (zero past its heads)
             need_q = false;
-            const bool hv = r < cu.nh;
-            const unsigned char* qs = ws + C::kQOff + c_qslot * C::kQSlotBytes + (size_t)(hv ? r : 0) * D * QF::bytes;
+            if constexpr (QF::bytes == 2) {
+                // this unit's query is in qn (it is the oldest started unit); bf16 pairs as
+                // they are, or widened and rounded to fp16 pairs for an E4M3 cache
 #pragma unroll
-            for (int ks = 0; ks < C::KS; ++ks) {
-                int d0, d1;
-                if constexpr (FP8) {
-                    d0 = 64 * (ks / 4) + 16 * c + 4 * (ks % 4);      // 4 consecutive d: j = 0..3
-                    d1 = d0 + 2;
-                } else {
-                    d0 = 16 * ks + 2 * c;
-                    d1 = d0 + 8;
+                for (int ks = 0; ks < C::KS; ++ks)
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const uint32_t w = qn[ks][k];
+                        qf[ks][k] = FP8 ? pack2<true>(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)) : w;
+                    }
+                qn_for = -1;
+                if (q_tail > q_head) {
+                    // the next queued unit's query, loaded now to be ready at its start
+                    const int4 a = reinterpret_cast<const int4*>(queue + q_head % C::kQueue)[0];
+                    load_qn(a.x, a.z, a.w);
+                    qn_for = (int)q_head;
                 }
-                float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-                if (hv) {
-                    x0 = load_elem<QF>(qs, d0);
-                    x1 = load_elem<QF>(qs, d0 + 1);
-                    x2 = load_elem<QF>(qs, d1);
-                    x3 = load_elem<QF>(qs, d1 + 1);
+            } else {
+                // an fp32 query: head r of the unit read at its start (zero past its heads)
+                const bool hv = r < cu.nh;
+                const unsigned char* qs = static_cast<const unsigned char*>(p.q) +
+                                          ((size_t)cu.s * p.Hq + cu.h0 + (hv ? r : 0)) * D * QF::bytes;
+#pragma unroll
+                for (int ks = 0; ks < C::KS; ++ks) {
+                    int d0, d1;
+                    q_cols(ks, d0, d1);
+                    float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+                    if (hv) {
+                        x0 = load_elem<QF>(qs, d0);
+                        x1 = load_elem<QF>(qs, d0 + 1);
+                        x2 = load_elem<QF>(qs, d1);
+                        x3 = load_elem<QF>(qs, d1 + 1);
+                    }
+                    qf[ks][0] = pack2<FP8>(x0, x1);
+                    qf[ks][1] = pack2<FP8>(x2, x3);
                 }
-                qf[ks][0] = pack2<FP8>(x0, x1);
-                qf[ks][1] = pack2<FP8>(x2, x3);
             }
         }
         const uint32_t vmask = masks[slot];

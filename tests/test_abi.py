@@ -78,8 +78,8 @@ def test_workspace_plan(pkv):
 def test_default_partition_rules(pkv):
     """The library's partition from the sizes alone: about four units per
     worker warp of a full GB300 (halving from 2^20 down to 512 tokens); a
-    small launch (under 1.5 units per bf16 worker warp at the maximum
-    length) then shrinks in 128-token steps down to 256."""
+    small launch (under 1,368 units, about 1.3 per bf16 worker warp, at the
+    maximum length) then shrinks in 128-token steps down to 256."""
     # 72B-shaped: 32 x 8 head sets, 32K tokens -> 1024 (the bench's 512 is a request)
     assert pkv.decode_partition_size(32, 64, 8, 128, 16, 32768, 0) == 1024
     # 7B-shaped: 256 x 4 head sets, 8K tokens -> 1024
