@@ -63,8 +63,8 @@ using namespace tc;
 // Tuning knobs: workers per CTA, stages per worker, tokens per stage, for
 // bf16 and for E4M3 caches (E4M3 does more arithmetic per byte and wants
 // more workers).  With two stages a bf16 worker takes 32 KB of shared
-// memory, so 7 are as many as fit; 11 E4M3 workers (16 KB each) keep within
-// the registers of a 170-register thread.
+// memory, so 7 are as many as fit.  An E4M3 worker takes 16 KB; 11 measured
+// fastest (12: 1.2% slower; 13 no longer fit their registers).
 #ifndef PKV_TC_WARPS_BF16
 #define PKV_TC_WARPS_BF16 7
 #endif
