@@ -120,8 +120,37 @@ def prefill_bytes(w: W.Workload, qlens: np.ndarray) -> int:
 
 # ------------------------------------------------------------------ clocks
 
+# A clock sampler through NVML, the library nvidia-smi reads from (read-only calls:
+# the SM clock, its maximum, the clock-event reasons), polling every PERIOD seconds
+# and printing nvidia-smi's CSV fields; it runs as a process of its own so that it
+# takes no time from the thread that queues the timed work.
+NVML_SAMPLER = r"""
+import ctypes, sys, time
+uuid, period = sys.argv[1], float(sys.argv[2])
+lib = ctypes.CDLL("libnvidia-ml.so.1")
+if lib.nvmlInit_v2() != 0:
+    sys.exit(3)
+h = ctypes.c_void_p()
+if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+    sys.exit(4)
+get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or lib.nvmlDeviceGetCurrentClocksThrottleReasons
+sm, mx, r = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+flag = lambda v, b: "Active" if v & b else "Not Active"
+while True:
+    if (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0 and
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and get_reasons(h, ctypes.byref(r)) == 0):
+        v = r.value
+        # hw slowdown (with the hardware power brake), hw thermal, sw thermal, sw power cap
+        print(sm.value, mx.value, "-", hex(v), flag(v, 0x88), flag(v, 0x40), flag(v, 0x20), flag(v, 0x4), sep=", ", flush=True)
+    time.sleep(period)
+"""
+NVML_PERIOD_S = 0.002
+
+
 class ClockSampler:
-    """Samples SM clock and throttle reasons with nvidia-smi while running."""
+    """Samples the SM clock and the clock-event (throttle) reasons while the
+    timed region runs: through NVML every 2 ms where the driver's library
+    loads, else with nvidia-smi every 20 ms."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -131,28 +160,40 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self._t = None
+        self.source = None
+
+    def _start(self, cmd) -> bool:
+        """Starts a sampler process; true once it has printed its first reading."""
+        self.lines = []
+        self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+        t0 = time.perf_counter()
+        while not self.lines and time.perf_counter() - t0 < 5.0 and self.proc.poll() is None:
+            time.sleep(0.005)
+        if self.lines:
+            return True
+        self._stop()
+        return False
 
     def __enter__(self):
+        # the sampler is live before the timed region starts: its first reading is in
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", self.uuid, "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self._t = threading.Thread(target=self._read, daemon=True)
-            self._t.start()
-            # the sampler is live before the timed region starts: wait for its first reading
-            t0 = time.perf_counter()
-            while not self.lines and time.perf_counter() - t0 < 3.0 and self.proc.poll() is None:
-                time.sleep(0.005)
-            self._skip = len(self.lines)
+            if self._start([sys.executable, "-c", NVML_SAMPLER, self.uuid, str(NVML_PERIOD_S)]):
+                self.source = "nvml, %g ms" % (NVML_PERIOD_S * 1e3)
+            elif self._start(["nvidia-smi", "-i", self.uuid, "--query-gpu=" + self.FIELDS,
+                              "--format=csv,noheader,nounits", "-lms", "20"]):
+                self.source = "nvidia-smi, 20 ms"
         except (OSError, ValueError):
             self.proc = None
+        self._skip = len(self.lines)
         return self
 
     def _read(self):
         for ln in self.proc.stdout:
             self.lines.append(ln.strip())
 
-    def __exit__(self, *a):
+    def _stop(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -161,6 +202,10 @@ class ClockSampler:
                 self.proc.kill()
             if self._t is not None:
                 self._t.join(timeout=2)
+        self.proc = None
+
+    def __exit__(self, *a):
+        self._stop()
 
     def summary(self):
         sm, mx, reasons = [], None, set()
@@ -185,7 +230,8 @@ class ClockSampler:
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+               "sampler": self.source}
         if before:
             out["sampled_before_region"] = True
         return out
