@@ -5,8 +5,9 @@
  * comment says "host".  Every call is asynchronous on `stream`: it validates
  * its arguments on the host, enqueues kernels, and returns without waiting
  * for the GPU.  No call allocates memory or synchronises the host, so the
- * calls can be recorded into a CUDA graph.  The caller owns every buffer,
- * including the decode workspace.
+ * write, decode and copy calls can be recorded into a CUDA graph (tested);
+ * pkv_paged_attention_decode_static is described on its own below.  The
+ * caller owns every buffer, including the decode workspace.
  *
  * Layouts (all row-major, contiguous, 16-byte aligned base pointers):
  *   new tokens  key / value        [T,  Hkv, d]
@@ -315,10 +316,9 @@ PKV_API pkv_status pkv_copy_blocks(void* const* key_caches, void* const* value_c
  *    current device's); a stream of another device gives
  *    PKV_ERR_INVALID_ARG and nothing is enqueued.
  *  - The first call on a device looks up the array's device address (with
- *    that device current) and caches it with the device's CUDA context;
- *    make that first call before any stream capture.  After a device reset
- *    (a new context) the next call looks the address up again, so it too
- *    should come before any capture.
+ *    that device current) and caches it with the device's CUDA context.
+ *    After a device reset (a new context) the next call looks the address
+ *    up again.
  *  - Each call clears the array's 256-byte work-counter header on `stream`
  *    (a memset) before the decode; the rest keeps the previous call's
  *    contents and needs no clearing.
