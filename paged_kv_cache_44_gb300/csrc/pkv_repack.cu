@@ -25,20 +25,39 @@ __device__ __forceinline__ bool move_ok(const RepackParams& p, int m, int64_t& s
            p.token_slots[seq * p.MT + idx] == src;
 }
 
-// grid (moves, layers); a block copies one token's K and V rows of one layer
-__global__ void __launch_bounds__(128) repack_copy_kernel(const __grid_constant__ RepackParams p) {
+// grid (moves / 8, layers), a warp per move: the token's K and V rows of one
+// layer, each lane's 16-byte loads issued before its stores
+constexpr int kMovesPerBlock = 8;
+__global__ void __launch_bounds__(32 * kMovesPerBlock) repack_copy_kernel(const __grid_constant__ RepackParams p) {
+    const int lane = threadIdx.x & 31;
+    const long long m = (long long)blockIdx.x * kMovesPerBlock + (threadIdx.x >> 5);
     int64_t seq, idx, src, dst;
-    if (!move_ok(p, blockIdx.x, seq, idx, src, dst)) return;
+    if (m >= p.M || !move_ok(p, (int)m, seq, idx, src, dst)) return;
     const int l = blockIdx.y;
     const size_t n16 = p.token_bytes / 16;
     const uint4* ks = reinterpret_cast<const uint4*>(static_cast<const char*>(p.k[l]) + src * p.token_bytes);
     const uint4* vs = reinterpret_cast<const uint4*>(static_cast<const char*>(p.v[l]) + src * p.token_bytes);
     uint4* kd = reinterpret_cast<uint4*>(static_cast<char*>(p.k[l]) + dst * p.token_bytes);
     uint4* vd = reinterpret_cast<uint4*>(static_cast<char*>(p.v[l]) + dst * p.token_bytes);
-    for (size_t i = threadIdx.x; i < n16; i += blockDim.x) {
-        const uint4 a = ks[i], b = vs[i];
-        kd[i] = a;
-        vd[i] = b;
+    constexpr int kBatch = 4;            // chunks of K (and of V) per lane in flight
+    for (size_t i0 = 0; i0 < n16; i0 += 32 * kBatch) {
+        uint4 a[kBatch], b[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const size_t i = i0 + 32 * j + lane;
+            if (i < n16) {
+                a[j] = ks[i];
+                b[j] = vs[i];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const size_t i = i0 + 32 * j + lane;
+            if (i < n16) {
+                kd[i] = a[j];
+                vd[i] = b[j];
+            }
+        }
     }
 }
 
@@ -58,7 +77,8 @@ __global__ void __launch_bounds__(256) repack_table_kernel(const __grid_constant
 
 cudaError_t launch_repack(const RepackParams& p, cudaStream_t st) {
     if (p.M == 0 || p.L == 0) return cudaSuccess;
-    repack_copy_kernel<<<dim3((unsigned)p.M, (unsigned)p.L), 128, 0, st>>>(p);
+    repack_copy_kernel<<<dim3((unsigned)((p.M + kMovesPerBlock - 1) / kMovesPerBlock), (unsigned)p.L),
+                         32 * kMovesPerBlock, 0, st>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     repack_table_kernel<<<(unsigned)((p.M + 255) / 256), 256, 0, st>>>(p);
