@@ -7,8 +7,9 @@
 // streaming.
 //
 // Work unit: (sequence, K/V head, set of <= 8 query heads, partition of P
-// tokens).  Each warp is an independent worker: it claims units from a
-// counter in the workspace header (or takes them round-robin without one),
+// tokens).  Each warp is an independent worker: it takes its first unit by
+// its index and claims the rest from a counter in the workspace header (or
+// takes them round-robin without one),
 // and streams the unit's K/V through its own ring of shared-memory stages.
 // A stage is 32 tokens of K and V for one K/V head.  The cache is seen by
 // the TMA engine as a 2-D tensor [NB * bs rows, Hkv * d elements]; one
@@ -275,12 +276,22 @@ __global__ void __launch_bounds__(Cfg<D, FP8, QF::bytes>::kWarps * 32, 1)
     int i_stage = 0, i_nst = 0;
     unsigned g_issue = 0, q_tail = 0;
 
+    // A worker's first unit is taken without the counter: unit (warp * CTAs +
+    // CTA), a one-to-one map of the first round of units onto the workers
+    // that spreads consecutive units (neighbouring sequences) over the SMs as
+    // the counter's arrival order does, and saves the contended atomic of the
+    // launch's ramp.  Later claims come from the counter, offset by the
+    // number of workers.
+    bool first_claim = true;
     auto claim = [&](unsigned long long& u) -> bool {
         for (;;) {
             unsigned long long v = 0;
-            if (lane == 0) {
+            if (first_claim) {
+                v = (unsigned long long)warp * gridDim.x + blockIdx.x;   // consecutive units on different SMs
+                first_claim = false;
+            } else if (lane == 0) {
                 if (p.sched != nullptr) {
-                    v = atomicAdd(reinterpret_cast<unsigned long long*>(p.sched), 1ull);
+                    v = atomicAdd(reinterpret_cast<unsigned long long*>(p.sched), 1ull) + total_warps;
                 } else {
                     v = static_next;
                 }
