@@ -341,6 +341,54 @@ def test_conflicting_copy_pairs_are_skipped_and_reported(layers):
         np.testing.assert_array_equal(_np_cache(kcs[layer]), oks[layer])
 
 
+# ------------------------------------------------------------ maximum sizes
+
+def _bounded(out, c, w):
+    """Finite, and within max |V| (every output is a convex combination of V rows)."""
+    of = out.float()
+    assert torch.isfinite(of).all()
+    vmax = 448.0 * c.v_scale if w.cache_dtype == W.DT_E4M3 else float(c.v_cache.float().abs().max())
+    assert float(of.abs().max()) <= vmax * 1.01 + 1e-3
+
+
+@pytest.mark.parametrize("cache", [W.DT_BF16, W.DT_E4M3])
+def test_largest_batch(cache):
+    """65,535 sequences, the most one decode takes, of 1..64 tokens: unsplit
+    and in 16-token partitions (a merge grid of 65,535 blocks of 8 rows, a
+    CUDA-core grid of 65,535 sequences).  A sample of sequences (shortest,
+    longest, random) against the oracle; every output finite and bounded."""
+    import dataclasses
+    lens = np.random.default_rng(5).integers(1, 65, size=65535)
+    w = dataclasses.replace(W.make("qwen2.5-1.5b", S=65535, lengths=lens), Hq=8, Hkv=1, d=64, cache_dtype=cache)
+    c = build_case(w, sample=256)
+    ref = oracle_decode(c)
+    rows = torch.from_numpy(c.seqs).cuda()
+    for P in (-1, 16):
+        for kernel in _kernels_for(w):
+            out = gpu_decode(c, partition_size=P, kernel=kernel)
+            assert_close(out[rows], ref, w.cache_dtype, f"S=65535 P={P} {kernel}")
+            _bounded(out, c, w)
+
+
+@pytest.mark.parametrize("cache", [W.DT_BF16, W.DT_E4M3])
+def test_longest_context(cache):
+    """A 262,143-token sequence beside a 5-token one: the library's partition
+    (about a thousand partial results per row, merged 16 at a time) and
+    unsplit (one unit streams the whole sequence).  Every output against the
+    oracle."""
+    import dataclasses
+    lens = np.array([262143, 5])
+    w = dataclasses.replace(W.make("qwen2.5-1.5b", S=2, lengths=lens), Hq=8, Hkv=1, d=64, cache_dtype=cache)
+    c = build_case(w)
+    ref = oracle_decode(c)
+    assert pkv.decode_partition_size(w.S, w.Hq, w.Hkv, w.d, w.bs, w.max_context_len, 0) > 0
+    for P in (0, -1):
+        for kernel in _kernels_for(w):
+            out = gpu_decode(c, partition_size=P, kernel=kernel)
+            assert_close(out, ref, w.cache_dtype, f"262,143 tokens P={P} {kernel}")
+            _bounded(out, c, w)
+
+
 # ------------------------------------------------------------ full-size runs
 
 FULL = [("qwen2.5-1.5b", None), ("qwen2.5-7b-prefix", None), ("qwen2.5-72b-long", 3), ("fp8-bs16", 4),
