@@ -341,6 +341,27 @@ def test_conflicting_copy_pairs_are_skipped_and_reported(layers):
         np.testing.assert_array_equal(_np_cache(kcs[layer]), oks[layer])
 
 
+def test_decode_growing_logits_rescale():
+    """Keys scaled by 1 + t / 40 along each sequence: every stage's largest
+    logit exceeds all earlier ones by far more than 2^8, so the running
+    output is rescaled at nearly every stage and each partition starts from
+    its own maximum; split or not, the result matches the oracle."""
+    from tests.gpu_cases import host_raw, to_device
+    lens = np.array([1, 40, 700, 1100, 2049])
+    w = W.make("qwen2.5-1.5b", S=len(lens), lengths=lens)
+    c = build_case(w)
+    for s_ in range(w.S):
+        for t in range(int(w.context_lens[s_])):
+            c.hv.k_pool[int(w.block_tables[s_, t // w.bs]), t % w.bs] *= np.float32(1.0 + t / 40.0)
+    c.k_cache = to_device(c.hv.k_pool, w.cache_dtype)
+    c.o_k = host_raw(c.hv.k_pool, w.cache_dtype)
+    ref = oracle_decode(c)
+    for kernel in _kernels_for(w):
+        for P in (-1, 0, 128, 16):
+            out = gpu_decode(c, partition_size=P, kernel=kernel)
+            assert_close(out, ref, w.cache_dtype, f"growing logits {kernel} P={P}")
+
+
 # ------------------------------------------------------------ maximum sizes
 
 def _bounded(out, c, w):

@@ -61,6 +61,8 @@ CASES = [
     ("qwen2.5-1.5b", [5, 600, 1500], 8, 1, 128, W.DT_BF16, 0.9),
     ("fp8-bs32", [33, 700, 1400], 16, 2, 128, W.DT_E4M3, 0.5),
     ("fp8-bs16", [100, 900], 8, 2, 64, W.DT_E4M3, 0.25),
+    # a 262,143-token table with half its tokens live (131,284), beside a short one
+    ("qwen2.5-1.5b", [262143, 7], 8, 1, 64, W.DT_BF16, 0.5),
 ]
 
 
