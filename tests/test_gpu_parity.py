@@ -374,14 +374,21 @@ def _bounded(out, c, w):
 
 @pytest.mark.parametrize("cache", [W.DT_BF16, W.DT_E4M3])
 def test_largest_batch(cache):
-    """65,535 sequences, the most one decode takes, of 1..64 tokens: unsplit
-    and in 16-token partitions (a merge grid of 65,535 blocks of 8 rows, a
+    """65,535 sequences, the most one decode takes, of 1..64 tokens: first
+    the write of each sequence's new token (65,535 tokens in one launch,
+    bit-exact on the sampled sequences' blocks), then the decode unsplit and
+    in 16-token partitions (a merge grid of 65,535 blocks of 8 rows, a
     CUDA-core grid of 65,535 sequences).  A sample of sequences (shortest,
     longest, random) against the oracle; every output finite and bounded."""
     import dataclasses
     lens = np.random.default_rng(5).integers(1, 65, size=65535)
     w = dataclasses.replace(W.make("qwen2.5-1.5b", S=65535, lengths=lens), Hq=8, Hkv=1, d=64, cache_dtype=cache)
     c = build_case(w, sample=256)
+    gpu_write(c)
+    oracle_write(c)
+    ids = torch.from_numpy(c.ow.renumber.astype(np.int64)).cuda()
+    np.testing.assert_array_equal(_np_cache(c.k_cache[ids]), c.o_k)
+    np.testing.assert_array_equal(_np_cache(c.v_cache[ids]), c.o_v)
     ref = oracle_decode(c)
     rows = torch.from_numpy(c.seqs).cuda()
     for P in (-1, 16):
